@@ -1,0 +1,331 @@
+"""Seeded request batches shaped like the pages' workloads.
+
+Sources of the shapes (all synthetic; no dataset is involved):
+
+* "Chunked prefill" (k4i.top), section "The core idea" (#core-idea): a 2048-token
+  prompt cut into chunks of C=512 and interleaved with decode requests under a
+  token budget T = C_prefill + N_decode.
+* "Disaggregated prefill and decode" (Perplexity), section "Prefill vs decode
+  performance": decode requests carry qo_len=1, prefill requests carry large
+  qo_len, and attention cost grows with kv_len.
+
+Five named workloads mirror the five configurations of the benchmark spec
+(tiny mixed batch, 7B-class MHA decode, chunked-prefill mixed batch, large-model
+GQA decode shard, long-prompt prefill).  Values are bf16 rounded (RNE) from fp32
+N(0,1) draws; every draw comes from a ``torch.Generator`` seeded from a
+``numpy.random.SeedSequence`` of (workload seed, sequence id, tensor kind,
+token block), so one sequence's tensors can be regenerated without drawing the
+others.
+
+Data model
+----------
+A *sequence* is one user request with a final length (tokens) and the list of
+page ids reserved for it.  A *step* is one call of the hot path: a list of
+(sequence, qo_len, kv_len) entries, where ``kv_len`` counts the tokens that
+attention reads *after* this step's append (the cached prefix plus the qo_len
+new tokens).  Before the first step of a workload, each sequence already holds
+``kv_len - qo_len`` cached tokens of its first step.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import Dict, List, Sequence, Tuple
+
+import numpy as np
+import torch
+
+# bf16 quiet-NaN bit pattern used to fill pages (and page slots) that hold no
+# token; any read of one poisons an output, and any stray write is visible in a
+# byte comparison.
+SENTINEL_BF16 = 0x7FC1
+
+# tensor kinds for seeding
+_KIND_Q, _KIND_K, _KIND_V = 0, 1, 2
+_BLOCK = 256  # tokens per independently seeded block
+
+
+@dataclass
+class Seq:
+    length: int                 # final number of tokens of the sequence
+    pages: np.ndarray           # int32 page ids reserved, ceil(length / page_size) of them
+
+
+@dataclass
+class Request:
+    seq: int                    # index into Workload.seqs
+    qo_len: int                 # new tokens appended and attended this step
+    kv_len: int                 # tokens attended after the append (cached + new)
+
+
+@dataclass
+class Step:
+    requests: List[Request]
+
+
+@dataclass
+class Workload:
+    name: str
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    num_pages: int
+    seed: int
+    seqs: List[Seq]
+    steps: List[Step]
+    causal: bool = True
+    description: str = ""
+
+    # ------------------------------------------------------------------ shapes
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def group_size(self) -> int:
+        return self.num_qo_heads // self.num_kv_heads
+
+    def pool_shape(self) -> Tuple[int, int, int, int, int]:
+        """[num_pages, 2 (K then V), num_kv_heads, page_size, head_dim]."""
+        return (self.num_pages, 2, self.num_kv_heads, self.page_size, self.head_dim)
+
+    def npages(self, kv_len: int) -> int:
+        return -(-kv_len // self.page_size)
+
+    # --------------------------------------------------------- page-table arrays
+    def _table(self, entries: Sequence[Tuple[int, int, int]]):
+        """CSR page table for (seq, n_new, kv_len) entries (int32 numpy arrays)."""
+        P = self.page_size
+        qo_indptr = [0]
+        kv_indptr = [0]
+        pages: List[np.ndarray] = []
+        last = []
+        for s, n_new, kv_len in entries:
+            qo_indptr.append(qo_indptr[-1] + n_new)
+            n = self.npages(kv_len)
+            pages.append(self.seqs[s].pages[:n])
+            kv_indptr.append(kv_indptr[-1] + n)
+            last.append(0 if kv_len == 0 else kv_len - (n - 1) * P)
+        page_indices = (np.concatenate(pages) if pages else np.zeros(0)).astype(np.int32)
+        return dict(
+            qo_indptr=np.asarray(qo_indptr, np.int32),
+            kv_indptr=np.asarray(kv_indptr, np.int32),
+            page_indices=page_indices,
+            last_page_len=np.asarray(last, np.int32),
+        )
+
+    def step_table(self, k: int):
+        """Page table of step k; ``qo_indptr`` doubles as the append indptr."""
+        return self._table([(r.seq, r.qo_len, r.kv_len) for r in self.steps[k].requests])
+
+    def initial_entries(self) -> List[Tuple[int, int]]:
+        """(seq, cached tokens) held before the first step each sequence appears in."""
+        seen = {}
+        for st in self.steps:
+            for r in st.requests:
+                if r.seq not in seen:
+                    seen[r.seq] = r.kv_len - r.qo_len
+        return sorted(seen.items())
+
+    def initial_table(self):
+        """Page table that appends every sequence's initially cached prefix."""
+        return self._table([(s, c, c) for s, c in self.initial_entries()])
+
+    # ------------------------------------------------------------------- values
+    def _block(self, seq: int, kind: int, block: int) -> torch.Tensor:
+        heads = self.num_qo_heads if kind == _KIND_Q else self.num_kv_heads
+        ss = np.random.SeedSequence([self.seed, seq, kind, block])
+        g = torch.Generator().manual_seed(int(ss.generate_state(1, np.uint64)[0]))
+        t = torch.randn(_BLOCK, heads, self.head_dim, generator=g, dtype=torch.float32)
+        t = t.to(torch.bfloat16)
+        return t
+
+    def rows(self, seq: int, kind: int, lo: int, hi: int) -> torch.Tensor:
+        """bf16 rows [lo, hi) of tensor ``kind`` of sequence ``seq``: [hi-lo, H, d]."""
+        heads = self.num_qo_heads if kind == _KIND_Q else self.num_kv_heads
+        if hi <= lo:
+            return torch.empty(0, heads, self.head_dim, dtype=torch.bfloat16)
+        b0, b1 = lo // _BLOCK, (hi - 1) // _BLOCK
+        blocks = [self._block(seq, kind, b) for b in range(b0, b1 + 1)]
+        cat = torch.cat(blocks, 0) if len(blocks) > 1 else blocks[0]
+        return cat[lo - b0 * _BLOCK: hi - b0 * _BLOCK]
+
+    def q_rows(self, seq, lo, hi):
+        return self.rows(seq, _KIND_Q, lo, hi)
+
+    def k_rows(self, seq, lo, hi):
+        return self.rows(seq, _KIND_K, lo, hi)
+
+    def v_rows(self, seq, lo, hi):
+        return self.rows(seq, _KIND_V, lo, hi)
+
+    def initial_kv(self) -> Tuple[torch.Tensor, torch.Tensor]:
+        """K and V of every sequence's initially cached prefix, concatenated."""
+        ks, vs = [], []
+        for s, c in self.initial_entries():
+            ks.append(self.k_rows(s, 0, c))
+            vs.append(self.v_rows(s, 0, c))
+        return _cat(ks, self.num_kv_heads, self.head_dim), _cat(vs, self.num_kv_heads, self.head_dim)
+
+    def step_inputs(self, k: int) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+        """(q [nnz_qo, Hq, d], k_new [nnz_qo, Hkv, d], v_new) of step k, bf16."""
+        qs, ks, vs = [], [], []
+        for r in self.steps[k].requests:
+            lo, hi = r.kv_len - r.qo_len, r.kv_len
+            qs.append(self.q_rows(r.seq, lo, hi))
+            ks.append(self.k_rows(r.seq, lo, hi))
+            vs.append(self.v_rows(r.seq, lo, hi))
+        return (_cat(qs, self.num_qo_heads, self.head_dim),
+                _cat(ks, self.num_kv_heads, self.head_dim),
+                _cat(vs, self.num_kv_heads, self.head_dim))
+
+    # ------------------------------------------------------------- accounting
+    def summary(self, k: int = 0) -> Dict:
+        reqs = self.steps[k].requests
+        pre = [r for r in reqs if r.qo_len > 1]
+        dec = [r for r in reqs if r.qo_len == 1]
+        return dict(
+            name=self.name, requests=len(reqs), prefill_requests=len(pre),
+            decode_requests=len(dec), nnz_qo=sum(r.qo_len for r in reqs),
+            kv_tokens=sum(r.kv_len for r in reqs),
+            pages_used=sum(self.npages(r.kv_len) for r in reqs),
+            num_pages=self.num_pages, Hq=self.num_qo_heads, Hkv=self.num_kv_heads,
+            head_dim=self.head_dim, page_size=self.page_size,
+        )
+
+
+def _cat(ts, heads, d):
+    ts = [t for t in ts if t.shape[0] > 0]
+    if not ts:
+        return torch.empty(0, heads, d, dtype=torch.bfloat16)
+    return torch.cat(ts, 0).contiguous()
+
+
+def chunk_schedule(L: int, C: int) -> List[Tuple[int, int]]:
+    """0-based token ranges [start, end) of the ceil(L/C) chunks of an L-token prompt.
+
+    "Chunked prefill" (k4i.top), #core-idea and #correctness: chunk s (1-based)
+    covers tokens (s-1)C+1 .. sC; in 0-based half-open form [(s-1)C, min(sC, L)).
+    """
+    return [(s * C, min((s + 1) * C, L)) for s in range(-(-L // C))]
+
+
+def _alloc_pages(gen: torch.Generator, num_pages: int, lengths: Sequence[int], P: int) -> List[np.ndarray]:
+    """Random page assignment: a permutation of the pool, consecutive entries per sequence."""
+    perm = torch.randperm(num_pages, generator=gen).numpy().astype(np.int32)
+    out, at = [], 0
+    for L in lengths:
+        n = -(-L // P)
+        if at + n > num_pages:
+            raise ValueError("page pool too small for the workload")
+        out.append(perm[at:at + n].copy())
+        at += n
+    return out
+
+
+def _pool_pages(pages_used: int) -> int:
+    """Next power of two >= twice the pages used (pool size where none is stated)."""
+    return 1 << max(0, (2 * pages_used - 1).bit_length())
+
+
+def _single_step(name, Hq, Hkv, d, P, seed, prompts, decodes, num_pages=None, description=""):
+    """prompts: list of (qo_len, kv_len); decodes: list of kv_len (qo_len = 1)."""
+    lengths = [kv for _, kv in prompts] + list(decodes)
+    used = sum(-(-L // P) for L in lengths)
+    if num_pages is None:
+        num_pages = _pool_pages(used)
+    gen = torch.Generator().manual_seed(seed + 7919)
+    pages = _alloc_pages(gen, num_pages, lengths, P)
+    seqs = [Seq(L, pg) for L, pg in zip(lengths, pages)]
+    reqs = [Request(i, qo, kv) for i, (qo, kv) in enumerate(prompts)]
+    reqs += [Request(len(prompts) + j, 1, kv) for j, kv in enumerate(decodes)]
+    return Workload(name, Hq, Hkv, d, P, num_pages, seed, seqs, [Step(reqs)], description=description)
+
+
+CONFIG_NAMES = ["tiny_mixed", "mha_decode", "chunked_prefill_mixed", "gqa_decode_shard", "long_prefill"]
+
+
+def make_workload(name: str) -> Workload:
+    """The five named workloads (seed = 1000 + 1-based config number)."""
+    if name == "tiny_mixed":
+        # 1 prompt of 64 tokens prefilled in 4 chunks of 16 + decodes at kv 40 and 73
+        # that each advance one token per step (continuous batching).
+        Hq, Hkv, d, P, num_pages, seed = 4, 2, 64, 16, 64, 1001
+        lengths = [64, 40 + 3, 73 + 3]
+        gen = torch.Generator().manual_seed(seed + 7919)
+        pages = _alloc_pages(gen, num_pages, lengths, P)
+        seqs = [Seq(L, pg) for L, pg in zip(lengths, pages)]
+        steps = []
+        for k, (c0, c1) in enumerate(chunk_schedule(64, 16)):
+            steps.append(Step([Request(0, c1 - c0, c1), Request(1, 1, 40 + k), Request(2, 1, 73 + k)]))
+        return Workload(name, Hq, Hkv, d, P, num_pages, seed, seqs, steps,
+                        description="1 prompt L=64 in 4 chunks of C=16 + 2 decodes (kv 40, 73); "
+                                    "Hq 4 / Hkv 2, d 64, P 16, 64-page pool")
+    if name == "mha_decode":
+        seed = 1002
+        g = torch.Generator().manual_seed(seed)
+        kv = torch.randint(512, 4096 + 1, (32,), generator=g).tolist()
+        return _single_step(name, 32, 32, 128, 16, seed, [], kv,
+                            description="32 decodes, kv ~ U[512,4096], Hq=Hkv=32, d 128, P 16, "
+                                        "+ append of 1 token each")
+    if name == "chunked_prefill_mixed":
+        seed = 1003
+        g = torch.Generator().manual_seed(seed)
+        kv = torch.randint(1024, 4096 + 1, (32,), generator=g).tolist()
+        return _single_step(name, 32, 8, 128, 16, seed, [(512, 2048)], kv,
+                            description="2048-token prompt at chunk [1536,2048) + 32 decodes "
+                                        "kv ~ U[1024,4096]; Hq 32 / Hkv 8, d 128, P 16")
+    if name == "gqa_decode_shard":
+        seed = 1004
+        g = torch.Generator().manual_seed(seed)
+        z = torch.randn(128, generator=g, dtype=torch.float64)
+        kv = torch.exp(math.log(8192.0) + math.log(2.0) * z).round().clamp(1024, 32768).long().tolist()
+        return _single_step(name, 12, 1, 128, 16, seed, [], kv, num_pages=300_000,
+                            description="128 decodes, kv log-normal (median 8192, sigma ln 2, "
+                                        "clip [1024,32768]); Hq 12 / Hkv 1, d 128, P 16, 300k-page pool")
+    if name == "long_prefill":
+        seed = 1005
+        g = torch.Generator().manual_seed(seed)
+        kv = torch.randint(2048, 16384 + 1, (64,), generator=g).tolist()
+        return _single_step(name, 64, 8, 128, 16, seed, [(8192, 16384)] * 4, kv,
+                            description="4 prompts of 16384 at chunk 2 of 2 (8192 new over 8192 "
+                                        "cached) + 64 decodes kv ~ U[2048,16384]; Hq 64 / Hkv 8, d 128")
+    raise KeyError(name)
+
+
+def make_prompt_workload(L: int, C: int, Hq: int, Hkv: int, d: int, P: int, seed: int,
+                         num_pages: int | None = None, decodes: Sequence[int] = ()) -> Workload:
+    """One L-token prompt prefilled in chunks of C (one step per chunk), plus
+    optional decode sequences that advance one token per step.  C >= L gives the
+    one-shot prefill of the same prompt with the same pages and values."""
+    sched = chunk_schedule(L, C)
+    nsteps = len(sched)
+    lengths = [L] + [kv + nsteps - 1 for kv in decodes]
+    used = sum(-(-x // P) for x in lengths)
+    if num_pages is None:
+        num_pages = _pool_pages(used)
+    gen = torch.Generator().manual_seed(seed + 7919)
+    pages = _alloc_pages(gen, num_pages, lengths, P)
+    seqs = [Seq(x, pg) for x, pg in zip(lengths, pages)]
+    steps = []
+    for k, (c0, c1) in enumerate(sched):
+        reqs = [Request(0, c1 - c0, c1)]
+        reqs += [Request(1 + j, 1, kv + k) for j, kv in enumerate(decodes)]
+        steps.append(Step(reqs))
+    return Workload(f"prompt_L{L}_C{C}", Hq, Hkv, d, P, num_pages, seed, seqs, steps,
+                    description=f"prompt L={L} in chunks of C={C}")
+
+
+def make_random_workload(seed: int, Hq: int, Hkv: int, d: int, P: int, reqs: Sequence[Tuple[int, int]],
+                         num_pages: int | None = None, extra_pages: int = 0) -> Workload:
+    """Single step with explicit (qo_len, kv_len) per request (edge-case tests)."""
+    lengths = [kv for _, kv in reqs]
+    used = sum(-(-x // P) for x in lengths)
+    if num_pages is None:
+        num_pages = max(1, used + extra_pages)
+    gen = torch.Generator().manual_seed(seed + 7919)
+    pages = _alloc_pages(gen, num_pages, lengths, P)
+    seqs = [Seq(x, pg) for x, pg in zip(lengths, pages)]
+    step = Step([Request(i, qo, kv) for i, (qo, kv) in enumerate(reqs)])
+    return Workload(f"random_{seed}", Hq, Hkv, d, P, num_pages, seed, seqs, [step])
