@@ -1,0 +1,468 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-attention hot path: one step = kv_append of the step's
+new tokens + batch_attention over the whole mixed batch.
+
+Default workload (N=1): the 7B-class MHA decode batch -- 32 decode requests with
+kv_len ~ U[512, 4096], 32 query / 32 kv heads, head_dim 128, page_size 16, random
+page permutation, plus the append of one token per request.  Other workloads
+(``--workload``): tiny_mixed, chunked_prefill_mixed, gqa_decode_shard,
+long_prefill.
+
+Prints ONE JSON line (rank 0).  ``value`` = algorithmic HBM bytes of the step
+(K/V pages read once per request, q, out, page ids, append read + write) per
+second of device time with inputs resident in HBM; ``e2e`` = the same bytes per
+second of a step that also copies the step's inputs from pinned host memory and
+reads the output back; ``roofline`` = the dominant kernel's algorithmic bytes
+(or FLOPs) per launch over its mean CUDA-event duration, against the measured
+peak; ``cpu_baseline`` = the CPU oracle on a bounded sample of the workload.
+
+``--impl reference`` times the CPU oracle (the only reference this method has)
+on the same workload and metric.  Multi-GPU (torchrun): independent replicas,
+one per GPU, no collective on the data path (``scaling: weak``).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "mixed-batch paged attention: decode KV GB/s, prefill TFLOP/s, % of roofline"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+
+
+# ----------------------------------------------------------------- accounting
+def step_accounting(wl, k=0):
+    """Algorithmic bytes / FLOPs of one step, split by kernel class."""
+    Hq, Hkv, d, P = wl.num_qo_heads, wl.num_kv_heads, wl.head_dim, wl.page_size
+    dec_bytes = pre_flops = pre_bytes = 0
+    nnz_new = 0
+    for r in wl.steps[k].requests:
+        nnz_new += r.qo_len
+        npages = -(-r.kv_len // P)
+        if r.qo_len == 1:
+            dec_bytes += r.kv_len * Hkv * d * 2 * 2 + 2 * Hq * d * 2 + npages * 4
+        elif r.qo_len > 1:
+            cached = r.kv_len - r.qo_len
+            pairs = r.qo_len * cached + r.qo_len * (r.qo_len + 1) // 2 if wl.causal else r.qo_len * r.kv_len
+            pre_flops += 4 * d * Hq * pairs
+            pre_bytes += r.kv_len * Hkv * d * 2 * 2 + 2 * r.qo_len * Hq * d * 2 + npages * 4
+    app_bytes = nnz_new * Hkv * d * 2 * 2 * 2
+    return dict(decode_bytes=dec_bytes, append_bytes=app_bytes, prefill_flops=pre_flops,
+                prefill_bytes=pre_bytes, nnz_new=nnz_new)
+
+
+def kernel_source_hash(name):
+    src = os.path.join(ROOT, "decode_attention_append_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for f in (src, os.path.join(ROOT, "decode_attention_append_gb300", "csrc", "ptx.cuh")):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload, kernel_file):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since it was captured."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            tab = json.load(f)
+        ent = tab.get(workload)
+        if ent and ent.get("source_hash") == kernel_source_hash(kernel_file):
+            return ent.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------- GPU setup
+class GpuStep:
+    """Device-resident workload: pool with the cached prefixes, page table,
+    the step's q / k_new / v_new, outputs and workspace."""
+
+    def __init__(self, wl, device, k=0):
+        import decode_attention_append_gb300 as daa
+        self.daa = daa
+        self.wl, self.dev = wl, device
+        self.pool = torch.full(wl.pool_shape(), 0x7FC1, dtype=torch.int16, device=device).view(torch.bfloat16)
+        it = wl.initial_table()
+        k0, v0 = wl.initial_kv()
+        if k0.shape[0]:
+            t0 = daa.PageTable.from_host(it["qo_indptr"], it["kv_indptr"], it["page_indices"],
+                                         it["last_page_len"], device)
+            daa.kv_append(k0.to(device), v0.to(device), self.pool, t0.qo_indptr, t0.page_indices,
+                          t0.kv_indptr, t0.last_page_len)
+        del k0, v0
+        st = wl.step_table(k)
+        self.host_table = st
+        self.table = daa.PageTable.from_host(st["qo_indptr"], st["kv_indptr"], st["page_indices"],
+                                             st["last_page_len"], device)
+        q, kn, vn = wl.step_inputs(k)
+        self.h_q, self.h_k, self.h_v = (x.pin_memory() for x in (q, kn, vn))
+        self.q, self.k_new, self.v_new = (x.to(device) for x in (q, kn, vn))
+        self.runner = daa.BatchAttention(self.table, wl.num_qo_heads, self.pool, causal=wl.causal,
+                                         sm_scale=wl.sm_scale)
+        self.out = torch.empty_like(self.q)
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        # pinned host copies of the int32 page table (re-sent every e2e step)
+        self.h_ints = [torch.from_numpy(st[n]).pin_memory() for n in
+                       ("qo_indptr", "kv_indptr", "page_indices", "last_page_len")]
+        self.d_ints = [torch.empty_like(x, device=device) for x in self.h_ints]
+        torch.cuda.synchronize()
+
+    def step(self):
+        self.runner.append(self.k_new, self.v_new)
+        self.runner.run(self.q, out=self.out)
+
+    def step_e2e(self, stream):
+        """Public API call with host buffers: H2D inputs, append + attention, D2H out."""
+        for d, h in zip(self.d_ints, self.h_ints):
+            d.copy_(h, non_blocking=True)
+        self.q.copy_(self.h_q, non_blocking=True)
+        self.k_new.copy_(self.h_k, non_blocking=True)
+        self.v_new.copy_(self.h_v, non_blocking=True)
+        qo, kv, pi, ll = self.d_ints
+        self.daa.kv_append(self.k_new, self.v_new, self.pool, qo, pi, kv, ll)
+        self.daa.batch_attention(self.q, self.pool, qo, kv, pi, ll, self.wl.causal, self.wl.sm_scale,
+                                 out=self.out, workspace=self.runner.workspace,
+                                 host_indptr=(self.host_table["qo_indptr"], self.host_table["kv_indptr"],
+                                              self.host_table["last_page_len"]))
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def e2e_bytes(self):
+        h2d = sum(x.numel() * x.element_size() for x in self.h_ints)
+        h2d += sum(x.numel() * x.element_size() for x in (self.h_q, self.h_k, self.h_v))
+        d2h = self.h_out.numel() * self.h_out.element_size()
+        return h2d, d2h
+
+
+def timed(fn, steps, flush=None):
+    """Sum of per-step CUDA-event times (ms) on the current stream."""
+    s = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush()
+        evs[i][0].record(s)
+        fn()
+        evs[i][1].record(s)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs)
+
+
+# --------------------------------------------------------------- CPU oracle
+class OracleSample:
+    """The CPU oracle on a bounded sample of step 0: whole requests (decodes
+    first, then prefill requests) until the estimated fp64 work reaches the
+    budget.  Inputs are generated once; each run() appends the step's new
+    tokens and attends, and is timed."""
+
+    def __init__(self, wl, budget_s=12.0):
+        import copy
+
+        import oracle
+        from synth import SENTINEL_BF16, Request, Step
+        self.oracle = oracle
+        reqs = wl.steps[0].requests
+        P = wl.page_size
+        threads = max(1, oracle.num_threads())
+        order = ([i for i, r in enumerate(reqs) if r.qo_len == 1] +
+                 [i for i, r in enumerate(reqs) if r.qo_len > 1])
+        picked, est = [], 0.0
+        for i in order:
+            r = reqs[i]
+            # ~0.5 GFLOP/s per thread for the fp64 loops (4 d flops per pair and head)
+            cost = r.kv_len * max(1, r.qo_len) * wl.num_qo_heads * wl.head_dim * 4 / 0.5e9 / threads
+            if picked and est + cost > budget_s:
+                break
+            picked.append(i)
+            est += cost
+        sw = copy.copy(wl)
+        seqs, sreqs, nxt, orig = [], [], 0, []
+        for j, i in enumerate(picked):
+            r = reqs[i]
+            n = -(-r.kv_len // P)
+            seqs.append(type(wl.seqs[r.seq])(wl.seqs[r.seq].length, np.arange(nxt, nxt + n, dtype=np.int32)))
+            nxt += n
+            sreqs.append(Request(j, r.qo_len, r.kv_len))
+            orig.append(r.seq)
+        sw.seqs, sw.steps, sw.num_pages = seqs, [Step(sreqs)], max(1, nxt)
+        # the sampled sequences keep their original values
+        sw._block = lambda seq, kind, block, _w=wl, _o=orig: _w._block(_o[seq], kind, block)
+        self.sw = sw
+        self.pool = oracle.new_pool(sw.pool_shape(), SENTINEL_BF16)
+        it = sw.initial_table()
+        k0, v0 = sw.initial_kv()
+        oracle.kv_append(self.pool, k0, v0, it["qo_indptr"], it["page_indices"], it["kv_indptr"],
+                         it["last_page_len"])
+        self.table = sw.step_table(0)
+        self.q, self.kn, self.vn = sw.step_inputs(0)
+        acc = step_accounting(sw)
+        self.nbytes = acc["decode_bytes"] + acc["append_bytes"] + acc["prefill_bytes"]
+        self.sample = (f"{len(picked)} of {len(reqs)} requests of step 0 (whole requests, decodes "
+                       f"first); fp64 oracle on {threads} host threads")
+        self.cores = threads
+
+    def run(self):
+        o, st = self.oracle, self.table
+        t0 = time.perf_counter()
+        o.kv_append(self.pool, self.kn, self.vn, st["qo_indptr"], st["page_indices"], st["kv_indptr"],
+                    st["last_page_len"])
+        o.attention(self.q, self.pool, st["qo_indptr"], st["kv_indptr"], st["page_indices"],
+                    st["last_page_len"], self.sw.causal, self.sw.sm_scale, self.sw.num_qo_heads)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, budget_s=12.0, reps=None):
+    s = OracleSample(wl, budget_s)
+    dt = s.run()
+    reps = reps or max(1, min(20, int(budget_s / max(dt, 1e-3))))
+    times = [dt] + [s.run() for _ in range(reps - 1)]
+    t = float(np.median(times))
+    return dict(value=s.nbytes / t / 1e9, unit="GB/s", cores=s.cores, kind="oracle",
+                sample=s.sample + f", median of {len(times)} runs of {t:.3f} s")
+
+
+# ---------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="mha_decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from synth import make_workload
+    wl = make_workload(args.workload)
+    acc = step_accounting(wl)
+    algo_bytes = acc["decode_bytes"] + acc["append_bytes"] + acc["prefill_bytes"]
+    summary = wl.summary()
+    config = {"workload": args.workload, "description": wl.description,
+              "requests": summary["requests"], "decode_requests": summary["decode_requests"],
+              "prefill_requests": summary["prefill_requests"], "kv_tokens": summary["kv_tokens"],
+              "Hq": wl.num_qo_heads, "Hkv": wl.num_kv_heads, "head_dim": wl.head_dim,
+              "page_size": wl.page_size, "num_pages": wl.num_pages,
+              "parallelism": f"replicas{args.gpus}"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        sample = OracleSample(wl, budget_s=6.0)
+        for _ in range(args.warmup):
+            sample.run()
+        secs = [sample.run() for _ in range(args.steps)]
+        v = sample.nbytes * len(secs) / sum(secs) / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(secs) / len(secs),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": v, "unit": "GB/s", "cores": sample.cores, "kind": "oracle",
+                                 "sample": sample.sample},
+                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if dist is not None:
+        dist.barrier()
+        if rank != 0:
+            __graft_entry__.build()
+    import decode_attention_append_gb300 as daa
+
+    g = GpuStep(wl, dev)
+    flush_buf = None
+    need_flush = algo_bytes < 2 * L2_BYTES
+    if need_flush:
+        flush_buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = (lambda: flush_buf.fill_(1.0)) if need_flush else None
+    config["l2"] = ("flushed between steps (256 MB write)" if need_flush
+                    else f"inputs larger than L2 ({algo_bytes / 1e9:.2f} GB per step)")
+
+    for _ in range(max(3, args.warmup)):
+        g.step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- main timed region: device-resident inputs
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    ms = timed(g.step, args.steps, flush)
+    barrier()
+    # ---- per-kernel roofline pass: CUDA events around each launch
+    daa.trace_enable(8 * args.steps + 64)
+    ms_traced = timed(g.step, args.steps, flush)
+    recs = daa.trace_read()
+    daa.trace_disable()
+    barrier()
+    clk = clocks.stop()
+
+    # ---- e2e: host buffers through the public API
+    for _ in range(2):
+        g.step_e2e(torch.cuda.current_stream())
+    barrier()
+    ms_e2e = timed(lambda: g.step_e2e(torch.cuda.current_stream()), args.steps, flush)
+    barrier()
+    h2d, d2h = g.e2e_bytes()
+    err = daa.device_error(reset=True)
+
+    t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms, ms_e2e = float(t[0]), float(t[1])
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    per_kernel = {}
+    for name, kms in recs:
+        per_kernel.setdefault(name, []).append(kms)
+    launches = len(recs) / max(1, args.steps)
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    # dominant kernel: largest share of traced time
+    tot = {k: sum(v) for k, v in per_kernel.items()}
+    dom = max(tot, key=tot.get) if tot else None
+    roof = None
+    if dom is not None:
+        mean_ms = float(np.mean(per_kernel[dom]))
+        n_launch = len(per_kernel[dom]) / args.steps
+        if dom == "prefill_tc":
+            achieved = acc["prefill_flops"] / n_launch / (mean_ms * 1e-3) / 1e12
+            roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                    "frac": achieved / bf16, "kernel": dom, "mean_ms": mean_ms,
+                    "peak_source": f"{peak_src} bf16 dense (burst)"}
+            kfile = "prefill.cu"
+        else:
+            kb = {"decode_splitkv": acc["decode_bytes"], "kv_append": acc["append_bytes"]}.get(dom, 0)
+            achieved = kb / n_launch / (mean_ms * 1e-3) / 1e9
+            roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                    "frac": achieved / hbm, "kernel": dom, "mean_ms": mean_ms,
+                    "peak_source": f"{peak_src} HBM copy"}
+            kfile = {"decode_splitkv": "decode.cu", "kv_append": "append.cu"}.get(dom, "decode.cu")
+        roof["traffic"] = measured_traffic(args.workload, kfile)
+        roof["share"] = {k: round(v / sum(tot.values()), 4) for k, v in tot.items()}
+
+    value = algo_bytes * args.steps * world / (ms * 1e-3) / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config,
+            "e2e": {"value": algo_bytes * args.steps * world / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": ms_e2e / args.steps},
+            "gpu_launches": int(round(launches * args.steps)),
+            "roofline": roof,
+            "algorithmic": {"bytes_per_step": algo_bytes, "decode_bytes": acc["decode_bytes"],
+                            "append_bytes": acc["append_bytes"], "prefill_flops": acc["prefill_flops"]},
+            "clocks": clk, "device_error": err}
+    if acc["prefill_flops"] and "prefill_tc" in per_kernel:
+        pm = float(np.mean(per_kernel["prefill_tc"]))
+        line["prefill_tflops"] = acc["prefill_flops"] / (pm * 1e-3) / 1e12
+    if "decode_splitkv" in per_kernel and acc["decode_bytes"]:
+        dm = float(np.mean(per_kernel["decode_splitkv"]))
+        line["decode_gbs"] = acc["decode_bytes"] / (dm * 1e-3) / 1e9
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,276 @@
+"""GB300 (sm_103a) paged KV append + mixed-batch paged attention.
+
+A thin ctypes binding over the C ABI of ``libdaa.so`` (declared in
+``include/daa.h``).  It only marshals torch tensors into pointers and sizes:
+every step of the computation runs in the library's CUDA kernels.  There is no
+CPU or PyTorch fallback; if the library is missing the calls raise.
+
+Entry points (same names as the C ABI, without the ``daa_`` prefix):
+
+* ``kv_append(k_new, v_new, kv_pages, append_indptr, page_indices, kv_indptr,
+  last_page_len)`` -- write each new token's K/V into its page slot.
+* ``batch_attention(q, kv_pages, qo_indptr, kv_indptr, page_indices,
+  last_page_len, causal, sm_scale, ...)`` -- attention for a batch mixing
+  chunked-prefill requests (qo_len > 1, causal with the cache offset) and decode
+  requests (qo_len = 1).
+* ``BatchAttention`` -- plans once from host copies of the page table and owns
+  the workspace, for repeated calls over the same batch shape.
+
+Tensors: bf16 ``q [nnz_qo, Hq, d]``, ``k_new/v_new [nnz_new, Hkv, d]``, page
+pool ``kv_pages [num_pages, 2, Hkv, page_size, d]`` (K then V, HND inside a
+page), int32 CSR arrays on the same CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libdaa.so")
+_lib = None
+_lock = threading.Lock()
+
+DAA_OK = 0
+STATUS = {0: "ok", -1: "invalid argument", -2: "shape", -3: "page range", -4: "unsupported",
+          -5: "CUDA error", -6: "workspace", -7: "alignment"}
+KERNEL_NAMES = {1: "kv_append", 2: "decode_splitkv", 3: "softmax_merge", 4: "prefill_tc"}
+
+
+class DaaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status})")
+        self.status = status
+
+
+class _Dims(ctypes.Structure):
+    _fields_ = [("num_qo_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_pages", ctypes.c_int64)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libdaa.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(f"libdaa.so not built at {_LIB_PATH}; run decode_attention_append_gb300.build.build()")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        lib.daa_status_string.restype = ctypes.c_char_p
+        lib.daa_status_string.argtypes = [i32]
+        lib.daa_version.restype = i32
+        lib.daa_kv_append.restype = i32
+        lib.daa_kv_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, _Dims, vp]
+        lib.daa_batch_attention_workspace_size.restype = sz
+        lib.daa_batch_attention_workspace_size.argtypes = [vp, vp, vp, i32, _Dims, ctypes.POINTER(i32)]
+        lib.daa_batch_attention.restype = i32
+        lib.daa_batch_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, vp, vp,
+                                            vp, sz, _Dims, vp]
+        lib.daa_device_error.restype = i32
+        lib.daa_device_error.argtypes = [ctypes.POINTER(i32), i32]
+        lib.daa_trace_enable.restype = i32
+        lib.daa_trace_enable.argtypes = [i32]
+        lib.daa_trace_disable.restype = i32
+        lib.daa_trace_read.restype = i32
+        lib.daa_trace_read.argtypes = [ctypes.POINTER(i32), ctypes.POINTER(f32), i32]
+        _lib = lib
+        return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        return ctypes.c_void_p(t.data_ptr())
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data_as(ctypes.c_void_p)
+    raise TypeError(type(t))
+
+
+def _host_i32(a) -> np.ndarray:
+    if isinstance(a, torch.Tensor):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _dev_i32(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.int32 and t.is_contiguous()):
+        raise TypeError(f"{name} must be a contiguous int32 CUDA tensor")
+    return t
+
+
+def _dev_bf16(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+        raise TypeError(f"{name} must be a contiguous bf16 CUDA tensor")
+    return t
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dims(kv_pages: torch.Tensor, num_qo_heads: int) -> _Dims:
+    if kv_pages.dim() != 5 or kv_pages.shape[1] != 2:
+        raise ValueError("kv_pages must be [num_pages, 2, Hkv, page_size, head_dim]")
+    n, _, hkv, p, d = kv_pages.shape
+    return _Dims(num_qo_heads, hkv, d, p, n)
+
+
+def _check(st: int, what: str):
+    if st != DAA_OK:
+        raise DaaError(st, what)
+
+
+def kv_append(k_new, v_new, kv_pages, append_indptr, page_indices, kv_indptr, last_page_len,
+              stream=None) -> None:
+    """Append new tokens' K/V into their pages (asynchronous on ``stream``)."""
+    lib = load_library()
+    _dev_bf16(k_new, "k_new"), _dev_bf16(v_new, "v_new"), _dev_bf16(kv_pages, "kv_pages")
+    for n, t in (("append_indptr", append_indptr), ("page_indices", page_indices),
+                 ("kv_indptr", kv_indptr), ("last_page_len", last_page_len)):
+        _dev_i32(t, n)
+    dims = _dims(kv_pages, kv_pages.shape[2])
+    batch = append_indptr.numel() - 1
+    _check(lib.daa_kv_append(_ptr(k_new), _ptr(v_new), _ptr(kv_pages), _ptr(append_indptr),
+                             _ptr(page_indices), _ptr(kv_indptr), _ptr(last_page_len), batch,
+                             k_new.shape[0], dims, _stream(stream)), "kv_append")
+
+
+def batch_attention_workspace_size(h_qo_indptr, h_kv_indptr, h_last_page_len, num_qo_heads,
+                                   num_kv_heads, head_dim, page_size, num_pages) -> int:
+    lib = load_library()
+    qo, kv, ll = _host_i32(h_qo_indptr), _host_i32(h_kv_indptr), _host_i32(h_last_page_len)
+    st = ctypes.c_int32(0)
+    n = lib.daa_batch_attention_workspace_size(_ptr(qo), _ptr(kv), _ptr(ll), len(qo) - 1,
+                                               _Dims(num_qo_heads, num_kv_heads, head_dim,
+                                                     page_size, num_pages), ctypes.byref(st))
+    _check(st.value, "batch_attention_workspace_size")
+    return int(n)
+
+
+def batch_attention(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len, causal=True,
+                    sm_scale=None, out=None, lse=None, workspace=None, host_indptr=None,
+                    stream=None):
+    """Mixed-batch paged attention.  Returns ``out`` (and fills ``lse`` if given).
+
+    ``host_indptr`` = (h_qo_indptr, h_kv_indptr, h_last_page_len) host copies of
+    the page table used for planning; when omitted they are copied from the
+    device (a synchronisation).  ``workspace`` (uint8 CUDA tensor) is allocated
+    by torch here when omitted; the library itself never allocates.
+    """
+    lib = load_library()
+    _dev_bf16(q, "q"), _dev_bf16(kv_pages, "kv_pages")
+    for n, t in (("qo_indptr", qo_indptr), ("kv_indptr", kv_indptr), ("page_indices", page_indices),
+                 ("last_page_len", last_page_len)):
+        _dev_i32(t, n)
+    Hq, d = q.shape[1], q.shape[2]
+    dims = _dims(kv_pages, Hq)
+    if sm_scale is None:
+        sm_scale = 1.0 / float(d) ** 0.5
+    if host_indptr is None:
+        host_indptr = (qo_indptr, kv_indptr, last_page_len)
+    hq, hk, hl = (_host_i32(x) for x in host_indptr)
+    batch = len(hq) - 1
+    if out is None:
+        out = torch.empty_like(q)
+    _dev_bf16(out, "out")
+    if lse is not None and not (lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous()):
+        raise TypeError("lse must be a contiguous fp32 CUDA tensor")
+    st = ctypes.c_int32(0)
+    need = lib.daa_batch_attention_workspace_size(_ptr(hq), _ptr(hk), _ptr(hl), batch, dims,
+                                                  ctypes.byref(st))
+    _check(st.value, "batch_attention")
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.daa_batch_attention(_ptr(q), _ptr(kv_pages), _ptr(qo_indptr), _ptr(kv_indptr),
+                                   _ptr(page_indices), _ptr(last_page_len), _ptr(hq), _ptr(hk),
+                                   _ptr(hl), batch, int(bool(causal)), float(sm_scale), _ptr(out),
+                                   _ptr(lse), _ptr(workspace), ws_bytes, dims, _stream(stream)),
+           "batch_attention")
+    return out
+
+
+@dataclass
+class PageTable:
+    """Device int32 CSR page table plus its host mirror (numpy)."""
+    qo_indptr: torch.Tensor
+    kv_indptr: torch.Tensor
+    page_indices: torch.Tensor
+    last_page_len: torch.Tensor
+    h_qo_indptr: np.ndarray
+    h_kv_indptr: np.ndarray
+    h_last_page_len: np.ndarray
+
+    @classmethod
+    def from_host(cls, qo_indptr, kv_indptr, page_indices, last_page_len, device="cuda"):
+        hq, hk, hp, hl = (_host_i32(x) for x in (qo_indptr, kv_indptr, page_indices, last_page_len))
+        dev = lambda a: torch.from_numpy(a).to(device)  # noqa: E731
+        return cls(dev(hq), dev(hk), dev(hp), dev(hl), hq, hk, hl)
+
+
+class BatchAttention:
+    """Plan-once / run-many wrapper for one batch shape (FlashInfer-style)."""
+
+    def __init__(self, table: PageTable, num_qo_heads: int, kv_pages: torch.Tensor, causal=True,
+                 sm_scale=None):
+        self.t = table
+        self.kv_pages = kv_pages
+        self.causal = causal
+        self.Hq = num_qo_heads
+        self.sm_scale = sm_scale if sm_scale is not None else 1.0 / float(kv_pages.shape[4]) ** 0.5
+        n, _, hkv, p, d = kv_pages.shape
+        need = batch_attention_workspace_size(table.h_qo_indptr, table.h_kv_indptr,
+                                              table.h_last_page_len, num_qo_heads, hkv, d, p, n)
+        self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=kv_pages.device)
+
+    def append(self, k_new, v_new, stream=None):
+        t = self.t
+        kv_append(k_new, v_new, self.kv_pages, t.qo_indptr, t.page_indices, t.kv_indptr,
+                  t.last_page_len, stream=stream)
+
+    def run(self, q, out=None, lse=None, stream=None):
+        t = self.t
+        return batch_attention(q, self.kv_pages, t.qo_indptr, t.kv_indptr, t.page_indices,
+                               t.last_page_len, self.causal, self.sm_scale, out=out, lse=lse,
+                               workspace=self.workspace,
+                               host_indptr=(t.h_qo_indptr, t.h_kv_indptr, t.h_last_page_len),
+                               stream=stream)
+
+
+def device_error(reset: bool = True) -> int:
+    """The library's device error word (0 = none); synchronises the device."""
+    lib = load_library()
+    code = ctypes.c_int32(0)
+    _check(lib.daa_device_error(ctypes.byref(code), int(reset)), "device_error")
+    return int(code.value)
+
+
+def trace_enable(capacity: int = 4096) -> None:
+    _check(load_library().daa_trace_enable(capacity), "trace_enable")
+
+
+def trace_disable() -> None:
+    _check(load_library().daa_trace_disable(), "trace_disable")
+
+
+def trace_read(max_records: int = 65536):
+    """[(kernel name, milliseconds)] of the launches recorded since the last read."""
+    lib = load_library()
+    ids = (ctypes.c_int32 * max_records)()
+    ms = (ctypes.c_float * max_records)()
+    n = lib.daa_trace_read(ids, ms, max_records)
+    return [(KERNEL_NAMES.get(ids[i], str(ids[i])), float(ms[i])) for i in range(n)]

@@ -1,0 +1,130 @@
+// KV append: scatter each new token's K and V rows into its page slot.
+//
+// "Chunked prefill" (k4i.top), #correctness: after a chunk the new k, v
+// vectors are appended to the KV cache (K_cache += [k_{(s-1)C+1} .. k_{sC}]);
+// #io-overhead: the append moves C x 2 x Hkv x d x 2 bytes per layer.
+// "Disaggregated prefill and decode" (Perplexity), "Sharded KV cache
+// transfers": HND pages, so head h of token slot s is one contiguous d-row.
+//
+// Bandwidth design: a CTA copies R whole token rows (R chosen so each thread
+// moves ~8-16 16-byte chunks); the owner request of each row is found once per
+// row (binary search over append_indptr) into shared memory, then all threads
+// stream 16-byte chunks with read-only loads.  Source rows are contiguous
+// ([Hkv][d] per token); each destination (head, slot) row is 2*d contiguous
+// bytes, so every warp writes whole 128-byte lines.
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace daa {
+
+namespace {
+
+constexpr int kAppendThreads = 128;
+constexpr int kAppendMaxRows = 64;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAppendThreads)
+kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                 uint4* __restrict__ pool, const int32_t* __restrict__ append_indptr,
+                 const int32_t* __restrict__ page_indices, const int32_t* __restrict__ kv_indptr,
+                 const int32_t* __restrict__ last_page_len, int batch, int nnz_new, int Hkv,
+                 int rows_per_cta, int64_t num_pages, int* err) {
+  constexpr int P = 16;
+  constexpr int CH = D / 8;  // 16-byte chunks per (head, slot) row
+  __shared__ int64_t s_dst[kAppendMaxRows];  // chunk index of (page, K, head 0, slot, 0); -1 = skip
+
+  const int row0 = blockIdx.x * rows_per_cta;
+  const int nrows = min(rows_per_cta, nnz_new - row0);
+  if (threadIdx.x < nrows) {
+    const int row = row0 + threadIdx.x;
+    int lo = 0, hi = batch - 1;  // largest r with append_indptr[r] <= row
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(append_indptr + mid) <= row) lo = mid; else hi = mid - 1;
+    }
+    const int r = lo;
+    const int a0 = __ldg(append_indptr + r), a1 = __ldg(append_indptr + r + 1);
+    const int p0 = __ldg(kv_indptr + r), np = __ldg(kv_indptr + r + 1) - p0;
+    const int last = np > 0 ? __ldg(last_page_len + r) : 0;
+    const int64_t kv_len = np > 0 ? (int64_t)(np - 1) * P + last : 0;
+    const int n_new = a1 - a0;
+    int64_t dst = -1;
+    if (row < a0 || row >= a1 || n_new > kv_len || (np > 0 && (last < 1 || last > P))) {
+      set_device_error(err, kDevErrShape);
+    } else {
+      const int64_t pos = kv_len - n_new + (row - a0);
+      const int64_t page = __ldg(page_indices + p0 + pos / P);
+      if (page < 0 || page >= num_pages) {
+        set_device_error(err, kDevErrPageRange);
+      } else {
+        dst = ((page * 2) * Hkv * P + (pos % P)) * CH;
+      }
+    }
+    s_dst[threadIdx.x] = dst;
+  }
+  __syncthreads();
+
+  // flat chunk index i over (row, kv, head, c), c fastest
+  const int per_row = 2 * Hkv * CH;
+  const int total = nrows * per_row;
+  constexpr int U = 4;
+  for (int base = threadIdx.x; base < total; base += kAppendThreads * U) {
+    uint4 val[U];
+    int64_t dst[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * kAppendThreads;
+      dst[u] = -1;
+      if (i < total) {
+        const int rr = i / per_row;
+        const int rem = i - rr * per_row;
+        const int kv = rem / (Hkv * CH);
+        const int hc = rem - kv * (Hkv * CH);  // h * CH + c
+        const int h = hc / CH, c = hc - h * CH;
+        const int64_t d0 = s_dst[rr];
+        if (d0 >= 0) {
+          const uint4* src = (kv == 0 ? k_new : v_new) + (int64_t)(row0 + rr) * Hkv * CH + hc;
+          val[u] = ld_stream(src);
+          dst[u] = d0 + ((int64_t)kv * Hkv + h) * P * CH + c;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (dst[u] >= 0) pool[dst[u]] = val[u];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* pool,
+                             const int32_t* append_indptr, const int32_t* page_indices,
+                             const int32_t* kv_indptr, const int32_t* last_page_len, int batch,
+                             int nnz_new, int Hkv, int head_dim, int64_t num_pages, int* err,
+                             cudaStream_t stream) {
+  if (nnz_new <= 0 || batch <= 0) return cudaSuccess;
+  const int per_row_chunks = 2 * Hkv * (head_dim / 8);
+  int rows = (kAppendThreads * 16) / per_row_chunks;
+  rows = rows < 1 ? 1 : (rows > kAppendMaxRows ? kAppendMaxRows : rows);
+  const int grid = (nnz_new + rows - 1) / rows;
+  if (head_dim == 128) {
+    kv_append_kernel<128><<<grid, kAppendThreads, 0, stream>>>(
+        (const uint4*)k_new, (const uint4*)v_new, (uint4*)pool, append_indptr, page_indices,
+        kv_indptr, last_page_len, batch, nnz_new, Hkv, rows, num_pages, err);
+  } else {
+    kv_append_kernel<64><<<grid, kAppendThreads, 0, stream>>>(
+        (const uint4*)k_new, (const uint4*)v_new, (uint4*)pool, append_indptr, page_indices,
+        kv_indptr, last_page_len, batch, nnz_new, Hkv, rows, num_pages, err);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace daa

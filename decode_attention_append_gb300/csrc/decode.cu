@@ -1,0 +1,355 @@
+// Split-KV decode attention (qo_len == 1) over HND pages, on CUDA cores.
+//
+// "Disaggregated prefill and decode" (Perplexity), "Prefill vs decode
+// performance": decode attention is memory bound and can be split over
+// requests and over kv_len.  "Chunked prefill" (k4i.top), #correctness: the
+// partial attentions over disjoint key ranges are combined by softmax_merge
+// (the merge kernel), so each CTA handles one page-aligned key range (a split)
+// of one request for one kv head.
+//
+// CTA organisation (G = query heads per kv head):
+//   - a "page group" of NWH warps shares one ring of NSTAGE shared-memory
+//     stages; each stage holds one page's K slice and V slice for this kv head
+//     (2 x page_size x d bf16, contiguous in HND), filled by two 1-D TMA bulk
+//     copies issued by one lane and tracked by an mbarrier;
+//   - the NWH warps of a group split the G query heads (4 per warp), so one
+//     page read from HBM serves every query head of its group (GQA packing);
+//   - NPG page groups per CTA take pages round-robin and keep separate
+//     online-softmax states, merged in shared memory at the end.
+// Inside a warp, 16 lanes cover one token's d-vector (8 dims each for d=128)
+// and the two half-warps take alternate tokens.  q.k partial sums are reduced
+// across the 16 lanes with a reduce-scatter of warp shuffles (each level halves
+// the values a lane holds), so a page of 16 tokens x 4 heads costs 30
+// shuffles per lane instead of 128.  Scores live in the log2 domain (q is
+// pre-scaled by sm_scale * log2 e).
+#include <cfloat>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace daa {
+namespace {
+
+constexpr int kP = 16;
+
+template <int D, int G>
+struct DecodeShape {
+  static constexpr int HPW = G >= 4 ? 4 : G;          // query heads per warp
+  static constexpr int NWH = (G + HPW - 1) / HPW;     // warps sharing a page
+  static constexpr int NPG = NWH >= 4 ? 1 : 4 / NWH;  // page groups per CTA
+  static constexpr int NWARPS = NWH * NPG;
+  static constexpr int THREADS = 32 * NWARPS;
+  static constexpr int DPL = D / 16;                  // dims per lane
+  static constexpr int ITERS = kP / 2;                // two tokens per warp step
+  static constexpr int SLICE = kP * D * 2;            // bytes of one head's K (or V) page slice
+  static constexpr int STAGE = 2 * SLICE;
+  static constexpr int NSTAGE = NPG >= 4 ? 3 : (NPG == 2 ? 4 : 6);
+  static constexpr int RING = NPG * NSTAGE * STAGE;
+  static constexpr int NRED = ITERS * HPW;            // partial dots per lane per page
+  static constexpr int NF = NRED >= 16 ? NRED / 16 : 1;
+  static constexpr int SH = NRED >= 16 ? 0 : 1;       // NRED == 8 when HPW == 1
+  static_assert(NRED >= 8, "reduce-scatter layout");
+  static constexpr int MERGE_BYTES = NPG * G * (D + 2) * 4;
+  static constexpr int BODY = RING > MERGE_BYTES ? RING : MERGE_BYTES;
+  static constexpr int BARS = 2 * NPG * NSTAGE * 8;
+  static constexpr int SCORES = NWARPS * kP * HPW * 4;
+  static constexpr int ALPHA = NWARPS * HPW * 4;
+  static constexpr int SMEM = BODY + BARS + SCORES + ALPHA;
+};
+
+// Reduce-scatter over the 16 lanes of a half-warp: on entry every lane holds N
+// partial sums; on exit lane li holds the full sums of entries
+// [(li >> SH) * NF, (li >> SH) * NF + NF) in v[0 .. NF).
+template <int N, int M>
+__device__ __forceinline__ void reduce_scatter16(float* v, int li) {
+  if constexpr (M > 0) {
+    if constexpr (N >= 2) {
+      constexpr int H = N / 2;
+      const bool upper = (li & M) != 0;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float a = v[i], b = v[H + i];
+        const float send = upper ? a : b;
+        const float keep = upper ? b : a;
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, M);
+      }
+      reduce_scatter16<H, M / 2>(v, li);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], M);
+      reduce_scatter16<1, M / 2>(v, li);
+    }
+  }
+}
+
+template <int DPL>
+__device__ __forceinline__ void load_row_f32(const uint8_t* p, float (&f)[DPL]) {
+  if constexpr (DPL == 8) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    f[0] = bf16lo_to_f32(w.x); f[1] = bf16hi_to_f32(w.x);
+    f[2] = bf16lo_to_f32(w.y); f[3] = bf16hi_to_f32(w.y);
+    f[4] = bf16lo_to_f32(w.z); f[5] = bf16hi_to_f32(w.z);
+    f[6] = bf16lo_to_f32(w.w); f[7] = bf16hi_to_f32(w.w);
+  } else {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    f[0] = bf16lo_to_f32(w.x); f[1] = bf16hi_to_f32(w.x);
+    f[2] = bf16lo_to_f32(w.y); f[3] = bf16hi_to_f32(w.y);
+  }
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
+  return static_cast<uint16_t>(pack_bf16x2(x, 0.f) & 0xFFFFu);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(DecodeShape<D, G>::THREADS)
+decode_splitkv_kernel(const DecodeArgs a) {
+  using S = DecodeShape<D, G>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::BODY);
+  uint64_t* empty = full + S::NPG * S::NSTAGE;
+  float* s_scores = reinterpret_cast<float*>(empty + S::NPG * S::NSTAGE);
+  float* s_alpha = s_scores + S::NWARPS * kP * S::HPW;
+
+  const DecodeUnit u = a.units[blockIdx.x];
+  const int kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = warp / S::NWH;
+  const int wh = warp - grp * S::NWH;
+  const int hb = wh * S::HPW;  // first head (within the group of G) of this warp
+  const int half = lane >> 4, li = lane & 15;
+
+  const int pg_lo = u.tok_begin / kP;
+  const int pg_hi = (u.tok_end + kP - 1) / kP;
+  const int npg_unit = pg_hi - pg_lo;
+  const int my_n = npg_unit > grp ? (npg_unit - grp + S::NPG - 1) / S::NPG : 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S::NPG * S::NSTAGE; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], S::NWH);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  uint64_t* gfull = full + grp * S::NSTAGE;
+  uint64_t* gempty = empty + grp * S::NSTAGE;
+  uint8_t* gring = ring + grp * S::NSTAGE * S::STAGE;
+  const bool producer = (wh == 0 && lane == 0);
+
+  auto issue = [&](int k) {
+    const int stage = k % S::NSTAGE;
+    const int pg = pg_lo + grp + k * S::NPG;
+    const int64_t page = a.page_indices[u.page_base + pg];
+    if (page < 0 || page >= a.num_pages) {
+      set_device_error(a.err, kDevErrPageRange);
+      mbar_arrive(&gfull[stage]);  // completes the phase with no bytes; data is stale
+      return;
+    }
+    uint8_t* dst = gring + stage * S::STAGE;
+    mbar_arrive_expect_tx(&gfull[stage], 2 * S::SLICE);
+    const uint16_t* kp = a.pool + ((page * 2 + 0) * a.Hkv + kvh) * (int64_t)(kP * D);
+    const uint16_t* vp = a.pool + ((page * 2 + 1) * a.Hkv + kvh) * (int64_t)(kP * D);
+    bulk_g2s(dst, kp, S::SLICE, &gfull[stage]);
+    bulk_g2s(dst + S::SLICE, vp, S::SLICE, &gfull[stage]);
+  };
+
+  if (producer) {
+    const int n0 = my_n < S::NSTAGE ? my_n : S::NSTAGE;
+    for (int k = 0; k < n0; ++k) issue(k);
+  }
+
+  // q rows of this warp's heads, scaled into the log2 domain
+  float qr[S::HPW][S::DPL];
+#pragma unroll
+  for (int j = 0; j < S::HPW; ++j) {
+    const int hg = hb + j;
+    if (hg < a.group) {
+      const int hq = kvh * a.group + hg;
+      const uint8_t* qp = reinterpret_cast<const uint8_t*>(
+          a.q + ((int64_t)u.q_row * a.Hq + hq) * D + li * S::DPL);
+      float f[S::DPL];
+      load_row_f32<S::DPL>(qp, f);
+#pragma unroll
+      for (int c = 0; c < S::DPL; ++c) qr[j][c] = f[c] * a.sm_scale_log2;
+    } else {
+#pragma unroll
+      for (int c = 0; c < S::DPL; ++c) qr[j][c] = 0.f;
+    }
+  }
+
+  float o[S::HPW][S::DPL];
+#pragma unroll
+  for (int j = 0; j < S::HPW; ++j)
+#pragma unroll
+    for (int c = 0; c < S::DPL; ++c) o[j][c] = 0.f;
+  float m_run = -INFINITY, l_run = 0.f;  // meaningful in lanes j < HPW for head hb + j
+
+  float* sw = s_scores + warp * kP * S::HPW;
+  float* aw = s_alpha + warp * S::HPW;
+
+  for (int k = 0; k < my_n; ++k) {
+    const int stage = k % S::NSTAGE;
+    const uint32_t parity = (k / S::NSTAGE) & 1;
+    mbar_wait(&gfull[stage], parity, a.err);
+    const uint8_t* kbuf = gring + stage * S::STAGE;
+    const uint8_t* vbuf = kbuf + S::SLICE;
+    const int tok0 = (pg_lo + grp + k * S::NPG) * kP;
+    const int valid = min(kP, u.tok_end - tok0);
+
+    // ---- scores s[t][j] = q_j . k_t (log2 domain)
+    float part[S::NRED];
+#pragma unroll
+    for (int it = 0; it < S::ITERS; ++it) {
+      const int t = 2 * it + half;
+      float kf[S::DPL];
+      load_row_f32<S::DPL>(kbuf + (t * D + li * S::DPL) * 2, kf);
+#pragma unroll
+      for (int j = 0; j < S::HPW; ++j) {
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < S::DPL; ++c) acc = fmaf(qr[j][c], kf[c], acc);
+        part[it * S::HPW + j] = acc;
+      }
+    }
+    reduce_scatter16<S::NRED, 8>(part, li);
+    if ((li & ((1 << S::SH) - 1)) == 0) {
+#pragma unroll
+      for (int f = 0; f < S::NF; ++f) {
+        const int flat = (li >> S::SH) * S::NF + f;
+        const int it = flat / S::HPW, j = flat - it * S::HPW;
+        sw[(2 * it + half) * S::HPW + j] = part[f];
+      }
+    }
+    __syncwarp();
+
+    // ---- online softmax update, one lane per head
+    if (lane < S::HPW) {
+      float mx = -INFINITY;
+      for (int t = 0; t < valid; ++t) mx = fmaxf(mx, sw[t * S::HPW + lane]);
+      const float m_new = fmaxf(m_run, mx);
+      const float alpha = ex2_approx(m_run - m_new);
+      float sum = 0.f;
+      for (int t = 0; t < kP; ++t) {
+        const float p = t < valid ? ex2_approx(sw[t * S::HPW + lane] - m_new) : 0.f;
+        sw[t * S::HPW + lane] = p;
+        sum += p;
+      }
+      l_run = l_run * alpha + sum;
+      m_run = m_new;
+      aw[lane] = alpha;
+    }
+    __syncwarp();
+
+    // ---- o = alpha * o + sum_t p_t v_t
+#pragma unroll
+    for (int j = 0; j < S::HPW; ++j) {
+      const float al = aw[j];
+#pragma unroll
+      for (int c = 0; c < S::DPL; ++c) o[j][c] *= al;
+    }
+#pragma unroll
+    for (int it = 0; it < S::ITERS; ++it) {
+      const int t = 2 * it + half;
+      if (t < valid) {
+        float vf[S::DPL];
+        load_row_f32<S::DPL>(vbuf + (t * D + li * S::DPL) * 2, vf);
+#pragma unroll
+        for (int j = 0; j < S::HPW; ++j) {
+          const float p = sw[t * S::HPW + j];
+#pragma unroll
+          for (int c = 0; c < S::DPL; ++c) o[j][c] = fmaf(p, vf[c], o[j][c]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&gempty[stage]);
+    if (producer && k + S::NSTAGE < my_n) {
+      mbar_wait(&gempty[stage], parity, a.err);
+      issue(k + S::NSTAGE);
+    }
+  }
+
+  // ---- combine the two half-warps (same running max), then the page groups
+#pragma unroll
+  for (int j = 0; j < S::HPW; ++j)
+#pragma unroll
+    for (int c = 0; c < S::DPL; ++c) o[j][c] += __shfl_xor_sync(0xffffffffu, o[j][c], 16);
+
+  __syncthreads();  // ring is free: reuse it for the merge
+  float* mo = reinterpret_cast<float*>(ring);   // [NPG][G][D]
+  float* mm = mo + S::NPG * G * D;              // [NPG][G]
+  float* ml = mm + S::NPG * G;                  // [NPG][G]
+  if (half == 0) {
+#pragma unroll
+    for (int j = 0; j < S::HPW; ++j) {
+      const int hg = hb + j;
+      if (hg < G) {
+#pragma unroll
+        for (int c = 0; c < S::DPL; ++c) mo[(grp * G + hg) * D + li * S::DPL + c] = o[j][c];
+      }
+    }
+  }
+  if (lane < S::HPW && hb + lane < G) {
+    mm[grp * G + hb + lane] = m_run;
+    ml[grp * G + hb + lane] = l_run;
+  }
+  __syncthreads();
+
+  const int group = a.group;
+  for (int i = threadIdx.x; i < group * D; i += S::THREADS) {
+    const int hg = i / D, c = i - hg * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < S::NPG; ++g) M = fmaxf(M, mm[g * G + hg]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int g = 0; g < S::NPG; ++g) {
+      const float w = ex2_approx(mm[g * G + hg] - M);
+      L += w * ml[g * G + hg];
+      O += w * mo[(g * G + hg) * D + c];
+    }
+    const float inv = 1.f / L;
+    const int hq = kvh * group + hg;
+    const float lse2 = M + __log2f(L);
+    if (u.part < 0) {
+      a.out[((int64_t)u.q_row * a.Hq + hq) * D + c] = f32_to_bf16_rn(O * inv);
+      if (c == 0 && a.lse_out) a.lse_out[(int64_t)u.q_row * a.Hq + hq] = lse2 * 0.69314718055994531f;
+    } else {
+      a.part_o[((int64_t)u.part * a.Hq + hq) * D + c] = O * inv;
+      if (c == 0) a.part_lse[(int64_t)u.part * a.Hq + hq] = lse2;
+    }
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+  using S = DecodeShape<D, G>;
+  auto kern = decode_splitkv_kernel<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.n_units, a.Hkv);
+  kern<<<grid, S::THREADS, S::SMEM, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
+  const int g = a.group;
+  if (g <= 1) return launch_decode_t<D, 1>(a, stream);
+  if (g <= 2) return launch_decode_t<D, 2>(a, stream);
+  if (g <= 4) return launch_decode_t<D, 4>(a, stream);
+  if (g <= 8) return launch_decode_t<D, 8>(a, stream);
+  if (g <= 12) return launch_decode_t<D, 12>(a, stream);
+  return launch_decode_t<D, 16>(a, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.n_units <= 0) return cudaSuccess;
+  return a.head_dim == 128 ? launch_decode_d<128>(a, stream) : launch_decode_d<64>(a, stream);
+}
+
+}  // namespace daa

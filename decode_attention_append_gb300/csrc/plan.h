@@ -1,0 +1,55 @@
+// Work descriptors that the host planner writes into the workspace and the
+// kernels read.  Plain 32-byte PODs so one cudaMemcpyAsync moves the whole plan.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+namespace daa {
+
+// One split of the keys of one decode request (qo_len == 1).  The decode kernel
+// runs one CTA per (unit, kv head).  Splits are page aligned.
+struct DecodeUnit {
+  int32_t q_row;      // row of q / out / lse_out
+  int32_t page_base;  // index into page_indices of the request's first page
+  int32_t tok_begin;  // first key of this split (multiple of page_size)
+  int32_t tok_end;    // one past the last key of this split
+  int32_t kv_len;     // keys of the whole request
+  int32_t part;       // partial slot, or -1 when the split covers the request
+  int32_t pad0, pad1;
+};
+
+// softmax_merge of the partials of one decode request that was split.
+struct MergeItem {
+  int32_t q_row;
+  int32_t part_begin;  // first partial slot
+  int32_t n_parts;     // consecutive slots to merge
+  int32_t pad;
+};
+
+// One tile of packed query rows of one prefill request (qo_len > 1): new
+// tokens [tok0, tok0 + ntok) of the request, each with all g query heads of a
+// kv head, packed token-major into ntok * g <= 128 rows.  One CTA per
+// (tile, kv head).
+struct PrefillTile {
+  int32_t q_row0;     // row of the request's first new token
+  int32_t qo_len;
+  int32_t kv_len;
+  int32_t page_base;
+  int32_t tok0;       // first new-token index (0-based within the request)
+  int32_t ntok;       // tokens in this tile
+  int32_t pad0, pad1;
+};
+
+static_assert(sizeof(DecodeUnit) == 32, "DecodeUnit layout");
+static_assert(sizeof(MergeItem) == 16, "MergeItem layout");
+static_assert(sizeof(PrefillTile) == 32, "PrefillTile layout");
+
+// Kernel ids reported by the tracer.
+enum KernelId : int32_t {
+  kKernelAppend = 1,
+  kKernelDecode = 2,
+  kKernelMerge = 3,
+  kKernelPrefill = 4,
+};
+
+}  // namespace daa

@@ -1,0 +1,191 @@
+/*
+ * daa.h -- C ABI of libdaa: paged KV append and mixed-batch paged attention
+ * (chunked-prefill requests and decode requests in one batch) for sm_103a.
+ *
+ * The operation, from the pages it follows:
+ *  - "Chunked prefill" (k4i.top), section "Why chunking does not change the
+ *    result" (#correctness): a prompt is processed in chunks; token i of a
+ *    chunk attends to every position j <= i, i.e. to the cached prefix written
+ *    by earlier chunks plus the causal part of its own chunk, and the two parts
+ *    combine by softmax_merge; after each chunk its new k, v vectors are
+ *    appended to the KV cache.  Section "IO overhead" (#io-overhead) sizes that
+ *    append: C x 2 x n_h x d_h x 2 bytes per layer.
+ *  - "Disaggregated prefill and decode" (Perplexity), section "Prefill vs decode
+ *    performance": decode requests carry qo_len = 1 and are memory bound,
+ *    prefill requests carry large qo_len and are compute bound; attention can
+ *    be split over requests and over kv_len.  Section "Sharded KV cache
+ *    transfers" with the figure "NHD and HND KV cache layouts": the cache is
+ *    paged in the HND layout (heads before tokens), so each head's slice of a
+ *    page is contiguous.  Section "KV Messenger": KV entries are valid after
+ *    the append and before attention reads them.
+ *
+ * Conventions shared by every call
+ *  - All tensors are bf16 (bit patterns, 2 bytes per element), row-major and
+ *    contiguous, on the device unless a parameter says "host".
+ *  - Page pool `kv_pages`: [num_pages][2][Hkv][page_size][head_dim]; index 0 of
+ *    the second dimension holds K, index 1 holds V (HND inside each page).
+ *  - Page table (CSR): request r owns pages page_indices[kv_indptr[r] ..
+ *    kv_indptr[r+1]); its length after this step's append is
+ *    kv_len_r = (npages_r - 1) * page_size + last_page_len[r]
+ *    (kv_len_r = 0 when it owns no page).  1 <= last_page_len[r] <= page_size
+ *    whenever npages_r > 0.  The caller allocates pages; the table already
+ *    covers the post-append length.  Pages of different requests must not
+ *    overlap.
+ *  - Query / new-token rows (CSR): request r owns rows qo_indptr[r] ..
+ *    qo_indptr[r+1]) of q, k_new, v_new and out; qo_len_r <= kv_len_r.  The new
+ *    token i of request r sits at absolute position kv_len_r - qo_len_r + i.
+ *  - GQA: query head h reads kv head h / (Hq / Hkv) (contiguous groups).
+ *  - Ownership: the caller owns every buffer; the library allocates no device
+ *    memory.  Pointers must be 16-byte aligned.
+ *  - Ordering: work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and runs asynchronously; call daa_kv_append before
+ *    daa_batch_attention on the same stream.  No call synchronises the device.
+ *  - Errors: argument checks run on the host before anything is enqueued and
+ *    return a negative daa_status; nothing is thrown across the ABI.  Device
+ *    kernels never read or write outside the pool or the given arrays: a page
+ *    id outside [0, num_pages) or an inconsistent length seen on the device is
+ *    skipped and recorded in a device error word (daa_device_error).
+ *  - Supported: head_dim in {64, 128}; page_size 16; 1 <= Hq/Hkv <= 16 with Hq
+ *    divisible by Hkv.  Other shapes return DAA_ERR_UNSUPPORTED.
+ */
+#ifndef DAA_H_
+#define DAA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DAA_OK = 0,
+  DAA_ERR_INVALID_ARG = -1, /* null pointer, negative count, bad scalar */
+  DAA_ERR_SHAPE = -2,       /* indptr not monotonic, qo_len > kv_len, bad last_page_len */
+  DAA_ERR_PAGE_RANGE = -3,  /* page count inconsistent with the pool */
+  DAA_ERR_UNSUPPORTED = -4, /* head_dim / page_size / group size outside the support matrix */
+  DAA_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
+  DAA_ERR_WORKSPACE = -6,   /* workspace missing or smaller than the size query */
+  DAA_ERR_ALIGNMENT = -7    /* a pointer is not 16-byte aligned */
+} daa_status;
+
+typedef struct {
+  int32_t num_qo_heads; /* Hq */
+  int32_t num_kv_heads; /* Hkv */
+  int32_t head_dim;     /* d */
+  int32_t page_size;    /* P (tokens per page) */
+  int64_t num_pages;    /* pages in the pool */
+} daa_dims;
+
+/* Human-readable name of a status code (static storage). */
+const char* daa_status_string(daa_status s);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int32_t daa_version(void);
+
+/*
+ * KV append ("Chunked prefill", #correctness: K_cache += [k_{(s-1)C+1} .. k_{sC}];
+ * #io-overhead for its size).
+ *
+ * For every request r and each of its n_r = append_indptr[r+1] - append_indptr[r]
+ * new tokens t (0 <= t < n_r), writes
+ *   kv_pages[p][0][h][s][:] = k_new[append_indptr[r] + t][h][:]
+ *   kv_pages[p][1][h][s][:] = v_new[append_indptr[r] + t][h][:]
+ * for every kv head h, where pos = kv_len_r - n_r + t,
+ * p = page_indices[kv_indptr[r] + pos / page_size] and s = pos % page_size.
+ * A bit-exact copy; nothing else in the pool is touched.
+ *
+ *  k_new, v_new   device, bf16 [nnz_new][Hkv][head_dim]
+ *  kv_pages       device, bf16 pool (see conventions), written
+ *  append_indptr  device, int32 [batch + 1], append_indptr[batch] == nnz_new
+ *                 (the same array as qo_indptr of the attention call)
+ *  page_indices   device, int32 [kv_indptr[batch]]
+ *  kv_indptr      device, int32 [batch + 1]
+ *  last_page_len  device, int32 [batch], post-append
+ *  batch, nnz_new host scalars (batch >= 0, nnz_new >= 0)
+ *  dims           shapes; num_qo_heads is not used here but must be valid
+ *  stream         cudaStream_t
+ * Errors: DAA_ERR_INVALID_ARG / _UNSUPPORTED / _ALIGNMENT on the host,
+ * DAA_ERR_CUDA if the launch fails.  Lengths and page ids are checked on the
+ * device (see daa_device_error).
+ */
+daa_status daa_kv_append(const void* k_new, const void* v_new, void* kv_pages,
+                         const int32_t* append_indptr, const int32_t* page_indices,
+                         const int32_t* kv_indptr, const int32_t* last_page_len, int32_t batch,
+                         int32_t nnz_new, daa_dims dims, void* stream);
+
+/*
+ * Bytes of device workspace daa_batch_attention needs for this batch (0 if
+ * none).  Reads the host mirrors only; a pure function of its arguments and of
+ * the current device's SM count.  Returns 0 and sets *status (if non-NULL) to
+ * an error for invalid input.
+ */
+size_t daa_batch_attention_workspace_size(const int32_t* h_qo_indptr, const int32_t* h_kv_indptr,
+                                          const int32_t* h_last_page_len, int32_t batch,
+                                          daa_dims dims, daa_status* status);
+
+/*
+ * Mixed-batch paged attention ("Chunked prefill", #correctness; "Disaggregated
+ * prefill and decode", "Prefill vs decode performance").
+ *
+ * For every request r, new token i and query head h (kv head hk = h / (Hq/Hkv)),
+ * with pos = kv_len_r - qo_len_r + i and key range J = {j : j <= pos} when
+ * causal (J = {j < kv_len_r} otherwise):
+ *   s_j = sm_scale * q[row][h][:] . K_r[j][hk][:]
+ *   out[row][h][:] = sum_{j in J} softmax_J(s)_j * V_r[j][hk][:]      (bf16, RNE)
+ *   lse_out[row][h] = ln sum_{j in J} exp(s_j)                          (fp32)
+ * where row = qo_indptr[r] + i and K_r / V_r are read from the request's pages.
+ * Requests with qo_len = 1 run the split-KV decode kernel followed by the
+ * softmax_merge pass; requests with qo_len > 1 run the tensor-core prefill
+ * kernel.  Rows of requests with qo_len = 0 do not exist; nothing is written.
+ *
+ *  q              device, bf16 [nnz_qo][Hq][head_dim]
+ *  kv_pages       device, bf16 pool (read only)
+ *  qo_indptr, kv_indptr, page_indices, last_page_len    device int32 (as above)
+ *  h_qo_indptr, h_kv_indptr, h_last_page_len            host int32 copies of
+ *                 the same arrays; used to validate and to plan the split of the
+ *                 work on the host, so the call never waits on the device
+ *  batch          number of requests
+ *  causal         1: keys j <= pos; 0: all kv_len keys
+ *  sm_scale       score scale, e.g. 1/sqrt(head_dim)
+ *  out            device, bf16 [nnz_qo][Hq][head_dim], written
+ *  lse_out        device, fp32 [nnz_qo][Hq] natural-log LSE, or NULL
+ *  workspace      device scratch of at least
+ *                 daa_batch_attention_workspace_size(...) bytes (NULL if 0);
+ *                 the call owns it until the enqueued work completes
+ *  stream         cudaStream_t
+ * Errors: DAA_ERR_* on the host before any launch; DAA_ERR_CUDA on a failed
+ * launch or copy.
+ */
+daa_status daa_batch_attention(const void* q, const void* kv_pages, const int32_t* qo_indptr,
+                               const int32_t* kv_indptr, const int32_t* page_indices,
+                               const int32_t* last_page_len, const int32_t* h_qo_indptr,
+                               const int32_t* h_kv_indptr, const int32_t* h_last_page_len,
+                               int32_t batch, int32_t causal, float sm_scale, void* out,
+                               float* lse_out, void* workspace, size_t workspace_bytes,
+                               daa_dims dims, void* stream);
+
+/*
+ * Reads the device error word of the current device into *code (0 = none, 1 =
+ * page id out of range, 2 = a bounded wait timed out, 3 = inconsistent request
+ * lengths) and clears it when `reset` is non-zero.  Synchronises the device.
+ */
+daa_status daa_device_error(int32_t* code, int32_t reset);
+
+/*
+ * Per-kernel timing with CUDA events.  While enabled, every kernel the library
+ * launches is bracketed by two events on its stream (up to `capacity` launches
+ * are kept, older ones dropped).  daa_trace_read synchronises on the recorded
+ * events and copies out up to `max_records` (kernel id, milliseconds) pairs in
+ * launch order, returning how many were written, then clears the record.
+ * Kernel ids: 1 kv_append, 2 decode split-KV, 3 softmax_merge, 4 prefill.
+ */
+daa_status daa_trace_enable(int32_t capacity);
+daa_status daa_trace_disable(void);
+int32_t daa_trace_read(int32_t* kernel_ids, float* milliseconds, int32_t max_records);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DAA_H_ */

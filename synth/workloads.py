@@ -141,15 +141,25 @@ class Workload:
         t = t.to(torch.bfloat16)
         return t
 
+    def rows_into(self, out: torch.Tensor, seq: int, kind: int, lo: int, hi: int) -> None:
+        """Write bf16 rows [lo, hi) of tensor ``kind`` of sequence ``seq`` into out[:hi-lo]."""
+        at = 0
+        b = lo // _BLOCK
+        while lo + at < hi:
+            blk = self._block(seq, kind, b)
+            s0 = lo + at - b * _BLOCK
+            n = min(_BLOCK - s0, hi - lo - at)
+            out[at:at + n].copy_(blk[s0:s0 + n])
+            at += n
+            b += 1
+
     def rows(self, seq: int, kind: int, lo: int, hi: int) -> torch.Tensor:
         """bf16 rows [lo, hi) of tensor ``kind`` of sequence ``seq``: [hi-lo, H, d]."""
         heads = self.num_qo_heads if kind == _KIND_Q else self.num_kv_heads
-        if hi <= lo:
-            return torch.empty(0, heads, self.head_dim, dtype=torch.bfloat16)
-        b0, b1 = lo // _BLOCK, (hi - 1) // _BLOCK
-        blocks = [self._block(seq, kind, b) for b in range(b0, b1 + 1)]
-        cat = torch.cat(blocks, 0) if len(blocks) > 1 else blocks[0]
-        return cat[lo - b0 * _BLOCK: hi - b0 * _BLOCK]
+        out = torch.empty(max(0, hi - lo), heads, self.head_dim, dtype=torch.bfloat16)
+        if hi > lo:
+            self.rows_into(out, seq, kind, lo, hi)
+        return out
 
     def q_rows(self, seq, lo, hi):
         return self.rows(seq, _KIND_Q, lo, hi)
@@ -160,25 +170,26 @@ class Workload:
     def v_rows(self, seq, lo, hi):
         return self.rows(seq, _KIND_V, lo, hi)
 
+    def _gather(self, kind: int, spans: Sequence[Tuple[int, int, int]]) -> torch.Tensor:
+        heads = self.num_qo_heads if kind == _KIND_Q else self.num_kv_heads
+        n = sum(hi - lo for _, lo, hi in spans)
+        out = torch.empty(n, heads, self.head_dim, dtype=torch.bfloat16)
+        at = 0
+        for seq, lo, hi in spans:
+            if hi > lo:
+                self.rows_into(out[at:at + hi - lo], seq, kind, lo, hi)
+                at += hi - lo
+        return out
+
     def initial_kv(self) -> Tuple[torch.Tensor, torch.Tensor]:
         """K and V of every sequence's initially cached prefix, concatenated."""
-        ks, vs = [], []
-        for s, c in self.initial_entries():
-            ks.append(self.k_rows(s, 0, c))
-            vs.append(self.v_rows(s, 0, c))
-        return _cat(ks, self.num_kv_heads, self.head_dim), _cat(vs, self.num_kv_heads, self.head_dim)
+        spans = [(s, 0, c) for s, c in self.initial_entries()]
+        return self._gather(_KIND_K, spans), self._gather(_KIND_V, spans)
 
     def step_inputs(self, k: int) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
         """(q [nnz_qo, Hq, d], k_new [nnz_qo, Hkv, d], v_new) of step k, bf16."""
-        qs, ks, vs = [], [], []
-        for r in self.steps[k].requests:
-            lo, hi = r.kv_len - r.qo_len, r.kv_len
-            qs.append(self.q_rows(r.seq, lo, hi))
-            ks.append(self.k_rows(r.seq, lo, hi))
-            vs.append(self.v_rows(r.seq, lo, hi))
-        return (_cat(qs, self.num_qo_heads, self.head_dim),
-                _cat(ks, self.num_kv_heads, self.head_dim),
-                _cat(vs, self.num_kv_heads, self.head_dim))
+        spans = [(r.seq, r.kv_len - r.qo_len, r.kv_len) for r in self.steps[k].requests]
+        return self._gather(_KIND_Q, spans), self._gather(_KIND_K, spans), self._gather(_KIND_V, spans)
 
     # ------------------------------------------------------------- accounting
     def summary(self, k: int = 0) -> Dict:
@@ -193,13 +204,6 @@ class Workload:
             num_pages=self.num_pages, Hq=self.num_qo_heads, Hkv=self.num_kv_heads,
             head_dim=self.head_dim, page_size=self.page_size,
         )
-
-
-def _cat(ts, heads, d):
-    ts = [t for t in ts if t.shape[0] > 0]
-    if not ts:
-        return torch.empty(0, heads, d, dtype=torch.bfloat16)
-    return torch.cat(ts, 0).contiguous()
 
 
 def chunk_schedule(L: int, C: int) -> List[Tuple[int, int]]:

@@ -1,0 +1,64 @@
+"""Drive the CUDA path over a synthetic workload (GPU tests and smoke only)."""
+from __future__ import annotations
+
+import copy
+
+import numpy as np
+import torch
+
+import decode_attention_append_gb300 as daa
+from synth import SENTINEL_BF16
+
+
+def new_pool(wl, device):
+    return torch.full(wl.pool_shape(), SENTINEL_BF16, dtype=torch.int16, device=device).view(torch.bfloat16)
+
+
+def gpu_fill(wl, pool, device):
+    """Append every sequence's initially cached prefix (the CUDA append)."""
+    it = wl.initial_table()
+    k0, v0 = wl.initial_kv()
+    if k0.shape[0] == 0:
+        return
+    t = daa.PageTable.from_host(it["qo_indptr"], it["kv_indptr"], it["page_indices"],
+                                it["last_page_len"], device)
+    daa.kv_append(k0.to(device), v0.to(device), pool, t.qo_indptr, t.page_indices, t.kv_indptr,
+                  t.last_page_len)
+
+
+def gpu_step(wl, pool, k, device, with_lse=True):
+    """Append step k's new K/V and run attention: (out bf16 cpu, lse fp32 cpu)."""
+    st = wl.step_table(k)
+    q, kn, vn = wl.step_inputs(k)
+    tab = daa.PageTable.from_host(st["qo_indptr"], st["kv_indptr"], st["page_indices"],
+                                  st["last_page_len"], device)
+    runner = daa.BatchAttention(tab, wl.num_qo_heads, pool, causal=wl.causal, sm_scale=wl.sm_scale)
+    if kn.shape[0]:
+        runner.append(kn.to(device), vn.to(device))
+    qd = q.to(device)
+    lse = torch.full((q.shape[0], wl.num_qo_heads), float("nan"), device=device) if with_lse else None
+    out = torch.full_like(qd, float("nan"))
+    runner.run(qd, out=out, lse=lse)
+    torch.cuda.synchronize()
+    return out.cpu(), (lse.cpu() if lse is not None else None)
+
+
+def pool_bits(pool: torch.Tensor) -> np.ndarray:
+    return pool.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def compact(wl):
+    """Copy of wl whose pages are renumbered 0..n-1 in order of use (so the
+    oracle's pool holds only the pages the workload touches)."""
+    w = copy.copy(wl)
+    w.seqs = []
+    mapping = {}
+    nxt = 0
+    for s in wl.seqs:
+        new = np.arange(nxt, nxt + len(s.pages), dtype=np.int32)
+        for a, b in zip(s.pages, new):
+            mapping[int(a)] = int(b)
+        nxt += len(s.pages)
+        w.seqs.append(type(s)(s.length, new))
+    w.num_pages = max(1, nxt)
+    return w, mapping

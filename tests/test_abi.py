@@ -1,0 +1,146 @@
+"""CPU-side checks of the C ABI: the library builds and loads, exports every
+symbol the header declares, and rejects invalid arguments on the host before
+touching the device.  No compute call runs here (there is no GPU)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decode_attention_append_gb300 import build
+    build.build()
+    import decode_attention_append_gb300 as daa
+    return daa.load_library()
+
+
+def _declared_symbols():
+    with open(os.path.join(ROOT, "include", "daa.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(daa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = _declared_symbols()
+    for s in ("daa_kv_append", "daa_batch_attention", "daa_batch_attention_workspace_size",
+              "daa_status_string", "daa_device_error", "daa_trace_enable", "daa_trace_read"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [s for s in _declared_symbols() if not hasattr(lib, s)]
+    assert not missing, missing
+
+
+def test_library_exports_nothing_undeclared(lib):
+    import subprocess
+    from decode_attention_append_gb300 import library_path
+    out = subprocess.run(["nm", "-D", "--defined-only", library_path()], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("nm unavailable")
+    exported = {ln.split()[-1] for ln in out.stdout.splitlines() if " T " in ln}
+    daa_syms = {s for s in exported if s.startswith("daa_")}
+    assert daa_syms == set(_declared_symbols())
+
+
+def test_status_strings(lib):
+    for code in range(0, -8, -1):
+        s = lib.daa_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.daa_version() > 0
+
+
+def _dims(Hq=4, Hkv=2, d=64, P=16, n=64):
+    import decode_attention_append_gb300 as daa
+    return daa._Dims(Hq, Hkv, d, P, n)
+
+
+def _ws(lib, qo, kv, last, dims):
+    st = ctypes.c_int32(0)
+    qo, kv, last = (np.asarray(x, np.int32) for x in (qo, kv, last))
+    n = lib.daa_batch_attention_workspace_size(qo.ctypes.data_as(ctypes.c_void_p),
+                                               kv.ctypes.data_as(ctypes.c_void_p),
+                                               last.ctypes.data_as(ctypes.c_void_p), len(qo) - 1,
+                                               dims, ctypes.byref(st))
+    return n, st.value
+
+
+@pytest.mark.parametrize("qo,kv,last,dims,expect", [
+    ([0, 2], [0, 1], [1], _dims(), -2),                 # qo_len 2 > kv_len 1
+    ([0, 1], [0, 1], [0], _dims(), -2),                 # last_page_len 0 with a page
+    ([0, 1], [0, 1], [17], _dims(), -2),                # last_page_len > page_size
+    ([1, 1], [0, 1], [1], _dims(), -2),                 # indptr not starting at 0
+    ([0, 3, 2], [0, 1, 2], [16, 16], _dims(), -2),      # decreasing qo_indptr
+    ([0, 1], [0, 1], [1], _dims(d=96), -4),             # head_dim unsupported
+    ([0, 1], [0, 1], [1], _dims(P=32), -4),             # page_size unsupported
+    ([0, 1], [0, 1], [1], _dims(Hq=34, Hkv=2), -4),     # group size 17
+    ([0, 1], [0, 1], [1], _dims(Hq=5, Hkv=2), -1),      # Hq not divisible by Hkv
+    ([0, 1], [0, 1], [1], _dims(n=0), -1),              # empty pool
+])
+def test_host_validation_rejects(lib, qo, kv, last, dims, expect):
+    n, st = _ws(lib, qo, kv, last, dims)
+    assert st == expect and n == 0
+
+
+def test_workspace_size_decode_and_prefill(lib):
+    # two decodes of 40 and 73 tokens plus a 16-token chunk at offset 48: only
+    # the plan is needed (the requests are short enough not to be split)
+    n, st = _ws(lib, [0, 16, 17, 18], [0, 4, 7, 12], [16, 8, 9], _dims())
+    assert st == 0 and n > 0 and n % 256 == 0
+    n0, st0 = _ws(lib, [0], [0], [], _dims())
+    assert st0 == 0 and n0 == 0
+
+
+def test_workspace_grows_with_split_decodes(lib):
+    # one long decode (40k tokens) gets split: partial outputs need space
+    pages = 2500
+    n_short, _ = _ws(lib, [0, 1], [0, 4], [16], _dims(Hq=8, Hkv=1, d=128))
+    n_long, _ = _ws(lib, [0, 1], [0, pages], [16], _dims(Hq=8, Hkv=1, d=128, n=4096))
+    assert n_long > n_short + 8 * 128 * 4
+
+
+def test_null_pointers_rejected_before_any_launch(lib):
+    import decode_attention_append_gb300 as daa
+    d = _dims()
+    st = lib.daa_kv_append(None, None, None, None, None, None, None, 1, 4, d, None)
+    assert st == -1
+    qo = np.asarray([0, 1], np.int32)
+    kv = np.asarray([0, 1], np.int32)
+    last = np.asarray([1], np.int32)
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+    st = lib.daa_batch_attention(None, None, None, None, None, None, p(qo), p(kv), p(last), 1, 1,
+                                 0.125, None, None, None, 0, d, None)
+    assert st == -1
+    st = lib.daa_batch_attention(None, None, None, None, None, None, p(qo), p(kv), p(last), 1, 1,
+                                 float("nan"), None, None, None, 0, d, None)
+    assert st == -1
+    assert daa.STATUS[-1] == "invalid argument"
+
+
+def test_misaligned_pointers_rejected(lib):
+    d = _dims()
+    st = lib.daa_kv_append(ctypes.c_void_p(0x1008), ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000),
+                           ctypes.c_void_p(0x4000), ctypes.c_void_p(0x5000), ctypes.c_void_p(0x6000),
+                           ctypes.c_void_p(0x7000), 1, 4, d, None)
+    assert st == -7
+
+
+def test_oracle_and_library_share_no_code():
+    """The checker and the product are independent: no source of one includes,
+    imports or links the other."""
+    pkg = os.path.join(ROOT, "decode_attention_append_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in re.sub(r"(#|//).*", "", text), f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c")):
+            text = open(os.path.join(ROOT, "oracle", f)).read()
+            assert "decode_attention_append_gb300" not in text and "daa.h" not in text, f

@@ -1,0 +1,156 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Both sides read the same seeded inputs from ``synth`` and each builds its own
+page pool with its own append.  Acceptance (task statement of the method):
+* kv_append and the page layout: bit-exact, sentinel bytes untouched;
+* attention (bf16 in, fp32 accumulate, bf16 out) against the fp64 oracle:
+  max |err| <= 1.5e-2 and mean |err| <= 2e-3; relative L2 <= 1e-2 as a
+  stricter diagnostic; natural-log LSE within 1e-3 (the GPU sums fp32
+  exponentials, so only fp32 rounding separates it from the fp64 value);
+* GPU chunked vs one-shot prefill within 1e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import SENTINEL_BF16, make_prompt_workload, make_random_workload, make_workload
+from support import err_stats, oracle_pool, oracle_step
+
+pytestmark = pytest.mark.gpu
+
+MAX_ERR, MEAN_ERR, REL_L2, LSE_ERR = 1.5e-2, 2e-3, 1e-2, 1e-3
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def _check(out, lse, ref, ref_lse, what):
+    got = out.double().numpy()
+    mx, mean, rel = err_stats(got, ref)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    assert mx <= MAX_ERR and mean <= MEAN_ERR and rel <= REL_L2, (what, mx, mean, rel)
+    if lse is not None:
+        le = np.abs(lse.double().numpy() - ref_lse).max()
+        assert le <= LSE_ERR, (what, "lse", le)
+    return mx, mean, rel
+
+
+def _run_both(wl, dev, sel_rows=None, compare_pool=True):
+    from gpu_support import compact, gpu_fill, gpu_step, new_pool, pool_bits
+    cw, mapping = compact(wl)
+    opool = oracle_pool(cw)
+    gpool = new_pool(wl, dev)
+    gpu_fill(wl, gpool, dev)
+    stats = []
+    for k in range(len(wl.steps)):
+        out, lse = gpu_step(wl, gpool, k, dev)
+        ref, ref_lse, _ = oracle_step(cw, opool, k, sel_rows=sel_rows)
+        if sel_rows is not None:
+            out, lse = out[sel_rows], lse[sel_rows]
+        stats.append(_check(out, lse, ref, ref_lse, f"{wl.name} step {k}"))
+    if compare_pool:
+        orig = np.asarray(sorted(mapping), np.int64)
+        new = np.asarray([mapping[int(p)] for p in orig], np.int64)
+        g = pool_bits(gpool[torch.from_numpy(orig).to(dev)])
+        assert np.array_equal(g, opool[new]), f"{wl.name}: page bytes differ"
+        # pages no request owns stay sentinel
+        untouched = torch.ones(wl.num_pages, dtype=torch.bool, device=dev)
+        untouched[torch.from_numpy(orig).to(dev)] = False
+        assert bool((gpool.view(torch.int16)[untouched] == SENTINEL_BF16).all())
+    return stats
+
+
+def test_tiny_mixed_all_steps_bit_exact_pool(dev):
+    from gpu_support import gpu_fill, gpu_step, new_pool, pool_bits
+    wl = make_workload("tiny_mixed")
+    opool = oracle_pool(wl)
+    gpool = new_pool(wl, dev)
+    gpu_fill(wl, gpool, dev)
+    for k in range(len(wl.steps)):
+        out, lse = gpu_step(wl, gpool, k, dev)
+        ref, ref_lse, _ = oracle_step(wl, opool, k)
+        _check(out, lse, ref, ref_lse, f"tiny step {k}")
+        assert np.array_equal(pool_bits(gpool), opool), f"pool differs after step {k}"
+
+
+EDGE = [
+    # (seed, Hq, Hkv, d, [(qo, kv), ...], causal)
+    (101, 4, 4, 128, [(1, 1), (1, 17), (2, 2), (3, 40)], True),
+    (102, 8, 1, 128, [(129, 300), (1, 5000), (0, 33), (128, 128)], True),
+    (103, 12, 1, 128, [(37, 1000), (1, 4097), (1, 16)], True),
+    (104, 6, 2, 64, [(5, 5), (17, 100), (1, 7)], True),
+    (105, 16, 1, 128, [(300, 300), (1, 20000)], True),
+    (106, 2, 2, 64, [(255, 1000), (1, 1)], True),
+    (107, 8, 1, 128, [(129, 300), (1, 5000), (0, 33), (128, 128)], False),
+    (108, 4, 2, 128, [(16, 16)] * 3 + [(1, 2049)] * 5, True),
+    (109, 32, 8, 128, [(512, 2048)] + [(1, 1024 + 97 * i) for i in range(8)], True),
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: f"seed{c[0]}")
+def test_edge_cases(dev, case):
+    seed, Hq, Hkv, d, reqs, causal = case
+    wl = make_random_workload(seed, Hq, Hkv, d, 16, reqs, extra_pages=7)
+    wl.causal = causal
+    _run_both(wl, dev)
+
+
+def test_decode_kv_len_one_returns_v(dev):
+    from gpu_support import gpu_fill, gpu_step, new_pool
+    wl = make_random_workload(111, 8, 2, 128, 16, [(1, 1), (1, 1)])
+    gpool = new_pool(wl, dev)
+    gpu_fill(wl, gpool, dev)
+    out, _ = gpu_step(wl, gpool, 0, dev)
+    for r in range(2):
+        v = wl.v_rows(r, 0, 1)[0]                          # [Hkv, d]
+        expect = v.repeat_interleave(4, dim=0)             # head h reads kv head h // 4
+        assert torch.equal(out[r], expect)
+
+
+@pytest.mark.parametrize("name", ["mha_decode", "chunked_prefill_mixed", "gqa_decode_shard"])
+def test_config_full_rows(dev, name):
+    _run_both(make_workload(name), dev)
+
+
+def test_long_prefill_sampled_rows(dev):
+    wl = make_workload("long_prefill")
+    rng = np.random.default_rng(5)
+    prompt_rows = []
+    for p in range(4):
+        base = p * 8192
+        prompt_rows += [base, base + 1, base + 15, base + 16, base + 8191]
+        prompt_rows += list(base + rng.choice(8192, 6, replace=False))
+    decode_rows = list(range(4 * 8192, 4 * 8192 + 64))
+    sel = sorted(set(prompt_rows)) + decode_rows
+    _run_both(wl, dev, sel_rows=sel)
+
+
+def test_chunked_vs_one_shot_gpu(dev):
+    """#correctness on the GPU: 4 chunks of 512 vs one 2048-token prefill give
+    a byte-identical cache and outputs within 1e-2."""
+    from gpu_support import gpu_fill, gpu_step, new_pool, pool_bits
+    wc = make_prompt_workload(2048, 512, 32, 8, 128, 16, 1003, decodes=[1500, 3000])
+    wo = make_prompt_workload(2048, 2048, 32, 8, 128, 16, 1003)
+    wo.num_pages = wc.num_pages
+    wo.seqs[0].pages = wc.seqs[0].pages.copy()
+    pc, po = new_pool(wc, dev), new_pool(wo, dev)
+    gpu_fill(wc, pc, dev)
+    gpu_fill(wo, po, dev)
+    chunks = [gpu_step(wc, pc, k, dev)[0][:512] for k in range(4)]
+    one, _ = gpu_step(wo, po, 0, dev)
+    pages = torch.from_numpy(wc.seqs[0].pages.astype(np.int64)).to(dev)
+    assert np.array_equal(pool_bits(pc[pages]), pool_bits(po[pages]))
+    diff = (torch.cat(chunks, 0).double() - one.double()).abs().max().item()
+    assert diff <= 1e-2, diff
+
+
+def test_no_device_error_recorded(dev):
+    import decode_attention_append_gb300 as daa
+    assert daa.device_error(reset=True) == 0
