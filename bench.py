@@ -26,6 +26,7 @@ import argparse
 import hashlib
 import json
 import math
+import shutil
 import os
 import subprocess
 import sys
@@ -109,6 +110,8 @@ class ClockSampler:
         self.path = None
 
     def start(self):
+        if not shutil.which("nvidia-smi"):
+            return
         try:
             os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
             self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
@@ -118,6 +121,14 @@ class ClockSampler:
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # wait for the first sample so the window is covered
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 5.0:
+            self.fh.flush()
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -210,6 +221,18 @@ class GpuStep:
         return h2d, d2h
 
 
+def soak(fn, seconds):
+    """Run fn back to back for about `seconds` of wall time (untimed)."""
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < seconds:
+        fn()
+        n += 1
+        if n % 16 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+
+
 def timed(fn, steps, flush=None):
     """Sum of per-step CUDA-event times (ms) on the current stream."""
     s = torch.cuda.current_stream()
@@ -297,6 +320,18 @@ def cpu_baseline(wl, budget_s=12.0, reps=None):
                 sample=s.sample + f", median of {len(times)} runs of {t:.3f} s")
 
 
+def compact_pool(wl):
+    """Same workload with pages renumbered 0..n-1 in order of use."""
+    import copy
+    w = copy.copy(wl)
+    nxt, seqs = 0, []
+    for s in wl.seqs:
+        seqs.append(type(s)(s.length, np.arange(nxt, nxt + len(s.pages), dtype=np.int32)))
+        nxt += len(s.pages)
+    w.seqs, w.num_pages = seqs, max(1, nxt)
+    return w
+
+
 # ---------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -306,6 +341,9 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="mha_decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--compact-pool", action="store_true",
+                    help="renumber pages densely so the pool holds only the pages used "
+                         "(same work; smaller device footprint for profiler captures)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -314,6 +352,8 @@ def main():
 
     from synth import make_workload
     wl = make_workload(args.workload)
+    if args.compact_pool:
+        wl = compact_pool(wl)
     acc = step_accounting(wl)
     algo_bytes = acc["decode_bytes"] + acc["append_bytes"] + acc["prefill_bytes"]
     summary = wl.summary()
@@ -322,7 +362,7 @@ def main():
               "prefill_requests": summary["prefill_requests"], "kv_tokens": summary["kv_tokens"],
               "Hq": wl.num_qo_heads, "Hkv": wl.num_kv_heads, "head_dim": wl.head_dim,
               "page_size": wl.page_size, "num_pages": wl.num_pages,
-              "parallelism": f"replicas{args.gpus}"}
+              "parallelism": f"replicas{args.gpus}", "compact_pool": bool(args.compact_pool)}
 
     if args.impl == "reference":
         if rank != 0:
@@ -378,9 +418,12 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    # ---- main timed region: device-resident inputs
+    # ---- main timed region: device-resident inputs.  Clocks are sampled by
+    # nvidia-smi (100 ms period) over a window of back-to-back identical steps
+    # that contains the timed region: ~1 s of steps before it, ~0.5 s after.
     clocks = ClockSampler(local)
     clocks.start()
+    soak(g.step, 1.0)
     barrier()
     ms = timed(g.step, args.steps, flush)
     barrier()
@@ -390,7 +433,10 @@ def main():
     recs = daa.trace_read()
     daa.trace_disable()
     barrier()
+    soak(g.step, 0.5)
     clk = clocks.stop()
+    if clk is not None:
+        clk["window"] = "nvidia-smi samples over back-to-back steps around the timed region"
 
     # ---- e2e: host buffers through the public API
     for _ in range(2):
