@@ -77,6 +77,9 @@ def load_library():
         lib.daa_batch_attention.restype = i32
         lib.daa_batch_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, vp, vp,
                                             vp, sz, _Dims, vp]
+        lib.daa_batch_attention_noalloc.restype = i32
+        lib.daa_batch_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32,
+                                                    vp, vp, _Dims, vp]
         lib.daa_device_error.restype = i32
         lib.daa_device_error.argtypes = [ctypes.POINTER(i32), i32]
         lib.daa_trace_enable.restype = i32
@@ -201,6 +204,33 @@ def batch_attention(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_l
                                    _ptr(hl), batch, int(bool(causal)), float(sm_scale), _ptr(out),
                                    _ptr(lse), _ptr(workspace), ws_bytes, dims, _stream(stream)),
            "batch_attention")
+    return out
+
+
+def batch_attention_noalloc(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len,
+                            host_indptr, causal=True, sm_scale=None, out=None, lse=None,
+                            stream=None):
+    """``batch_attention`` without a workspace: the library's fixed device
+    scratch array is used instead (see daa_batch_attention_noalloc in daa.h for
+    its size limit and for why calls must not overlap on the GPU)."""
+    lib = load_library()
+    _dev_bf16(q, "q"), _dev_bf16(kv_pages, "kv_pages")
+    for n, t in (("qo_indptr", qo_indptr), ("kv_indptr", kv_indptr), ("page_indices", page_indices),
+                 ("last_page_len", last_page_len)):
+        _dev_i32(t, n)
+    Hq, d = q.shape[1], q.shape[2]
+    dims = _dims(kv_pages, Hq)
+    if sm_scale is None:
+        sm_scale = 1.0 / float(d) ** 0.5
+    hq, hk, hl = (_host_i32(x) for x in host_indptr)
+    if out is None:
+        out = torch.empty_like(q)
+    _dev_bf16(out, "out")
+    _check(lib.daa_batch_attention_noalloc(_ptr(q), _ptr(kv_pages), _ptr(qo_indptr), _ptr(kv_indptr),
+                                           _ptr(page_indices), _ptr(last_page_len), _ptr(hq), _ptr(hk),
+                                           _ptr(hl), len(hq) - 1, int(bool(causal)), float(sm_scale),
+                                           _ptr(out), _ptr(lse), dims, _stream(stream)),
+           "batch_attention_noalloc")
     return out
 
 

@@ -165,6 +165,51 @@ daa_status daa_batch_attention(const void* q, const void* kv_pages, const int32_
                                float* lse_out, void* workspace, size_t workspace_bytes,
                                daa_dims dims, void* stream);
 
+/* Size of the device scratch array behind daa_batch_attention_noalloc (48 MiB). */
+#define DAA_NOALLOC_SCRATCH_BYTES (48u * 1024u * 1024u)
+
+/*
+ * daa_batch_attention for callers that cannot allocate device memory.  The
+ * pages describe no such call; it has no counterpart there.
+ *
+ * Who needs it: a caller with no device allocator at the call site -- e.g. a
+ * serving engine that has handed all free HBM to its KV page pool and keeps no
+ * allocator to carve a workspace from, code on a latency-critical path where a
+ * cudaMalloc/cudaFree could synchronise the device, or a foreign-language host
+ * with no binding to a CUDA allocator.  It computes exactly what
+ * daa_batch_attention computes, with the same arguments minus the workspace.
+ *
+ * Scratch: the work plan and the split-KV partial outputs live in one
+ * file-scope __device__ array of DAA_NOALLOC_SCRATCH_BYTES bytes, which every
+ * GPU that loads the library holds until the process exits.  The call makes no
+ * cudaMalloc/cudaFree and no other allocation (device or host heap); its plan
+ * is built in fixed-size static host buffers.  A batch whose scratch would
+ * exceed the array, or that needs more than 16384 decode splits, 16384 split
+ * requests or 16384 prefill tiles, is rejected with DAA_ERR_WORKSPACE before
+ * anything is enqueued.
+ *
+ * Set-up: the first call on each device (with that device current) looks up
+ * the array's device address with cudaGetSymbolAddress and caches it; make that
+ * first call before any stream capture on that device.
+ *
+ * Sharing: every call, on every stream and host thread, uses the same array,
+ * which keeps the last call's contents.  Nothing in it has to start at zero --
+ * every byte a call reads was written earlier in that same call -- but calls
+ * whose GPU work overlaps (concurrent streams, or calls from several host
+ * threads without ordering between their streams) race on the scratch and
+ * produce wrong results.  Serialise them, e.g. by issuing all such calls on one
+ * stream.  Host-side calls are serialised by an internal mutex.
+ *
+ * Arguments, layouts and the other errors are those of daa_batch_attention.
+ */
+daa_status daa_batch_attention_noalloc(const void* q, const void* kv_pages,
+                                       const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                       const int32_t* page_indices, const int32_t* last_page_len,
+                                       const int32_t* h_qo_indptr, const int32_t* h_kv_indptr,
+                                       const int32_t* h_last_page_len, int32_t batch,
+                                       int32_t causal, float sm_scale, void* out, float* lse_out,
+                                       daa_dims dims, void* stream);
+
 /*
  * Reads the device error word of the current device into *code (0 = none, 1 =
  * page id out of range, 2 = a bounded wait timed out, 3 = inconsistent request
