@@ -267,7 +267,7 @@ daa_status daa_kv_append(const void* k_new, const void* v_new, void* kv_pages,
   cudaError_t e = traced(kKernelAppend, s, [&] {
     return launch_kv_append(k_new, v_new, kv_pages, append_indptr, page_indices, kv_indptr,
                             last_page_len, batch, nnz_new, dims.num_kv_heads, dims.head_dim,
-                            dims.num_pages, err, s);
+                            dims.num_pages, num_sms(), err, s);
   });
   return e == cudaSuccess ? DAA_OK : DAA_ERR_CUDA;
 }

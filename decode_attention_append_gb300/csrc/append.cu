@@ -6,12 +6,14 @@
 // "Disaggregated prefill and decode" (Perplexity), "Sharded KV cache
 // transfers": HND pages, so head h of token slot s is one contiguous d-row.
 //
-// Bandwidth design: a CTA copies R whole token rows (R chosen so each thread
-// moves ~8-16 16-byte chunks); the owner request of each row is found once per
-// row (binary search over append_indptr) into shared memory, then all threads
-// stream 16-byte chunks with read-only loads.  Source rows are contiguous
-// ([Hkv][d] per token); each destination (head, slot) row is 2*d contiguous
-// bytes, so every warp writes whole 128-byte lines.
+// Bandwidth design: the (token row, K/V, head, 16-byte chunk) space is cut into
+// equal contiguous ranges, one per CTA, sized from the SM count so that small
+// appends (one token per request) still spread over every SM and large ones
+// give each thread ~16 chunks in flight.  The owner request of each row a CTA
+// touches is found once (binary search over append_indptr) into shared memory;
+// then all threads stream 16-byte chunks with read-only, no-allocate loads.
+// Source rows are contiguous ([Hkv][d] per token); each destination (head,
+// slot) row is 2*d contiguous bytes, so warps write whole 128-byte lines.
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -36,13 +38,17 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
                  uint4* __restrict__ pool, const int32_t* __restrict__ append_indptr,
                  const int32_t* __restrict__ page_indices, const int32_t* __restrict__ kv_indptr,
                  const int32_t* __restrict__ last_page_len, int batch, int nnz_new, int Hkv,
-                 int rows_per_cta, int64_t num_pages, int* err) {
+                 int chunks_per_cta, int64_t num_pages, int* err) {
   constexpr int P = 16;
   constexpr int CH = D / 8;  // 16-byte chunks per (head, slot) row
   __shared__ int64_t s_dst[kAppendMaxRows];  // chunk index of (page, K, head 0, slot, 0); -1 = skip
 
-  const int row0 = blockIdx.x * rows_per_cta;
-  const int nrows = min(rows_per_cta, nnz_new - row0);
+  const int per_row = 2 * Hkv * CH;
+  const int64_t total = (int64_t)nnz_new * per_row;
+  const int64_t first = (int64_t)blockIdx.x * chunks_per_cta;
+  const int64_t last = min(first + chunks_per_cta, total);
+  const int row0 = (int)(first / per_row);
+  const int nrows = (int)((last - 1) / per_row) - row0 + 1;
   if (threadIdx.x < nrows) {
     const int row = row0 + threadIdx.x;
     int lo = 0, hi = batch - 1;  // largest r with append_indptr[r] <= row
@@ -53,11 +59,11 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
     const int r = lo;
     const int a0 = __ldg(append_indptr + r), a1 = __ldg(append_indptr + r + 1);
     const int p0 = __ldg(kv_indptr + r), np = __ldg(kv_indptr + r + 1) - p0;
-    const int last = np > 0 ? __ldg(last_page_len + r) : 0;
-    const int64_t kv_len = np > 0 ? (int64_t)(np - 1) * P + last : 0;
+    const int last_len = np > 0 ? __ldg(last_page_len + r) : 0;
+    const int64_t kv_len = np > 0 ? (int64_t)(np - 1) * P + last_len : 0;
     const int n_new = a1 - a0;
     int64_t dst = -1;
-    if (row < a0 || row >= a1 || n_new > kv_len || (np > 0 && (last < 1 || last > P))) {
+    if (row < a0 || row >= a1 || n_new > kv_len || (np > 0 && (last_len < 1 || last_len > P))) {
       set_device_error(err, kDevErrShape);
     } else {
       const int64_t pos = kv_len - n_new + (row - a0);
@@ -73,25 +79,23 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
   __syncthreads();
 
   // flat chunk index i over (row, kv, head, c), c fastest
-  const int per_row = 2 * Hkv * CH;
-  const int total = nrows * per_row;
   constexpr int U = 4;
-  for (int base = threadIdx.x; base < total; base += kAppendThreads * U) {
+  for (int64_t base = first + threadIdx.x; base < last; base += kAppendThreads * U) {
     uint4 val[U];
     int64_t dst[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int i = base + u * kAppendThreads;
+      const int64_t i = base + (int64_t)u * kAppendThreads;
       dst[u] = -1;
-      if (i < total) {
-        const int rr = i / per_row;
-        const int rem = i - rr * per_row;
+      if (i < last) {
+        const int row = (int)(i / per_row);
+        const int rem = (int)(i - (int64_t)row * per_row);
         const int kv = rem / (Hkv * CH);
         const int hc = rem - kv * (Hkv * CH);  // h * CH + c
         const int h = hc / CH, c = hc - h * CH;
-        const int64_t d0 = s_dst[rr];
+        const int64_t d0 = s_dst[row - row0];
         if (d0 >= 0) {
-          const uint4* src = (kv == 0 ? k_new : v_new) + (int64_t)(row0 + rr) * Hkv * CH + hc;
+          const uint4* src = (kv == 0 ? k_new : v_new) + (int64_t)row * Hkv * CH + hc;
           val[u] = ld_stream(src);
           dst[u] = d0 + ((int64_t)kv * Hkv + h) * P * CH + c;
         }
@@ -108,21 +112,28 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* pool,
                              const int32_t* append_indptr, const int32_t* page_indices,
                              const int32_t* kv_indptr, const int32_t* last_page_len, int batch,
-                             int nnz_new, int Hkv, int head_dim, int64_t num_pages, int* err,
-                             cudaStream_t stream) {
+                             int nnz_new, int Hkv, int head_dim, int64_t num_pages, int num_sms,
+                             int* err, cudaStream_t stream) {
   if (nnz_new <= 0 || batch <= 0) return cudaSuccess;
-  const int per_row_chunks = 2 * Hkv * (head_dim / 8);
-  int rows = (kAppendThreads * 16) / per_row_chunks;
-  rows = rows < 1 ? 1 : (rows > kAppendMaxRows ? kAppendMaxRows : rows);
-  const int grid = (nnz_new + rows - 1) / rows;
+  const int per_row = 2 * Hkv * (head_dim / 8);
+  const int64_t total = (int64_t)nnz_new * per_row;
+  // ~4 CTAs per SM for small appends, up to 16 chunks per thread for large ones,
+  // and never more rows per CTA than the shared row table holds
+  int64_t cpc = (total + (int64_t)num_sms * 4 - 1) / ((int64_t)num_sms * 4);
+  cpc = ((cpc + kAppendThreads - 1) / kAppendThreads) * kAppendThreads;
+  cpc = cpc < kAppendThreads ? kAppendThreads : (cpc > 16 * kAppendThreads ? 16 * kAppendThreads : cpc);
+  const int64_t max_cpc = (int64_t)(kAppendMaxRows - 1) * per_row;
+  if (cpc > max_cpc) cpc = max_cpc;
+  const int64_t grid = (total + cpc - 1) / cpc;
+  if (grid > INT32_MAX) return cudaErrorInvalidValue;
   if (head_dim == 128) {
-    kv_append_kernel<128><<<grid, kAppendThreads, 0, stream>>>(
+    kv_append_kernel<128><<<(unsigned)grid, kAppendThreads, 0, stream>>>(
         (const uint4*)k_new, (const uint4*)v_new, (uint4*)pool, append_indptr, page_indices,
-        kv_indptr, last_page_len, batch, nnz_new, Hkv, rows, num_pages, err);
+        kv_indptr, last_page_len, batch, nnz_new, Hkv, (int)cpc, num_pages, err);
   } else {
-    kv_append_kernel<64><<<grid, kAppendThreads, 0, stream>>>(
+    kv_append_kernel<64><<<(unsigned)grid, kAppendThreads, 0, stream>>>(
         (const uint4*)k_new, (const uint4*)v_new, (uint4*)pool, append_indptr, page_indices,
-        kv_indptr, last_page_len, batch, nnz_new, Hkv, rows, num_pages, err);
+        kv_indptr, last_page_len, batch, nnz_new, Hkv, (int)cpc, num_pages, err);
   }
   return cudaGetLastError();
 }

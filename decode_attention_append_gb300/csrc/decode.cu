@@ -12,16 +12,18 @@
 //     stages; each stage holds one page's K slice and V slice for this kv head
 //     (2 x page_size x d bf16, contiguous in HND), filled by two 1-D TMA bulk
 //     copies issued by one lane and tracked by an mbarrier;
-//   - the NWH warps of a group split the G query heads (4 per warp), so one
+//   - the NWH warps of a group split the G query heads (HPW per warp), so one
 //     page read from HBM serves every query head of its group (GQA packing);
 //   - NPG page groups per CTA take pages round-robin and keep separate
 //     online-softmax states, merged in shared memory at the end.
 // Inside a warp, 16 lanes cover one token's d-vector (8 dims each for d=128)
 // and the two half-warps take alternate tokens.  q.k partial sums are reduced
 // across the 16 lanes with a reduce-scatter of warp shuffles (each level halves
-// the values a lane holds), so a page of 16 tokens x 4 heads costs 30
-// shuffles per lane instead of 128.  Scores live in the log2 domain (q is
-// pre-scaled by sm_scale * log2 e).
+// the values a lane holds); it leaves every lane owning whole scores of one
+// token for HPW/2 heads, so the online-softmax update (max, exp2, sum) runs in
+// all lanes at once with 4-level shuffle reductions over the page's tokens.
+// Scores live in the log2 domain (q is pre-scaled by sm_scale * log2 e).  The
+// FMAs are packed two-wide (sm_100 FFMA2).
 #include <cfloat>
 
 #include "launch.h"
@@ -34,21 +36,21 @@ constexpr int kP = 16;
 
 template <int D, int G>
 struct DecodeShape {
-  static constexpr int HPW = G >= 4 ? 4 : G;          // query heads per warp
+  static constexpr int HPW = G >= 16 ? 8 : (G >= 12 ? 6 : (G >= 4 ? 4 : G));  // heads per warp
   static constexpr int NWH = (G + HPW - 1) / HPW;     // warps sharing a page
   static constexpr int NPG = NWH >= 4 ? 1 : 4 / NWH;  // page groups per CTA
   static constexpr int NWARPS = NWH * NPG;
   static constexpr int THREADS = 32 * NWARPS;
   static constexpr int DPL = D / 16;                  // dims per lane
+  static constexpr int DP2 = DPL / 2;                 // float2 pairs per lane
   static constexpr int ITERS = kP / 2;                // two tokens per warp step
   static constexpr int SLICE = kP * D * 2;            // bytes of one head's K (or V) page slice
   static constexpr int STAGE = 2 * SLICE;
-  static constexpr int NSTAGE = NPG >= 4 ? 3 : (NPG == 2 ? 4 : 6);
+  static constexpr int NSTAGE = NPG >= 4 ? 3 : (NPG == 2 ? 4 : (NWH >= 2 ? 5 : 6));
   static constexpr int RING = NPG * NSTAGE * STAGE;
   static constexpr int NRED = ITERS * HPW;            // partial dots per lane per page
-  static constexpr int NF = NRED >= 16 ? NRED / 16 : 1;
-  static constexpr int SH = NRED >= 16 ? 0 : 1;       // NRED == 8 when HPW == 1
-  static_assert(NRED >= 8, "reduce-scatter layout");
+  static constexpr int NF = HPW >= 2 ? HPW / 2 : 1;   // scores a lane owns after the reduce
+  static_assert(HPW == 1 || HPW % 2 == 0, "heads per warp");
   static constexpr int MERGE_BYTES = NPG * G * (D + 2) * 4;
   static constexpr int BODY = RING > MERGE_BYTES ? RING : MERGE_BYTES;
   static constexpr int BARS = 2 * NPG * NSTAGE * 8;
@@ -59,7 +61,7 @@ struct DecodeShape {
 
 // Reduce-scatter over the 16 lanes of a half-warp: on entry every lane holds N
 // partial sums; on exit lane li holds the full sums of entries
-// [(li >> SH) * NF, (li >> SH) * NF + NF) in v[0 .. NF).
+// [li * N/16, li * N/16 + N/16) (N >= 16), or of entry li >> 1 (N == 8).
 template <int N, int M>
 __device__ __forceinline__ void reduce_scatter16(float* v, int li) {
   if constexpr (M > 0) {
@@ -81,18 +83,19 @@ __device__ __forceinline__ void reduce_scatter16(float* v, int li) {
   }
 }
 
+// One row slice of DPL bf16 values -> DPL/2 float2 pairs (exact widening).
 template <int DPL>
-__device__ __forceinline__ void load_row_f32(const uint8_t* p, float (&f)[DPL]) {
+__device__ __forceinline__ void load_row_f2(const uint8_t* p, float2 (&f)[DPL / 2]) {
   if constexpr (DPL == 8) {
     const uint4 w = *reinterpret_cast<const uint4*>(p);
-    f[0] = bf16lo_to_f32(w.x); f[1] = bf16hi_to_f32(w.x);
-    f[2] = bf16lo_to_f32(w.y); f[3] = bf16hi_to_f32(w.y);
-    f[4] = bf16lo_to_f32(w.z); f[5] = bf16hi_to_f32(w.z);
-    f[6] = bf16lo_to_f32(w.w); f[7] = bf16hi_to_f32(w.w);
+    f[0] = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
+    f[1] = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
+    f[2] = make_float2(bf16lo_to_f32(w.z), bf16hi_to_f32(w.z));
+    f[3] = make_float2(bf16lo_to_f32(w.w), bf16hi_to_f32(w.w));
   } else {
     const uint2 w = *reinterpret_cast<const uint2*>(p);
-    f[0] = bf16lo_to_f32(w.x); f[1] = bf16hi_to_f32(w.x);
-    f[2] = bf16lo_to_f32(w.y); f[3] = bf16hi_to_f32(w.y);
+    f[0] = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
+    f[1] = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
   }
 }
 
@@ -161,7 +164,7 @@ decode_splitkv_kernel(const DecodeArgs a) {
   }
 
   // q rows of this warp's heads, scaled into the log2 domain
-  float qr[S::HPW][S::DPL];
+  float2 q2[S::HPW][S::DP2];
 #pragma unroll
   for (int j = 0; j < S::HPW; ++j) {
     const int hg = hb + j;
@@ -169,22 +172,34 @@ decode_splitkv_kernel(const DecodeArgs a) {
       const int hq = kvh * a.group + hg;
       const uint8_t* qp = reinterpret_cast<const uint8_t*>(
           a.q + ((int64_t)u.q_row * a.Hq + hq) * D + li * S::DPL);
-      float f[S::DPL];
-      load_row_f32<S::DPL>(qp, f);
+      float2 f[S::DP2];
+      load_row_f2<S::DPL>(qp, f);
 #pragma unroll
-      for (int c = 0; c < S::DPL; ++c) qr[j][c] = f[c] * a.sm_scale_log2;
+      for (int c = 0; c < S::DP2; ++c)
+        q2[j][c] = make_float2(f[c].x * a.sm_scale_log2, f[c].y * a.sm_scale_log2);
     } else {
 #pragma unroll
-      for (int c = 0; c < S::DPL; ++c) qr[j][c] = 0.f;
+      for (int c = 0; c < S::DP2; ++c) q2[j][c] = make_float2(0.f, 0.f);
     }
   }
 
-  float o[S::HPW][S::DPL];
+  float2 o2[S::HPW][S::DP2];
 #pragma unroll
   for (int j = 0; j < S::HPW; ++j)
 #pragma unroll
-    for (int c = 0; c < S::DPL; ++c) o[j][c] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;  // meaningful in lanes j < HPW for head hb + j
+    for (int c = 0; c < S::DP2; ++c) o2[j][c] = make_float2(0.f, 0.f);
+
+  // online-softmax state of the NF heads this lane owns after the reduce:
+  // token t_own of each page, heads hj(f) = (li & 1) * NF + f (head 0 if HPW == 1)
+  float m_run[S::NF], l_run[S::NF];
+#pragma unroll
+  for (int f = 0; f < S::NF; ++f) {
+    m_run[f] = -INFINITY;
+    l_run[f] = 0.f;
+  }
+  const int t_own = 2 * (li >> 1) + half;
+  const int hj0 = S::HPW == 1 ? 0 : (li & 1) * S::NF;
+  const bool writer = S::HPW > 1 || (li & 1) == 0;
 
   float* sw = s_scores + warp * kP * S::HPW;
   float* aw = s_alpha + warp * S::HPW;
@@ -203,42 +218,43 @@ decode_splitkv_kernel(const DecodeArgs a) {
 #pragma unroll
     for (int it = 0; it < S::ITERS; ++it) {
       const int t = 2 * it + half;
-      float kf[S::DPL];
-      load_row_f32<S::DPL>(kbuf + (t * D + li * S::DPL) * 2, kf);
+      float2 kf[S::DP2];
+      load_row_f2<S::DPL>(kbuf + (t * D + li * S::DPL) * 2, kf);
 #pragma unroll
       for (int j = 0; j < S::HPW; ++j) {
-        float acc = 0.f;
+        float2 acc = __fmul2_rn(q2[j][0], kf[0]);
 #pragma unroll
-        for (int c = 0; c < S::DPL; ++c) acc = fmaf(qr[j][c], kf[c], acc);
-        part[it * S::HPW + j] = acc;
+        for (int c = 1; c < S::DP2; ++c) acc = __ffma2_rn(q2[j][c], kf[c], acc);
+        part[it * S::HPW + j] = acc.x + acc.y;
       }
     }
     reduce_scatter16<S::NRED, 8>(part, li);
-    if ((li & ((1 << S::SH) - 1)) == 0) {
-#pragma unroll
-      for (int f = 0; f < S::NF; ++f) {
-        const int flat = (li >> S::SH) * S::NF + f;
-        const int it = flat / S::HPW, j = flat - it * S::HPW;
-        sw[(2 * it + half) * S::HPW + j] = part[f];
-      }
-    }
-    __syncwarp();
 
-    // ---- online softmax update, one lane per head
-    if (lane < S::HPW) {
-      float mx = -INFINITY;
-      for (int t = 0; t < valid; ++t) mx = fmaxf(mx, sw[t * S::HPW + lane]);
-      const float m_new = fmaxf(m_run, mx);
-      const float alpha = ex2_approx(m_run - m_new);
-      float sum = 0.f;
-      for (int t = 0; t < kP; ++t) {
-        const float p = t < valid ? ex2_approx(sw[t * S::HPW + lane] - m_new) : 0.f;
-        sw[t * S::HPW + lane] = p;
-        sum += p;
+    // ---- online softmax over this page's tokens, all lanes at once
+    const bool tok_ok = t_own < valid;
+    float p[S::NF], alpha[S::NF];
+#pragma unroll
+    for (int f = 0; f < S::NF; ++f) {
+      const float s = tok_ok ? part[f] : -INFINITY;
+      float mx = s;
+#pragma unroll
+      for (int msk = 2; msk <= 16; msk <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
+      const float m_new = fmaxf(m_run[f], mx);
+      alpha[f] = ex2_approx(m_run[f] - m_new);
+      p[f] = ex2_approx(s - m_new);
+      float sum = p[f];
+#pragma unroll
+      for (int msk = 2; msk <= 16; msk <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, msk);
+      l_run[f] = l_run[f] * alpha[f] + sum;
+      m_run[f] = m_new;
+    }
+    if (writer) {
+#pragma unroll
+      for (int f = 0; f < S::NF; ++f) sw[t_own * S::HPW + hj0 + f] = p[f];
+      if (half == 0 && li < 2) {
+#pragma unroll
+        for (int f = 0; f < S::NF; ++f) aw[hj0 + f] = alpha[f];
       }
-      l_run = l_run * alpha + sum;
-      m_run = m_new;
-      aw[lane] = alpha;
     }
     __syncwarp();
 
@@ -246,20 +262,22 @@ decode_splitkv_kernel(const DecodeArgs a) {
 #pragma unroll
     for (int j = 0; j < S::HPW; ++j) {
       const float al = aw[j];
+      const float2 al2 = make_float2(al, al);
 #pragma unroll
-      for (int c = 0; c < S::DPL; ++c) o[j][c] *= al;
+      for (int c = 0; c < S::DP2; ++c) o2[j][c] = __fmul2_rn(o2[j][c], al2);
     }
 #pragma unroll
     for (int it = 0; it < S::ITERS; ++it) {
       const int t = 2 * it + half;
       if (t < valid) {
-        float vf[S::DPL];
-        load_row_f32<S::DPL>(vbuf + (t * D + li * S::DPL) * 2, vf);
+        float2 vf[S::DP2];
+        load_row_f2<S::DPL>(vbuf + (t * D + li * S::DPL) * 2, vf);
 #pragma unroll
         for (int j = 0; j < S::HPW; ++j) {
-          const float p = sw[t * S::HPW + j];
+          const float pj = sw[t * S::HPW + j];
+          const float2 p2 = make_float2(pj, pj);
 #pragma unroll
-          for (int c = 0; c < S::DPL; ++c) o[j][c] = fmaf(p, vf[c], o[j][c]);
+          for (int c = 0; c < S::DP2; ++c) o2[j][c] = __ffma2_rn(p2, vf[c], o2[j][c]);
         }
       }
     }
@@ -275,7 +293,10 @@ decode_splitkv_kernel(const DecodeArgs a) {
 #pragma unroll
   for (int j = 0; j < S::HPW; ++j)
 #pragma unroll
-    for (int c = 0; c < S::DPL; ++c) o[j][c] += __shfl_xor_sync(0xffffffffu, o[j][c], 16);
+    for (int c = 0; c < S::DP2; ++c) {
+      o2[j][c].x += __shfl_xor_sync(0xffffffffu, o2[j][c].x, 16);
+      o2[j][c].y += __shfl_xor_sync(0xffffffffu, o2[j][c].y, 16);
+    }
 
   __syncthreads();  // ring is free: reuse it for the merge
   float* mo = reinterpret_cast<float*>(ring);   // [NPG][G][D]
@@ -287,13 +308,22 @@ decode_splitkv_kernel(const DecodeArgs a) {
       const int hg = hb + j;
       if (hg < G) {
 #pragma unroll
-        for (int c = 0; c < S::DPL; ++c) mo[(grp * G + hg) * D + li * S::DPL + c] = o[j][c];
+        for (int c = 0; c < S::DP2; ++c) {
+          mo[(grp * G + hg) * D + li * S::DPL + 2 * c] = o2[j][c].x;
+          mo[(grp * G + hg) * D + li * S::DPL + 2 * c + 1] = o2[j][c].y;
+        }
       }
     }
-  }
-  if (lane < S::HPW && hb + lane < G) {
-    mm[grp * G + hb + lane] = m_run;
-    ml[grp * G + hb + lane] = l_run;
+    if (li < 2 && writer) {
+#pragma unroll
+      for (int f = 0; f < S::NF; ++f) {
+        const int hg = hb + hj0 + f;
+        if (hg < G) {
+          mm[grp * G + hg] = m_run[f];
+          ml[grp * G + hg] = l_run[f];
+        }
+      }
+    }
   }
   __syncthreads();
 

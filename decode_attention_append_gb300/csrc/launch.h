@@ -13,8 +13,8 @@ int* device_error_word();
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* pool,
                              const int32_t* append_indptr, const int32_t* page_indices,
                              const int32_t* kv_indptr, const int32_t* last_page_len, int batch,
-                             int nnz_new, int Hkv, int head_dim, int64_t num_pages, int* err,
-                             cudaStream_t stream);
+                             int nnz_new, int Hkv, int head_dim, int64_t num_pages, int num_sms,
+                             int* err, cudaStream_t stream);
 
 struct DecodeArgs {
   const uint16_t* q;            // [nnz_qo][Hq][d]
