@@ -341,6 +341,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="mha_decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="profiling runs: timed steps only (no clock window, no traced or e2e pass)")
     ap.add_argument("--compact-pool", action="store_true",
                     help="renumber pages densely so the pool holds only the pages used "
                          "(same work; smaller device footprint for profiler captures)")
@@ -422,28 +424,33 @@ def main():
     # nvidia-smi (100 ms period) over a window of back-to-back identical steps
     # that contains the timed region: ~1 s of steps before it, ~0.5 s after.
     clocks = ClockSampler(local)
-    clocks.start()
-    soak(g.step, 1.0)
+    if not args.quick:
+        clocks.start()
+        soak(g.step, 1.0)
     barrier()
     ms = timed(g.step, args.steps, flush)
     barrier()
     # ---- per-kernel roofline pass: CUDA events around each launch
-    daa.trace_enable(8 * args.steps + 64)
-    ms_traced = timed(g.step, args.steps, flush)
-    recs = daa.trace_read()
-    daa.trace_disable()
-    barrier()
-    soak(g.step, 0.5)
-    clk = clocks.stop()
+    recs, clk = [], None
+    if not args.quick:
+        daa.trace_enable(8 * args.steps + 64)
+        timed(g.step, args.steps, flush)
+        recs = daa.trace_read()
+        daa.trace_disable()
+        barrier()
+        soak(g.step, 0.5)
+        clk = clocks.stop()
     if clk is not None:
         clk["window"] = "nvidia-smi samples over back-to-back steps around the timed region"
 
     # ---- e2e: host buffers through the public API
-    for _ in range(2):
-        g.step_e2e(torch.cuda.current_stream())
-    barrier()
-    ms_e2e = timed(lambda: g.step_e2e(torch.cuda.current_stream()), args.steps, flush)
-    barrier()
+    ms_e2e = float("nan")
+    if not args.quick:
+        for _ in range(2):
+            g.step_e2e(torch.cuda.current_stream())
+        barrier()
+        ms_e2e = timed(lambda: g.step_e2e(torch.cuda.current_stream()), args.steps, flush)
+        barrier()
     h2d, d2h = g.e2e_bytes()
     err = daa.device_error(reset=True)
 
@@ -502,7 +509,7 @@ def main():
     if "decode_splitkv" in per_kernel and acc["decode_bytes"]:
         dm = float(np.mean(per_kernel["decode_splitkv"]))
         line["decode_gbs"] = acc["decode_bytes"] / (dm * 1e-3) / 1e9
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
         line["cpu_baseline"] = cpu_baseline(wl)
     print(json.dumps(line), flush=True)
     if dist is not None:

@@ -144,7 +144,8 @@ daa_status make_plan(const int32_t* qo, const int32_t* kv, const int32_t* last, 
   pl.units = std::move(full_units);
   pl.units.insert(pl.units.end(), tail_units.begin(), tail_units.end());
 
-  // prefill tiles: ntok * g <= 128 packed rows each, longest key range first
+  // prefill tiles: pairs of 128-row tiles (ntok * g <= 128 packed rows each;
+  // the second tile's tokens in pad0), longest key range first
   const int tpt = kPrefillTileRows / g;
   std::vector<std::pair<int, PrefillTile>> tw;
   for (int r = 0; r < batch; ++r) {
@@ -152,7 +153,7 @@ daa_status make_plan(const int32_t* qo, const int32_t* kv, const int32_t* last, 
     if (nq < 2) continue;
     const int np = kv[r + 1] - kv[r];
     const int kv_len = (np - 1) * P + last[r];
-    for (int t0 = 0; t0 < nq; t0 += tpt) {
+    for (int t0 = 0; t0 < nq; t0 += 2 * tpt) {
       PrefillTile t{};
       t.q_row0 = qo[r];
       t.qo_len = nq;
@@ -160,7 +161,8 @@ daa_status make_plan(const int32_t* qo, const int32_t* kv, const int32_t* last, 
       t.page_base = kv[r];
       t.tok0 = t0;
       t.ntok = std::min(tpt, nq - t0);
-      const int keys = std::min(kv_len, kv_len - nq + t0 + t.ntok);
+      t.pad0 = t.ntok == tpt ? std::max(0, std::min(tpt, nq - t0 - tpt)) : 0;  // second tile
+      const int keys = std::min(kv_len, kv_len - nq + t0 + t.ntok + t.pad0);
       tw.emplace_back(keys, t);
     }
   }

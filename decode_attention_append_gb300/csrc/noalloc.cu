@@ -80,7 +80,7 @@ struct Counts {
 
 // The same split of the work as daa_batch_attention (decode splits of
 // max(16, min(1024, ceil(page_heads / (40 * SMs)))) pages; 128-row prefill
-// tiles), written into the static buffers.  Unit and tile order do not affect
+// tiles, paired two per CTA), written into the static buffers.  Unit and tile order do not affect
 // any result.
 daa_status plan_fixed(const int32_t* qo, const int32_t* kv, const int32_t* last, int32_t batch,
                       const daa_dims& d, int sms, Counts& c) {
@@ -141,7 +141,7 @@ daa_status plan_fixed(const int32_t* qo, const int32_t* kv, const int32_t* last,
     if (nq < 2) continue;
     const int np = kv[r + 1] - kv[r];
     const int kv_len = (np - 1) * P + last[r];
-    for (int t0 = 0; t0 < nq; t0 += tpt) {
+    for (int t0 = 0; t0 < nq; t0 += 2 * tpt) {
       if (nt >= kMaxTiles) return DAA_ERR_WORKSPACE;
       PrefillTile t{};
       t.q_row0 = qo[r];
@@ -150,7 +150,8 @@ daa_status plan_fixed(const int32_t* qo, const int32_t* kv, const int32_t* last,
       t.page_base = kv[r];
       t.tok0 = t0;
       t.ntok = std::min(tpt, nq - t0);
-      g_tile_keys[nt] = std::min(kv_len, kv_len - nq + t0 + t.ntok);
+      t.pad0 = t.ntok == tpt ? std::max(0, std::min(tpt, nq - t0 - tpt)) : 0;  // second tile
+      g_tile_keys[nt] = std::min(kv_len, kv_len - nq + t0 + t.ntok + t.pad0);
       g_order[nt] = nt;
       g_tiles[nt++] = t;
     }

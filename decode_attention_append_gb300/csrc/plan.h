@@ -26,18 +26,20 @@ struct MergeItem {
   int32_t pad;
 };
 
-// One tile of packed query rows of one prefill request (qo_len > 1): new
-// tokens [tok0, tok0 + ntok) of the request, each with all g query heads of a
-// kv head, packed token-major into ntok * g <= 128 rows.  One CTA per
-// (tile, kv head).
+// One or two tiles of packed query rows of one prefill request (qo_len > 1):
+// tile 0 holds new tokens [tok0, tok0 + ntok) of the request, tile 1 (if pad0
+// > 0) the next pad0 tokens; each token brings all g query heads of a kv head,
+// packed token-major into ntok * g <= 128 rows per tile.  One CTA per
+// (tile pair, kv head); both tiles share every K/V tile the CTA loads.
 struct PrefillTile {
   int32_t q_row0;     // row of the request's first new token
   int32_t qo_len;
   int32_t kv_len;
   int32_t page_base;
   int32_t tok0;       // first new-token index (0-based within the request)
-  int32_t ntok;       // tokens in this tile
-  int32_t pad0, pad1;
+  int32_t ntok;       // tokens in tile 0
+  int32_t pad0;       // tokens in tile 1 (0: no second tile)
+  int32_t pad1;
 };
 
 static_assert(sizeof(DecodeUnit) == 32, "DecodeUnit layout");

@@ -1,5 +1,5 @@
 // Prefill-chunk attention (qo_len > 1, causal with a cache offset) on the
-// sm_103a tensor cores (tcgen05 + tensor memory).
+// sm_103a tensor cores (tcgen05 + tensor memory), warp specialised.
 //
 // "Chunked prefill" (k4i.top), #correctness: new token i of a chunk sits at
 // absolute position kv_len - qo_len + i and attends to every key j <= that
@@ -10,16 +10,25 @@
 // HND, so one (page, head) K or V slice is a contiguous [page_size][d] block,
 // which a 3-D tensor map over the pool fetches as one TMA box per 64 columns.
 //
-// CTA = one PrefillTile x one kv head, 128 threads.  The tile packs the g query
-// heads of the kv head token-major into M = 128 rows (row = token * g + head),
-// so every K/V tile loaded from HBM serves all g query heads (GQA packing).
-// Per 128-key tile kt:
-//   S = Q K^T          tcgen05.mma M=128 N=128 K=16 x (d/16), S in TMEM
-//   P = exp2(S*scale - m) per row (thread = row = TMEM lane), P bf16 -> smem
-//   O += P V           tcgen05.mma M=128 N=d K=16 x 8, O in TMEM
-// The running max is raised lazily (only when it grows by more than 2^8), and
-// O is rescaled in TMEM only then.  Thread 0 issues TMA and MMAs; K/V tiles
-// are double buffered so the next tile's pages stream in during this tile.
+// CTA = a pair of 128-row Q tiles of one request and one kv head (the second
+// tile may be absent).  Each tile packs the g query heads of the kv head
+// token-major into M = 128 rows (row = token * g + head), so every K/V tile
+// loaded from HBM serves 2 x 128 query rows.  Warp roles:
+//   warps 0-3 / 4-7  softmax of Q tile 0 / 1 (thread = row = TMEM lane)
+//   warp 8           TMA producer: Q tiles, then K_0, V_0, K_1, V_1, ... into a
+//                    ring of RS shared-memory stages (one 128-key tile each)
+//   warp 9           MMA issuer (one lane)
+// Tensor memory (512 columns): S_q / P_q at q*128, O_q at 256 + q*128.
+//   S_q = Q_q K_j^T      A = Q (smem), B = K (smem), fp32 S in TMEM
+//   P_q (bf16) overwrites the first 64 columns of S_q (softmax, tcgen05.st)
+//   O_q += P_q V_j       A = P (TMEM), B = V (smem, MN-major), fp32 O in TMEM
+// Per key tile the MMA warp issues PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): S_q(j+1)
+// follows PV_q(j) in the tensor pipe, which reads P_q(j) from the columns
+// S_q(j+1) overwrites; the other tile's softmax runs meanwhile (ping-pong).
+// Softmax keeps a lazily raised running max (raised only when it grows by
+// more than 2^8) and rescales O in TMEM only then.  V rows past the request's
+// last key (stale slots, or pages not loaded) are zeroed by the producer
+// before the last PV so they cannot poison it.
 #include <cuda.h>
 
 #include "launch.h"
@@ -32,7 +41,10 @@ constexpr int kP = 16;
 constexpr int kRows = kPrefillTileRows;  // 128
 constexpr int kKeys = 128;               // keys per K/V tile (8 pages)
 constexpr int kPagesPerTile = kKeys / kP;
-constexpr int kThreads = 128;
+constexpr int kNumWarps = 10;
+constexpr int kThreads = 32 * kNumWarps;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 domain
 
 struct __align__(64) PrefillParams {
@@ -42,23 +54,21 @@ struct __align__(64) PrefillParams {
 };
 
 template <int D>
-struct PrefillSmem {
+struct Smem {
   static constexpr int KB = D / 64;                 // 64-column (128-byte) blocks per row
-  static constexpr int Q_BYTES = kRows * D * 2;     // 128 rows
+  static constexpr int Q_BYTES = kRows * D * 2;
   static constexpr int T_BYTES = kKeys * D * 2;     // one K or V tile
-  static constexpr int P_BYTES = kRows * kKeys * 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K0 = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V0 = OFF_K0 + T_BYTES;
-  static constexpr int OFF_K1 = OFF_V0 + T_BYTES;
-  static constexpr int OFF_V1 = OFF_K1 + T_BYTES;
-  static constexpr int OFF_P = OFF_V1 + T_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  static constexpr int NBAR = 8;
+  static constexpr int RS = D == 128 ? 5 : 8;       // ring stages
+  static constexpr int OFF_Q = 0;                   // [2]
+  static constexpr int OFF_RING = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + RS * T_BYTES;
+  // barriers: q_full, ring_full[RS], ring_empty[RS], s_full[2], p_full[2],
+  // o_done[2], v_clean
+  static constexpr int NBAR = 1 + 2 * RS + 6 + 1;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_TMEM + 16;
   static constexpr int ALLOC = BYTES + 1024;        // slack to align the base to 1024
-  static constexpr int TMEM_COLS = 256;             // S: [0,128)  O: [128, 128+D)
+  static constexpr int TMEM_COLS = 512;
 };
 
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t addr) {
@@ -74,264 +84,277 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t addr, uint32_t lbo) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
-  using L = PrefillSmem<D>;
+  using L = Smem<D>;
+  constexpr int RS = L::RS;
   const PrefillArgs& a = prm.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-  uint64_t* q_bar = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_bar = bars + 5;
-  uint64_t* o_bar = bars + 6;
+  uint64_t* q_full = bars;
+  uint64_t* ring_full = bars + 1;
+  uint64_t* ring_empty = ring_full + RS;
+  uint64_t* s_full = ring_empty + RS;  // [2]
+  uint64_t* p_full = s_full + 2;       // [2]
+  uint64_t* o_done = p_full + 2;       // [2]
+  uint64_t* v_clean = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
 
   const PrefillTile tile = a.tiles[blockIdx.x];
   const int kvh = blockIdx.y;
   const int g = a.group;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int rows_valid = tile.ntok * g;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nq = tile.pad0 > 0 ? 2 : 1;  // Q tiles in this CTA (pad0 = tokens of tile 1)
 
-  // key range this tile needs
+  // keys [0, kv_end) are read; causal rows mask beyond their own position
   const int pos_first = tile.kv_len - tile.qo_len + tile.tok0;
-  const int pos_last = pos_first + tile.ntok - 1;
-  const int kv_end = a.causal ? min(tile.kv_len, pos_last + 1) : tile.kv_len;
+  const int ntok_all = tile.ntok + tile.pad0;
+  const int kv_end = a.causal ? min(tile.kv_len, pos_first + ntok_all) : tile.kv_len;
   const int n_kt = (kv_end + kKeys - 1) / kKeys;
   const int npages_req = (tile.kv_len + kP - 1) / kP;
+  const bool last_partial = tile.kv_len - (n_kt - 1) * kKeys < kKeys;
 
   if (tid == 0) {
     prefetch_tmap(&prm.tmap_q);
     prefetch_tmap(&prm.tmap_kv);
-    mbar_init(q_bar, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+    mbar_init(q_full, 1);
+    for (int i = 0; i < RS; ++i) {
+      mbar_init(&ring_full[i], 1);
+      mbar_init(&ring_empty[i], 1);
     }
-    mbar_init(s_bar, 1);
-    mbar_init(o_bar, 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&s_full[q], 1);
+      mbar_init(&p_full[q], 4);
+      mbar_init(&o_done[q], 1);
+    }
+    mbar_init(v_clean, 1);
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tmem_relinquish();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem;
-  const uint32_t tmem_o = tmem + 128;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 
-  const uint32_t sQ = smem_u32(smem + L::OFF_Q);
-  const uint32_t sK[2] = {smem_u32(smem + L::OFF_K0), smem_u32(smem + L::OFF_K1)};
-  const uint32_t sV[2] = {smem_u32(smem + L::OFF_V0), smem_u32(smem + L::OFF_V1)};
-  const uint32_t sP = smem_u32(smem + L::OFF_P);
-  uint8_t* kbuf[2] = {smem + L::OFF_K0, smem + L::OFF_K1};
-  uint8_t* vbuf[2] = {smem + L::OFF_V0, smem + L::OFF_V1};
-
-  // ---- producer helpers (thread 0 only)
-  auto load_kv = [&](int kt, int st) {
-    const int pg0 = kt * kPagesPerTile;
-    int np = npages_req - pg0;
-    np = np > kPagesPerTile ? kPagesPerTile : np;
-    mbar_arrive_expect_tx(&kv_full[st], (uint32_t)(np * 2 * kP * D * 2));
-    for (int i = 0; i < np; ++i) {
-      int64_t page = a.page_indices[tile.page_base + pg0 + i];
-      if (page < 0 || page >= a.num_pages) {
-        set_device_error(a.err, kDevErrPageRange);
-        page = 0;  // fetch a valid page instead; the output is undefined anyway
-      }
-      const int32_t kslice = (int32_t)((page * 2 + 0) * a.Hkv + kvh);
-      const int32_t vslice = (int32_t)((page * 2 + 1) * a.Hkv + kvh);
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const int tpt = kRows / g;
+      mbar_arrive_expect_tx(q_full, (uint32_t)(nq * tpt * g * D * 2));
+      for (int q = 0; q < nq; ++q)
+        for (int b = 0; b < L::KB; ++b)
+          tma_load_3d(smem + L::OFF_Q + q * L::Q_BYTES + b * (kRows * 128), &prm.tmap_q, b * 64,
+                      kvh * g, tile.q_row0 + tile.tok0 + q * tile.ntok, q_full);
+      for (int i = 0; i < 2 * n_kt; ++i) {
+        const int st = i % RS;
+        const int j = i >> 1;
+        const int pg0 = j * kPagesPerTile;
+        const int np = min(kPagesPerTile, npages_req - pg0);
+        uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
+        if (i >= RS) mbar_wait(&ring_empty[st], ((i / RS) - 1) & 1, a.err);
+        mbar_arrive_expect_tx(&ring_full[st], (uint32_t)(np * kP * D * 2));
+        for (int pgi = 0; pgi < np; ++pgi) {
+          int64_t page = a.page_indices[tile.page_base + pg0 + pgi];
+          if (page < 0 || page >= a.num_pages) {
+            set_device_error(a.err, kDevErrPageRange);
+            page = 0;  // fetch a valid page instead; the output is undefined anyway
+          }
+          const int32_t slice = (int32_t)((page * 2 + (i & 1)) * a.Hkv + kvh);
 #pragma unroll
-      for (int b = 0; b < L::KB; ++b) {
-        tma_load_3d(kbuf[st] + b * (kKeys * 128) + i * (kP * 128), &prm.tmap_kv, b * 64, 0, kslice,
-                    &kv_full[st]);
-        tma_load_3d(vbuf[st] + b * (kKeys * 128) + i * (kP * 128), &prm.tmap_kv, b * 64, 0, vslice,
-                    &kv_full[st]);
-      }
-    }
-  };
-  auto issue_s = [&](int st) {
-    constexpr uint32_t idesc = idesc_bf16_f32(kRows, kKeys, 0, 0);
-#pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
-      const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
-      const uint32_t koff = (k >> 2) * (kKeys * 128) + (k & 3) * 32;
-      tc_mma_ss(tmem_s, desc_kmajor(sQ + off), desc_kmajor(sK[st] + koff), idesc, k > 0 ? 1u : 0u);
-    }
-    tc_commit(s_bar);
-  };
-  auto issue_pv = [&](int st, int kt) {
-    constexpr uint32_t idesc = idesc_bf16_f32(kRows, D, 0, 1);
-#pragma unroll
-    for (int k = 0; k < kKeys / 16; ++k) {
-      const uint32_t poff = (k >> 2) * (kRows * 128) + (k & 3) * 32;
-      const uint32_t voff = k * (16 * 128);
-      tc_mma_ss(tmem_o, desc_kmajor(sP + poff), desc_mnmajor(sV[st] + voff, kKeys * 128), idesc,
-                (kt > 0 || k > 0) ? 1u : 0u);
-    }
-    tc_commit(o_bar);
-    tc_commit(&kv_empty[st]);
-  };
-
-  if (tid == 0) {
-    const int d_blocks = L::KB;
-    mbar_arrive_expect_tx(q_bar, (uint32_t)(rows_valid > 0 ? (kRows / g) * g * D * 2 : 0));
-    for (int b = 0; b < d_blocks; ++b)
-      tma_load_3d(smem + L::OFF_Q + b * (kRows * 128), &prm.tmap_q, b * 64, kvh * g,
-                  tile.q_row0 + tile.tok0, q_bar);
-    load_kv(0, 0);
-    if (n_kt > 1) load_kv(1, 1);
-    mbar_wait(q_bar, 0, a.err);
-    mbar_wait(&kv_full[0], 0, a.err);
-    tc_fence_after();
-    issue_s(0);
-  }
-
-  // ---- per-row softmax state (thread = row)
-  const int row = tid;
-  const int tl = row / g;
-  const bool row_ok = row < rows_valid;
-  const int qpos = pos_first + tl;  // absolute position of this row's token
-  const int row_end = a.causal ? min(qpos + 1, tile.kv_len) : tile.kv_len;  // keys j < row_end
-  float m_run = -INFINITY, l_run = 0.f;
-  const float sc = a.sm_scale_log2;
-
-  for (int kt = 0; kt < n_kt; ++kt) {
-    const int st = kt & 1;
-    mbar_wait(s_bar, kt & 1, a.err);
-    tc_fence_after();
-
-    // scores of this row for keys kt*128 .. +128
-    float s[kKeys];
-#pragma unroll
-    for (int c = 0; c < kKeys; c += 32) {
-      uint32_t r[32];
-      tmem_ld32(tmem_s + lane_off + c, r);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 32; ++i) s[c + i] = __uint_as_float(r[i]);
-    }
-    const int key0 = kt * kKeys;
-    const int lim = row_end - key0;  // keys [key0, key0 + lim) are valid
-    float mt = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < kKeys; ++c) {
-      s[c] = (c < lim) ? s[c] * sc : -INFINITY;
-      mt = fmaxf(mt, s[c]);
-    }
-    float m_use = m_run;
-    float alpha = 1.f;
-    if (mt > m_run + kRescaleThreshold) {
-      m_use = mt;
-      alpha = ex2_approx(m_run - mt);  // 0 on the first tile
-    }
-    float sum = 0.f;
-#pragma unroll
-    for (int c = 0; c < kKeys; ++c) {
-      s[c] = ex2_approx(s[c] - m_use);
-      sum += s[c];
-    }
-    l_run = l_run * alpha + sum;
-    m_run = m_use;
-    const bool warp_rescale = __any_sync(0xffffffffu, alpha != 1.f) && kt > 0;
-
-    // PV of the previous tile must be done before P (smem) and O (TMEM) change
-    if (kt > 0) {
-      mbar_wait(o_bar, (kt - 1) & 1, a.err);
-      tc_fence_after();
-    }
-    if (warp_rescale) {
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem_o + lane_off + c, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-        tmem_st32(tmem_o + lane_off + c, r);
-      }
-      tmem_wait_st();
-    }
-    // P row -> smem, K-major 128-byte swizzle: 16-byte chunk ch of row `row`
-    // in 64-key block b lives at b*16K + row*128 + ((ch ^ (row & 7)) * 16)
-#pragma unroll
-    for (int cc = 0; cc < kKeys / 8; ++cc) {
-      uint4 v;
-      v.x = pack_bf16x2(s[cc * 8 + 0], s[cc * 8 + 1]);
-      v.y = pack_bf16x2(s[cc * 8 + 2], s[cc * 8 + 3]);
-      v.z = pack_bf16x2(s[cc * 8 + 4], s[cc * 8 + 5]);
-      v.w = pack_bf16x2(s[cc * 8 + 6], s[cc * 8 + 7]);
-      const int b = cc >> 3, ch = cc & 7;
-      uint8_t* dst = smem + L::OFF_P + b * (kRows * 128) + row * 128 + ((ch ^ (row & 7)) << 4);
-      *reinterpret_cast<uint4*>(dst) = v;
-    }
-    // keys past the request's last token (stale slots, or pages not loaded)
-    // must hold finite values in V: zero those rows of the last tile
-    const int tile_keys = tile.kv_len - key0;
-    if (tile_keys < kKeys) {
-      mbar_wait(&kv_full[st], (kt >> 1) & 1, a.err);
-      if (row >= tile_keys) {
-#pragma unroll
-        for (int b = 0; b < L::KB; ++b) {
-          uint4* dst = reinterpret_cast<uint4*>(vbuf[st] + b * (kKeys * 128) + row * 128);
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) dst[ch] = make_uint4(0, 0, 0, 0);
+          for (int b = 0; b < L::KB; ++b)
+            tma_load_3d(buf + b * (kKeys * 128) + pgi * (kP * 128), &prm.tmap_kv, b * 64, 0, slice,
+                        &ring_full[st]);
         }
       }
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    if (tid == 0) {
+    __syncwarp();
+    if (last_partial) {
+      // last V tile: rows past the request's last key must hold finite values
+      const int i = 2 * n_kt - 1, st = i % RS;
+      const int tile_keys = tile.kv_len - (n_kt - 1) * kKeys;
+      uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
+      mbar_wait(&ring_full[st], (i / RS) & 1, a.err);
+      const int nz = (kKeys - tile_keys) * 8;  // 16-byte chunks per 64-column block
+      for (int idx = lane; idx < nz * L::KB; idx += 32) {
+        const int b = idx / nz, rem = idx - b * nz;
+        const int r = tile_keys + (rem >> 3), ch = rem & 7;
+        *reinterpret_cast<uint4*>(buf + b * (kKeys * 128) + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(v_clean);
+    }
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0, 0);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 0, 1);
+      const uint32_t sQ = smem_u32(smem + L::OFF_Q);
+      const uint32_t sR = smem_u32(smem + L::OFF_RING);
+      auto issue_s = [&](int q, int st) {
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
+          const uint32_t koff = (k >> 2) * (kKeys * 128) + (k & 3) * 32;
+          tc_mma_ss(tmem + q * 128, desc_kmajor(sQ + q * L::Q_BYTES + off),
+                    desc_kmajor(sR + st * L::T_BYTES + koff), idesc_s, k > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[q]);
+      };
+      auto issue_pv = [&](int q, int st, int j) {
+#pragma unroll
+        for (int k = 0; k < kKeys / 16; ++k) {
+          const uint32_t voff = k * (16 * 128);
+          tc_mma_ts(tmem + 256 + q * 128, tmem + q * 128 + k * 8,
+                    desc_mnmajor(sR + st * L::T_BYTES + voff, kKeys * 128), idesc_o,
+                    (j > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(&o_done[q]);
+      };
+      mbar_wait(q_full, 0, a.err);
+      mbar_wait(&ring_full[0], 0, a.err);
       tc_fence_after();
-      issue_pv(st, kt);
-      if (kt + 1 < n_kt) {
-        mbar_wait(&kv_full[st ^ 1], ((kt + 1) >> 1) & 1, a.err);
-        issue_s(st ^ 1);
-      }
-      if (kt + 2 < n_kt) {
-        mbar_wait(&kv_empty[st], (kt >> 1) & 1, a.err);
-        load_kv(kt + 2, st);
+      for (int q = 0; q < nq; ++q) issue_s(q, 0);
+      tc_commit(&ring_empty[0]);
+      for (int j = 0; j < n_kt; ++j) {
+        const int iv = 2 * j + 1, sv = iv % RS;
+        const int ik = 2 * j + 2, sk = ik % RS;
+        mbar_wait(&ring_full[sv], (iv / RS) & 1, a.err);
+        if (j == n_kt - 1 && last_partial) mbar_wait(v_clean, 0, a.err);
+        bool k_ready = false;
+        for (int q = 0; q < nq; ++q) {
+          mbar_wait(&p_full[q], j & 1, a.err);
+          tc_fence_after();
+          issue_pv(q, sv, j);
+          if (j + 1 < n_kt) {
+            if (!k_ready) {
+              mbar_wait(&ring_full[sk], (ik / RS) & 1, a.err);
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(q, sk);
+          }
+        }
+        tc_commit(&ring_empty[sv]);
+        if (j + 1 < n_kt) tc_commit(&ring_empty[sk]);
       }
     }
-  }
+  } else if (warp / 4 < nq) {
+    // ------------------------------------------------------------- softmax
+    const int q = warp >> 2;
+    const int row = tid & 127;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tmem_s = tmem + q * 128 + lane_off;
+    const uint32_t tmem_o = tmem + 256 + q * 128 + lane_off;
+    const int q_ntok = q == 0 ? tile.ntok : tile.pad0;
+    const int q_tok0 = tile.tok0 + q * tile.ntok;  // first token of this Q tile
+    const int tl = row / g;
+    const int qpos = tile.kv_len - tile.qo_len + q_tok0 + tl;
+    const int row_end = a.causal ? min(qpos + 1, tile.kv_len) : tile.kv_len;  // keys j < row_end
+    const float sc = a.sm_scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;
 
-  // ---- epilogue: O / l -> bf16 rows of out; lse
-  mbar_wait(o_bar, (n_kt - 1) & 1, a.err);
-  tc_fence_after();
-  const float inv = 1.f / l_run;
-  const int hg = row - tl * g;
-  const int q_row = tile.q_row0 + tile.tok0 + tl;
-  const int hq = kvh * g + hg;
-  const bool write = row_ok && (tile.tok0 + tl) < tile.qo_len;
-  uint16_t* dst = a.out + ((int64_t)q_row * a.Hq + hq) * D;
+    for (int j = 0; j < n_kt; ++j) {
+      mbar_wait(&s_full[q], j & 1, a.err);
+      tc_fence_after();
+      float s[kKeys];
 #pragma unroll
-  for (int c = 0; c < D; c += 32) {
-    uint32_t r[32];
-    tmem_ld32(tmem_o + lane_off + c, r);
-    tmem_wait_ld();
-    if (write) {
+      for (int c = 0; c < kKeys; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem_s + c, r);
+        tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 32; i += 8) {
-        uint4 v;
-        v.x = pack_bf16x2(__uint_as_float(r[i + 0]) * inv, __uint_as_float(r[i + 1]) * inv);
-        v.y = pack_bf16x2(__uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
-        v.z = pack_bf16x2(__uint_as_float(r[i + 4]) * inv, __uint_as_float(r[i + 5]) * inv);
-        v.w = pack_bf16x2(__uint_as_float(r[i + 6]) * inv, __uint_as_float(r[i + 7]) * inv);
-        *reinterpret_cast<uint4*>(dst + c + i) = v;
+        for (int i2 = 0; i2 < 32; ++i2) s[c + i2] = __uint_as_float(r[i2]);
+      }
+      const int lim = row_end - j * kKeys;  // keys [j*128, j*128 + lim) are valid
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kKeys; ++c) {
+        s[c] = (c < lim) ? s[c] * sc : -INFINITY;
+        mt = fmaxf(mt, s[c]);
+      }
+      float m_use = m_run;
+      float alpha = 1.f;
+      if (mt > m_run + kRescaleThreshold) {
+        m_use = mt;
+        alpha = ex2_approx(m_run - mt);  // 0 on the first tile
+      }
+      // P = 2^(s - m) as bf16 pairs over the first 64 columns of S_q (the A
+      // operand of PV), 32 columns at a time so each chunk of s dies early
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kKeys / 2; c += 32) {
+        uint32_t r[32];
+#pragma unroll
+        for (int i2 = 0; i2 < 32; ++i2) {
+          const float p0 = ex2_approx(s[2 * (c + i2)] - m_use);
+          const float p1 = ex2_approx(s[2 * (c + i2) + 1] - m_use);
+          sum += p0 + p1;
+          r[i2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tmem_s + c, r);
+      }
+      l_run = l_run * alpha + sum;
+      m_run = m_use;
+      const bool warp_rescale = __any_sync(0xffffffffu, alpha != 1.f) && j > 0;
+
+      // O (TMEM) is rescaled once PV of the previous tile is done with it
+      if (warp_rescale) {
+        mbar_wait(&o_done[q], (j - 1) & 1, a.err);
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(tmem_o + c, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i2 = 0; i2 < 32; ++i2) r[i2] = __float_as_uint(__uint_as_float(r[i2]) * alpha);
+          tmem_st32(tmem_o + c, r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[q]);
+    }
+
+    // ---- epilogue: O / l -> bf16 rows of out; lse
+    mbar_wait(&o_done[q], (n_kt - 1) & 1, a.err);
+    tc_fence_after();
+    const float inv = 1.f / l_run;
+    const int hg = row - tl * g;
+    const int q_row = tile.q_row0 + q_tok0 + tl;
+    const int hq = kvh * g + hg;
+    const bool write = row < q_ntok * g;
+    uint16_t* dst = a.out + ((int64_t)q_row * a.Hq + hq) * D;
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+      uint32_t r[32];
+      tmem_ld32(tmem_o + c, r);
+      tmem_wait_ld();
+      if (write) {
+#pragma unroll
+        for (int i2 = 0; i2 < 32; i2 += 8) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(r[i2 + 0]) * inv, __uint_as_float(r[i2 + 1]) * inv);
+          v.y = pack_bf16x2(__uint_as_float(r[i2 + 2]) * inv, __uint_as_float(r[i2 + 3]) * inv);
+          v.z = pack_bf16x2(__uint_as_float(r[i2 + 4]) * inv, __uint_as_float(r[i2 + 5]) * inv);
+          v.w = pack_bf16x2(__uint_as_float(r[i2 + 6]) * inv, __uint_as_float(r[i2 + 7]) * inv);
+          *reinterpret_cast<uint4*>(dst + c + i2) = v;
+        }
       }
     }
+    if (write && a.lse_out)
+      a.lse_out[(int64_t)q_row * a.Hq + hq] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
   }
-  if (write && a.lse_out)
-    a.lse_out[(int64_t)q_row * a.Hq + hq] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_relinquish();
     tmem_dealloc(tmem, L::TMEM_COLS);
   }
 }
@@ -357,7 +380,7 @@ EncodeTiledFn get_encode_fn() {
 
 template <int D>
 cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
-  using L = PrefillSmem<D>;
+  using L = Smem<D>;
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return cudaErrorNotSupported;
   PrefillParams prm;
