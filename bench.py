@@ -44,6 +44,12 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 
 
 # ----------------------------------------------------------------- accounting
+# Decode requests whose kv head serves at least this many query heads run in
+# the tensor-core kernel (as key-split work items); the others in the CUDA-core
+# split-KV kernel.  Mirrors the library planner's routing rule.
+TC_DECODE_MIN_GROUP = 4
+
+
 def step_accounting(wl, k=0):
     """Algorithmic bytes / FLOPs of one step, split by kernel class."""
     Hq, Hkv, d, P = wl.num_qo_heads, wl.num_kv_heads, wl.head_dim, wl.page_size
@@ -60,8 +66,12 @@ def step_accounting(wl, k=0):
             pre_flops += 4 * d * Hq * pairs
             pre_bytes += r.kv_len * Hkv * d * 2 * 2 + 2 * r.qo_len * Hq * d * 2 + npages * 4
     app_bytes = nnz_new * Hkv * d * 2 * 2 * 2
+    tc_decode = wl.group_size >= TC_DECODE_MIN_GROUP
     return dict(decode_bytes=dec_bytes, append_bytes=app_bytes, prefill_flops=pre_flops,
-                prefill_bytes=pre_bytes, nnz_new=nnz_new)
+                prefill_bytes=pre_bytes, nnz_new=nnz_new,
+                # work per kernel
+                tc_flops=pre_flops, tc_bytes=pre_bytes + (dec_bytes if tc_decode else 0),
+                cuda_decode_bytes=0 if tc_decode else dec_bytes)
 
 
 def kernel_source_hash(name):
@@ -474,19 +484,28 @@ def main():
     if dom is not None:
         mean_ms = float(np.mean(per_kernel[dom]))
         n_launch = len(per_kernel[dom]) / args.steps
+        t = mean_ms * 1e-3
         if dom == "prefill_tc":
-            achieved = acc["prefill_flops"] / n_launch / (mean_ms * 1e-3) / 1e12
-            roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
-                    "frac": achieved / bf16, "kernel": dom, "mean_ms": mean_ms,
-                    "peak_source": f"{peak_src} bf16 dense (burst)"}
+            # the tensor-core kernel runs the prefill tiles and (for g >= 4) the
+            # decode splits: its bound is whichever ideal time is larger
+            fl, by = acc["tc_flops"] / n_launch, acc["tc_bytes"] / n_launch
+            t_tensor, t_hbm = fl / (bf16 * 1e12), by / (hbm * 1e9)
+            if t_tensor >= t_hbm:
+                roof = {"bound": "tensor", "achieved": fl / t / 1e12, "peak": bf16, "unit": "TFLOP/s",
+                        "peak_source": f"{peak_src} bf16 dense (burst)"}
+            else:
+                roof = {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm, "unit": "GB/s",
+                        "peak_source": f"{peak_src} HBM copy"}
+            roof["ideal_fraction"] = (t_tensor + t_hbm) / t
             kfile = "prefill.cu"
         else:
-            kb = {"decode_splitkv": acc["decode_bytes"], "kv_append": acc["append_bytes"]}.get(dom, 0)
-            achieved = kb / n_launch / (mean_ms * 1e-3) / 1e9
-            roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                    "frac": achieved / hbm, "kernel": dom, "mean_ms": mean_ms,
+            kb = {"decode_splitkv": acc["cuda_decode_bytes"], "kv_append": acc["append_bytes"]}.get(dom, 0)
+            roof = {"bound": "hbm", "achieved": kb / n_launch / t / 1e9, "peak": hbm, "unit": "GB/s",
                     "peak_source": f"{peak_src} HBM copy"}
             kfile = {"decode_splitkv": "decode.cu", "kv_append": "append.cu"}.get(dom, "decode.cu")
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["kernel"] = dom
+        roof["mean_ms"] = mean_ms
         roof["traffic"] = measured_traffic(args.workload, kfile)
         roof["share"] = {k: round(v / sum(tot.values()), 4) for k, v in tot.items()}
 
@@ -504,11 +523,15 @@ def main():
                             "append_bytes": acc["append_bytes"], "prefill_flops": acc["prefill_flops"]},
             "clocks": clk, "device_error": err}
     if acc["prefill_flops"] and "prefill_tc" in per_kernel:
+        # conservative: the kernel time also covers any decode splits it ran
         pm = float(np.mean(per_kernel["prefill_tc"]))
         line["prefill_tflops"] = acc["prefill_flops"] / (pm * 1e-3) / 1e12
-    if "decode_splitkv" in per_kernel and acc["decode_bytes"]:
-        dm = float(np.mean(per_kernel["decode_splitkv"]))
-        line["decode_gbs"] = acc["decode_bytes"] / (dm * 1e-3) / 1e9
+    if acc["decode_bytes"]:
+        kern = "decode_splitkv" if acc["cuda_decode_bytes"] else "prefill_tc"
+        if kern in per_kernel and not acc["prefill_flops"]:
+            dm = float(np.mean(per_kernel[kern]))
+            line["decode_gbs"] = acc["decode_bytes"] / (dm * 1e-3) / 1e9
+            line["decode_kernel"] = kern
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
         line["cpu_baseline"] = cpu_baseline(wl)
     print(json.dumps(line), flush=True)

@@ -18,6 +18,7 @@
 
 #include "../../include/daa.h"
 #include "launch.h"
+#include "planner.h"
 
 namespace daa {
 
@@ -37,10 +38,7 @@ int* device_error_word() {
 
 namespace {
 
-constexpr int kPageSize = 16;
-constexpr size_t kAlign = 256;
-
-size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+constexpr size_t kAlign = kPlanAlign;
 
 int num_sms() {
   static int cached[64] = {0};
@@ -60,130 +58,38 @@ int num_sms() {
   return cached[dev];
 }
 
-daa_status check_dims(const daa_dims& d) {
-  if (d.num_qo_heads <= 0 || d.num_kv_heads <= 0 || d.head_dim <= 0 || d.page_size <= 0 ||
-      d.num_pages <= 0)
-    return DAA_ERR_INVALID_ARG;
-  if (d.num_qo_heads % d.num_kv_heads != 0) return DAA_ERR_INVALID_ARG;
-  if (d.head_dim != 64 && d.head_dim != 128) return DAA_ERR_UNSUPPORTED;
-  if (d.page_size != kPageSize) return DAA_ERR_UNSUPPORTED;
-  const int g = d.num_qo_heads / d.num_kv_heads;
-  if (g < 1 || g > 16) return DAA_ERR_UNSUPPORTED;
-  // slices of the pool must be addressable by 32-bit TMA coordinates
-  if (d.num_pages * 2 * (int64_t)d.num_kv_heads > (int64_t)INT32_MAX) return DAA_ERR_UNSUPPORTED;
-  return DAA_OK;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-struct HostPlan {
-  std::vector<DecodeUnit> units;
-  std::vector<MergeItem> merges;
-  std::vector<PrefillTile> tiles;
-  int n_parts = 0;
-  size_t off_units = 0, off_merges = 0, off_tiles = 0, plan_bytes = 0;
-  size_t off_part_o = 0, off_part_lse = 0, total = 0;
+// growable plan containers (reused per host thread, so steady-state calls do
+// not allocate)
+template <class T>
+struct HostVec {
+  std::vector<T> v;
+  bool push_back(const T& x) {
+    v.push_back(x);
+    return true;
+  }
+  size_t size() const { return v.size(); }
+  T* data() { return v.data(); }
+  const T* data() const { return v.data(); }
+  void clear() { v.clear(); }
 };
+
+struct HostPlan {
+  HostVec<DecodeUnit> units;
+  HostVec<MergeItem> merges;
+  HostVec<PrefillTile> tiles;
+  PlanLayout lay;
+};
+
+HostPlan& host_plan() {
+  thread_local HostPlan p;
+  return p;
+}
 
 daa_status make_plan(const int32_t* qo, const int32_t* kv, const int32_t* last, int32_t batch,
                      const daa_dims& d, int sms, HostPlan& pl) {
-  daa_status st = check_dims(d);
-  if (st != DAA_OK) return st;
-  if (batch < 0) return DAA_ERR_INVALID_ARG;
-  if (batch > 0 && (!qo || !kv || !last)) return DAA_ERR_INVALID_ARG;
-  if (batch == 0) return DAA_OK;
-  if (qo[0] != 0 || kv[0] != 0) return DAA_ERR_SHAPE;
-  const int P = d.page_size;
-  const int g = d.num_qo_heads / d.num_kv_heads;
-  const int64_t Hkv = d.num_kv_heads;
-
-  int64_t dec_pages = 0;
-  for (int r = 0; r < batch; ++r) {
-    const int64_t nq = (int64_t)qo[r + 1] - qo[r];
-    const int64_t np = (int64_t)kv[r + 1] - kv[r];
-    if (nq < 0 || np < 0) return DAA_ERR_SHAPE;
-    if (np > 0 && (last[r] < 1 || last[r] > P)) return DAA_ERR_SHAPE;
-    const int64_t kv_len = np > 0 ? (np - 1) * P + last[r] : 0;
-    if (nq > kv_len) return DAA_ERR_SHAPE;
-    if (kv_len > INT32_MAX / 2) return DAA_ERR_SHAPE;
-    if (nq == 1) dec_pages += np;
-  }
-
-  // decode split size (pages): enough CTAs that the longest split is a small
-  // fraction of the whole pass, never fewer pages than fill the copy pipeline
-  const int64_t page_heads = dec_pages * Hkv;
-  int64_t split = (page_heads + (int64_t)sms * 40 - 1) / ((int64_t)sms * 40);
-  split = std::max<int64_t>(16, std::min<int64_t>(1024, split));
-
-  std::vector<DecodeUnit> full_units, tail_units;
-  for (int r = 0; r < batch; ++r) {
-    const int nq = qo[r + 1] - qo[r];
-    if (nq != 1) continue;
-    const int np = kv[r + 1] - kv[r];
-    const int kv_len = (np - 1) * P + last[r];
-    const int nsplit = (int)((np + split - 1) / split);
-    const int part0 = nsplit > 1 ? pl.n_parts : -1;
-    if (nsplit > 1) {
-      pl.merges.push_back(MergeItem{qo[r], pl.n_parts, nsplit, 0});
-      pl.n_parts += nsplit;
-    }
-    for (int s = 0; s < nsplit; ++s) {
-      DecodeUnit u{};
-      u.q_row = qo[r];
-      u.page_base = kv[r];
-      u.tok_begin = (int)(s * split * P);
-      u.tok_end = std::min<int>(kv_len, (int)((s + 1) * split * P));
-      u.kv_len = kv_len;
-      u.part = part0 >= 0 ? part0 + s : -1;
-      (u.tok_end - u.tok_begin == split * P ? full_units : tail_units).push_back(u);
-    }
-  }
-  std::stable_sort(tail_units.begin(), tail_units.end(), [](const DecodeUnit& x, const DecodeUnit& y) {
-    return (x.tok_end - x.tok_begin) > (y.tok_end - y.tok_begin);
-  });
-  pl.units = std::move(full_units);
-  pl.units.insert(pl.units.end(), tail_units.begin(), tail_units.end());
-
-  // prefill tiles: pairs of 128-row tiles (ntok * g <= 128 packed rows each;
-  // the second tile's tokens in pad0), longest key range first
-  const int tpt = kPrefillTileRows / g;
-  std::vector<std::pair<int, PrefillTile>> tw;
-  for (int r = 0; r < batch; ++r) {
-    const int nq = qo[r + 1] - qo[r];
-    if (nq < 2) continue;
-    const int np = kv[r + 1] - kv[r];
-    const int kv_len = (np - 1) * P + last[r];
-    for (int t0 = 0; t0 < nq; t0 += 2 * tpt) {
-      PrefillTile t{};
-      t.q_row0 = qo[r];
-      t.qo_len = nq;
-      t.kv_len = kv_len;
-      t.page_base = kv[r];
-      t.tok0 = t0;
-      t.ntok = std::min(tpt, nq - t0);
-      t.pad0 = t.ntok == tpt ? std::max(0, std::min(tpt, nq - t0 - tpt)) : 0;  // second tile
-      const int keys = std::min(kv_len, kv_len - nq + t0 + t.ntok + t.pad0);
-      tw.emplace_back(keys, t);
-    }
-  }
-  std::stable_sort(tw.begin(), tw.end(),
-                   [](const auto& x, const auto& y) { return x.first > y.first; });
-  for (auto& x : tw) pl.tiles.push_back(x.second);
-
-  size_t off = 0;
-  pl.off_units = off;
-  off = align_up(off + pl.units.size() * sizeof(DecodeUnit));
-  pl.off_merges = off;
-  off = align_up(off + pl.merges.size() * sizeof(MergeItem));
-  pl.off_tiles = off;
-  off = align_up(off + pl.tiles.size() * sizeof(PrefillTile));
-  pl.plan_bytes = off;
-  pl.off_part_o = off;
-  off = align_up(off + (size_t)pl.n_parts * d.num_qo_heads * d.head_dim * sizeof(float));
-  pl.off_part_lse = off;
-  off = align_up(off + (size_t)pl.n_parts * d.num_qo_heads * sizeof(float));
-  pl.total = (pl.units.empty() && pl.tiles.empty()) ? 0 : off;
-  return DAA_OK;
+  return plan_batch(qo, kv, last, batch, d, sms, pl.units, pl.merges, pl.tiles, pl.lay);
 }
 
 // ------------------------------------------------------------------ tracing
@@ -230,6 +136,74 @@ std::vector<uint8_t>& staging() {
 }
 
 }  // namespace
+
+daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s, bool trace) {
+  const daa_dims& dims = ls.dims;
+  const int g = dims.num_qo_heads / dims.num_kv_heads;
+  const float sc = ls.sm_scale * 1.4426950408889634f;
+  uint8_t* ws = static_cast<uint8_t*>(ls.scratch);
+  float* part_o = reinterpret_cast<float*>(ws + lay.off_part_o);
+  float* part_lse = reinterpret_cast<float*>(ws + lay.off_part_lse);
+  auto run = [&](int32_t kid, auto&& f) -> cudaError_t {
+    return trace ? traced(kid, s, f) : f();
+  };
+  if (lay.n_tiles > 0) {
+    PrefillArgs a{};
+    a.q = static_cast<const uint16_t*>(ls.q);
+    a.pool = static_cast<const uint16_t*>(ls.kv_pages);
+    a.page_indices = ls.page_indices;
+    a.tiles = reinterpret_cast<const PrefillTile*>(ws + lay.off_tiles);
+    a.n_tiles = lay.n_tiles;
+    a.Hq = dims.num_qo_heads;
+    a.Hkv = dims.num_kv_heads;
+    a.group = g;
+    a.head_dim = dims.head_dim;
+    a.num_pages = dims.num_pages;
+    a.nnz_qo = ls.nnz_qo;
+    a.causal = ls.causal ? 1 : 0;
+    a.sm_scale_log2 = sc;
+    a.out = static_cast<uint16_t*>(ls.out);
+    a.lse_out = ls.lse_out;
+    a.part_o = part_o;
+    a.part_lse = part_lse;
+    a.err = ls.err;
+    if (run(kKernelPrefill, [&] { return launch_prefill(a, s); }) != cudaSuccess) return DAA_ERR_CUDA;
+  }
+  if (lay.n_units > 0) {
+    DecodeArgs a{};
+    a.q = static_cast<const uint16_t*>(ls.q);
+    a.pool = static_cast<const uint16_t*>(ls.kv_pages);
+    a.page_indices = ls.page_indices;
+    a.units = reinterpret_cast<const DecodeUnit*>(ws + lay.off_units);
+    a.n_units = lay.n_units;
+    a.Hq = dims.num_qo_heads;
+    a.Hkv = dims.num_kv_heads;
+    a.group = g;
+    a.head_dim = dims.head_dim;
+    a.num_pages = dims.num_pages;
+    a.sm_scale_log2 = sc;
+    a.out = static_cast<uint16_t*>(ls.out);
+    a.lse_out = ls.lse_out;
+    a.part_o = part_o;
+    a.part_lse = part_lse;
+    a.err = ls.err;
+    if (run(kKernelDecode, [&] { return launch_decode(a, s); }) != cudaSuccess) return DAA_ERR_CUDA;
+  }
+  if (lay.n_merges > 0) {
+    MergeArgs m{};
+    m.items = reinterpret_cast<const MergeItem*>(ws + lay.off_merges);
+    m.n_items = lay.n_merges;
+    m.Hq = dims.num_qo_heads;
+    m.head_dim = dims.head_dim;
+    m.part_o = part_o;
+    m.part_lse = part_lse;
+    m.out = static_cast<uint16_t*>(ls.out);
+    m.lse_out = ls.lse_out;
+    if (run(kKernelMerge, [&] { return launch_merge(m, s); }) != cudaSuccess) return DAA_ERR_CUDA;
+  }
+  return DAA_OK;
+}
+
 }  // namespace daa
 
 using namespace daa;
@@ -256,7 +230,7 @@ daa_status daa_kv_append(const void* k_new, const void* v_new, void* kv_pages,
                          const int32_t* append_indptr, const int32_t* page_indices,
                          const int32_t* kv_indptr, const int32_t* last_page_len, int32_t batch,
                          int32_t nnz_new, daa_dims dims, void* stream) {
-  daa_status st = check_dims(dims);
+  daa_status st = plan_check_dims(dims);
   if (st != DAA_OK) return st;
   if (batch < 0 || nnz_new < 0) return DAA_ERR_INVALID_ARG;
   if (nnz_new == 0 || batch == 0) return nnz_new == 0 ? DAA_OK : DAA_ERR_SHAPE;
@@ -277,10 +251,10 @@ daa_status daa_kv_append(const void* k_new, const void* v_new, void* kv_pages,
 size_t daa_batch_attention_workspace_size(const int32_t* h_qo_indptr, const int32_t* h_kv_indptr,
                                           const int32_t* h_last_page_len, int32_t batch,
                                           daa_dims dims, daa_status* status) {
-  HostPlan pl;
+  HostPlan& pl = host_plan();
   daa_status st = make_plan(h_qo_indptr, h_kv_indptr, h_last_page_len, batch, dims, num_sms(), pl);
   if (status) *status = st;
-  return st == DAA_OK ? pl.total : 0;
+  return st == DAA_OK ? pl.lay.total : 0;
 }
 
 daa_status daa_batch_attention(const void* q, const void* kv_pages, const int32_t* qo_indptr,
@@ -290,93 +264,40 @@ daa_status daa_batch_attention(const void* q, const void* kv_pages, const int32_
                                int32_t batch, int32_t causal, float sm_scale, void* out,
                                float* lse_out, void* workspace, size_t workspace_bytes,
                                daa_dims dims, void* stream) {
-  if (!(std::isfinite(sm_scale))) return DAA_ERR_INVALID_ARG;
-  HostPlan pl;
+  if (!(std::isfinite(sm_scale)) || !(sm_scale > 0.f)) return DAA_ERR_INVALID_ARG;
+  HostPlan& pl = host_plan();
   daa_status st = make_plan(h_qo_indptr, h_kv_indptr, h_last_page_len, batch, dims, num_sms(), pl);
   if (st != DAA_OK) return st;
-  if (pl.units.empty() && pl.tiles.empty()) return DAA_OK;
+  const PlanLayout& lay = pl.lay;
+  if (lay.n_units == 0 && lay.n_tiles == 0) return DAA_OK;
   if (!q || !kv_pages || !qo_indptr || !kv_indptr || !page_indices || !last_page_len || !out)
     return DAA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv_pages) || !aligned16(out)) return DAA_ERR_ALIGNMENT;
   if ((reinterpret_cast<uintptr_t>(lse_out) & 3) != 0) return DAA_ERR_ALIGNMENT;
-  if (!workspace || workspace_bytes < pl.total) return DAA_ERR_WORKSPACE;
+  if (!workspace || workspace_bytes < lay.total) return DAA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DAA_ERR_ALIGNMENT;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   std::vector<uint8_t>& host = staging();
-  host.assign(pl.plan_bytes, 0);
-  if (!pl.units.empty())
-    std::memcpy(host.data() + pl.off_units, pl.units.data(), pl.units.size() * sizeof(DecodeUnit));
-  if (!pl.merges.empty())
-    std::memcpy(host.data() + pl.off_merges, pl.merges.data(), pl.merges.size() * sizeof(MergeItem));
-  if (!pl.tiles.empty())
-    std::memcpy(host.data() + pl.off_tiles, pl.tiles.data(), pl.tiles.size() * sizeof(PrefillTile));
-  if (cudaMemcpyAsync(ws, host.data(), pl.plan_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  if (host.size() < lay.plan_bytes) host.resize(lay.plan_bytes);
+  plan_stage(lay, pl.units, pl.merges, pl.tiles, host.data());
+  if (cudaMemcpyAsync(ws, host.data(), lay.plan_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return DAA_ERR_CUDA;
-
-  int* err = device_error_word();
-  const int g = dims.num_qo_heads / dims.num_kv_heads;
-  const float sc = sm_scale * 1.4426950408889634f;
-  const int nnz_qo = h_qo_indptr[batch];
-  cudaError_t e = cudaSuccess;
-
-  if (!pl.tiles.empty()) {
-    PrefillArgs a{};
-    a.q = static_cast<const uint16_t*>(q);
-    a.pool = static_cast<const uint16_t*>(kv_pages);
-    a.page_indices = page_indices;
-    a.tiles = reinterpret_cast<const PrefillTile*>(ws + pl.off_tiles);
-    a.n_tiles = (int)pl.tiles.size();
-    a.Hq = dims.num_qo_heads;
-    a.Hkv = dims.num_kv_heads;
-    a.group = g;
-    a.head_dim = dims.head_dim;
-    a.num_pages = dims.num_pages;
-    a.nnz_qo = nnz_qo;
-    a.causal = causal ? 1 : 0;
-    a.sm_scale_log2 = sc;
-    a.out = static_cast<uint16_t*>(out);
-    a.lse_out = lse_out;
-    a.err = err;
-    e = traced(kKernelPrefill, s, [&] { return launch_prefill(a, s); });
-    if (e != cudaSuccess) return DAA_ERR_CUDA;
-  }
-  if (!pl.units.empty()) {
-    DecodeArgs a{};
-    a.q = static_cast<const uint16_t*>(q);
-    a.pool = static_cast<const uint16_t*>(kv_pages);
-    a.page_indices = page_indices;
-    a.units = reinterpret_cast<const DecodeUnit*>(ws + pl.off_units);
-    a.n_units = (int)pl.units.size();
-    a.Hq = dims.num_qo_heads;
-    a.Hkv = dims.num_kv_heads;
-    a.group = g;
-    a.head_dim = dims.head_dim;
-    a.num_pages = dims.num_pages;
-    a.sm_scale_log2 = sc;
-    a.out = static_cast<uint16_t*>(out);
-    a.lse_out = lse_out;
-    a.part_o = reinterpret_cast<float*>(ws + pl.off_part_o);
-    a.part_lse = reinterpret_cast<float*>(ws + pl.off_part_lse);
-    a.err = err;
-    e = traced(kKernelDecode, s, [&] { return launch_decode(a, s); });
-    if (e != cudaSuccess) return DAA_ERR_CUDA;
-    if (!pl.merges.empty()) {
-      MergeArgs m{};
-      m.items = reinterpret_cast<const MergeItem*>(ws + pl.off_merges);
-      m.n_items = (int)pl.merges.size();
-      m.Hq = dims.num_qo_heads;
-      m.head_dim = dims.head_dim;
-      m.part_o = a.part_o;
-      m.part_lse = a.part_lse;
-      m.out = a.out;
-      m.lse_out = lse_out;
-      e = traced(kKernelMerge, s, [&] { return launch_merge(m, s); });
-      if (e != cudaSuccess) return DAA_ERR_CUDA;
-    }
-  }
-  return DAA_OK;
+  LaunchSet ls{};
+  ls.q = q;
+  ls.kv_pages = kv_pages;
+  ls.page_indices = page_indices;
+  ls.dims = dims;
+  ls.causal = causal;
+  ls.sm_scale = sm_scale;
+  ls.nnz_qo = h_qo_indptr[batch];
+  ls.out = out;
+  ls.lse_out = lse_out;
+  ls.scratch = ws;
+  ls.err = device_error_word();
+  ls.sms = num_sms();
+  return launch_all(ls, lay, s, /*trace=*/true);
 }
 
 daa_status daa_device_error(int32_t* code, int32_t reset) {

@@ -3,6 +3,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/daa.h"
 #include "plan.h"
 
 namespace daa {
@@ -58,10 +59,31 @@ struct PrefillArgs {
   float sm_scale_log2;
   uint16_t* out;
   float* lse_out;
+  float* part_o;                // split items: [n_parts][Hq][d]
+  float* part_lse;              // split items: [n_parts][Hq] (log2 domain)
   int* err;
 };
 // Rows of packed (token, head) a prefill tile holds.
 constexpr int kPrefillTileRows = 128;
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+// Everything one batch_attention call launches, given its plan in `scratch`
+// (the workspace, or the no-allocation entry point's static array).
+struct LaunchSet {
+  const void* q;
+  const void* kv_pages;
+  const int32_t* page_indices;
+  daa_dims dims;
+  int causal;
+  float sm_scale;
+  int nnz_qo;
+  void* out;
+  float* lse_out;
+  void* scratch;
+  int* err;
+  int sms;
+};
+struct PlanLayout;
+daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s, bool trace);
 
 }  // namespace daa

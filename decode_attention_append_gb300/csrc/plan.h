@@ -26,11 +26,15 @@ struct MergeItem {
   int32_t pad;
 };
 
-// One or two tiles of packed query rows of one prefill request (qo_len > 1):
-// tile 0 holds new tokens [tok0, tok0 + ntok) of the request, tile 1 (if pad0
-// > 0) the next pad0 tokens; each token brings all g query heads of a kv head,
-// packed token-major into ntok * g <= 128 rows per tile.  One CTA per
-// (tile pair, kv head); both tiles share every K/V tile the CTA loads.
+// A work item of the tensor-core kernel: one or two 128-row tiles of packed
+// query rows of one request, over keys [key_lo, min(key_hi, causal end)).
+// Tile 0 holds new tokens [tok0, tok0 + ntok) of the request, tile 1 (if
+// ntok1 > 0) the next ntok1 tokens; each token brings all g query heads of a
+// kv head, packed token-major into ntok * g <= 128 rows per tile.  One CTA per
+// (item, kv head); both tiles share every K/V tile the CTA loads.  Prefill
+// pairs cover all keys and write the output; a decode request (qo_len == 1,
+// ntok == 1) may be split over 128-key-aligned key ranges, each writing a
+// partial (o, lse) to slot `part` for softmax_merge.
 struct PrefillTile {
   int32_t q_row0;     // row of the request's first new token
   int32_t qo_len;
@@ -38,13 +42,17 @@ struct PrefillTile {
   int32_t page_base;
   int32_t tok0;       // first new-token index (0-based within the request)
   int32_t ntok;       // tokens in tile 0
-  int32_t pad0;       // tokens in tile 1 (0: no second tile)
-  int32_t pad1;
+  int32_t ntok1;      // tokens in tile 1 (0: no second tile)
+  int32_t key_lo;     // first key (multiple of 128)
+  int32_t key_hi;     // one past the last key
+  int32_t part;       // partial slot, or -1: write out / lse_out directly
+  int32_t work;       // planner's sort key (keys read)
+  int32_t pad;
 };
 
 static_assert(sizeof(DecodeUnit) == 32, "DecodeUnit layout");
 static_assert(sizeof(MergeItem) == 16, "MergeItem layout");
-static_assert(sizeof(PrefillTile) == 32, "PrefillTile layout");
+static_assert(sizeof(PrefillTile) == 48, "PrefillTile layout");
 
 // Kernel ids reported by the tracer.
 enum KernelId : int32_t {

@@ -1,0 +1,205 @@
+// Host-side plan of one batch_attention call, shared by the workspace entry
+// point and the no-allocation entry point (which instantiates it over
+// fixed-capacity static containers).
+//
+// "Disaggregated prefill and decode" (Perplexity), "Prefill vs decode
+// performance": attention parallelises over requests and over kv_len.  Work is
+// split three ways:
+//  * decode requests (qo_len == 1) whose kv head serves g >= kTcDecodeMinGroup
+//    query heads go to the tensor-core kernel as key-split work items (the g
+//    query heads are the rows of one M = 128 tile); the K/V bytes then stream
+//    at memory rate while the CUDA cores only run the softmax;
+//  * other decode requests go to the CUDA-core split-KV kernel as page-aligned
+//    key splits;
+//  * prefill requests (qo_len > 1) become pairs of 128-row tiles of packed
+//    (token, query head) rows for the tensor-core kernel, longest key range
+//    first.
+// Split decode requests get consecutive partial slots and one softmax_merge
+// item ("Chunked prefill" (k4i.top), #correctness).
+#pragma once
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/daa.h"
+#include "launch.h"
+
+namespace daa {
+
+constexpr int kPlanPageSize = 16;
+constexpr int kTcDecodeMinGroup = 4;
+constexpr size_t kPlanAlign = 256;
+
+inline size_t plan_align_up(size_t x) { return (x + kPlanAlign - 1) & ~(kPlanAlign - 1); }
+
+inline daa_status plan_check_dims(const daa_dims& d) {
+  if (d.num_qo_heads <= 0 || d.num_kv_heads <= 0 || d.head_dim <= 0 || d.page_size <= 0 ||
+      d.num_pages <= 0 || d.num_qo_heads % d.num_kv_heads != 0)
+    return DAA_ERR_INVALID_ARG;
+  if (d.head_dim != 64 && d.head_dim != 128) return DAA_ERR_UNSUPPORTED;
+  if (d.page_size != kPlanPageSize) return DAA_ERR_UNSUPPORTED;
+  const int g = d.num_qo_heads / d.num_kv_heads;
+  if (g < 1 || g > 16) return DAA_ERR_UNSUPPORTED;
+  // slices of the pool must be addressable by 32-bit TMA coordinates
+  if (d.num_pages * 2 * (int64_t)d.num_kv_heads > (int64_t)INT32_MAX) return DAA_ERR_UNSUPPORTED;
+  return DAA_OK;
+}
+
+// Offsets of the workspace sections (bytes).
+struct PlanLayout {
+  int n_units = 0, n_merges = 0, n_tiles = 0, n_parts = 0;
+  size_t off_units = 0, off_merges = 0, off_tiles = 0, plan_bytes = 0;
+  size_t off_part_o = 0, off_part_lse = 0, total = 0;
+};
+
+// Vec: push_back(const T&) -> bool (false when full), size(), data(), clear().
+template <class UnitVec, class MergeVec, class TileVec>
+daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last, int32_t batch,
+                      const daa_dims& d, int sms, UnitVec& units, MergeVec& merges,
+                      TileVec& tiles, PlanLayout& lay) {
+  units.clear();
+  merges.clear();
+  tiles.clear();
+  lay = PlanLayout{};
+  daa_status st = plan_check_dims(d);
+  if (st != DAA_OK) return st;
+  if (batch < 0) return DAA_ERR_INVALID_ARG;
+  if (batch == 0) return DAA_OK;
+  if (!qo || !kv || !last) return DAA_ERR_INVALID_ARG;
+  if (qo[0] != 0 || kv[0] != 0) return DAA_ERR_SHAPE;
+  const int P = d.page_size;
+  const int g = d.num_qo_heads / d.num_kv_heads;
+  const bool tc_decode = g >= kTcDecodeMinGroup;
+
+  int64_t dec_pages = 0;
+  for (int r = 0; r < batch; ++r) {
+    const int64_t nq = (int64_t)qo[r + 1] - qo[r];
+    const int64_t np = (int64_t)kv[r + 1] - kv[r];
+    if (nq < 0 || np < 0) return DAA_ERR_SHAPE;
+    if (np > 0 && (last[r] < 1 || last[r] > P)) return DAA_ERR_SHAPE;
+    const int64_t kv_len = np > 0 ? (np - 1) * P + last[r] : 0;
+    if (nq > kv_len || kv_len > INT32_MAX / 2) return DAA_ERR_SHAPE;
+    if (nq == 1) dec_pages += np;
+  }
+  const int64_t page_heads = dec_pages * d.num_kv_heads;
+
+  // split sizes (pages).  CUDA-core splits: enough CTAs that the longest split
+  // is a small fraction of the pass.  Tensor-core splits: whole 128-key tiles,
+  // about four items per SM (one 224 KB CTA per SM at a time).
+  int64_t split;
+  if (tc_decode) {
+    split = (page_heads + (int64_t)sms * 4 - 1) / ((int64_t)sms * 4);
+    split = (split + 7) / 8 * 8;
+    split = std::max<int64_t>(32, std::min<int64_t>(2048, split));
+  } else {
+    split = (page_heads + (int64_t)sms * 40 - 1) / ((int64_t)sms * 40);
+    split = std::max<int64_t>(16, std::min<int64_t>(1024, split));
+  }
+
+  for (int r = 0; r < batch; ++r) {
+    if (qo[r + 1] - qo[r] != 1) continue;
+    const int np = kv[r + 1] - kv[r];
+    const int kv_len = (np - 1) * P + last[r];
+    const int nsplit = (int)((np + split - 1) / split);
+    int part0 = -1;
+    if (nsplit > 1) {
+      if (!merges.push_back(MergeItem{qo[r], lay.n_parts, nsplit, 0})) return DAA_ERR_WORKSPACE;
+      part0 = lay.n_parts;
+      lay.n_parts += nsplit;
+    }
+    for (int s = 0; s < nsplit; ++s) {
+      const int lo = (int)(s * split * P);
+      const int hi = std::min<int>(kv_len, (int)((s + 1) * split * P));
+      if (tc_decode) {
+        PrefillTile t{};
+        t.q_row0 = qo[r];
+        t.qo_len = 1;
+        t.kv_len = kv_len;
+        t.page_base = kv[r];
+        t.tok0 = 0;
+        t.ntok = 1;
+        t.ntok1 = 0;
+        t.key_lo = lo;
+        t.key_hi = hi;
+        t.part = part0 >= 0 ? part0 + s : -1;
+        t.work = hi - lo;
+        if (!tiles.push_back(t)) return DAA_ERR_WORKSPACE;
+      } else {
+        DecodeUnit u{};
+        u.q_row = qo[r];
+        u.page_base = kv[r];
+        u.tok_begin = lo;
+        u.tok_end = hi;
+        u.kv_len = kv_len;
+        u.part = part0 >= 0 ? part0 + s : -1;
+        if (!units.push_back(u)) return DAA_ERR_WORKSPACE;
+      }
+    }
+  }
+  // longest splits first (only the last split of a request is shorter)
+  std::sort(units.data(), units.data() + units.size(), [](const DecodeUnit& x, const DecodeUnit& y) {
+    const int a = x.tok_end - x.tok_begin, b = y.tok_end - y.tok_begin;
+    return a != b ? a > b : (x.q_row != y.q_row ? x.q_row < y.q_row : x.tok_begin < y.tok_begin);
+  });
+
+  // prefill: pairs of 128-row tiles (ntok * g <= 128 packed rows each)
+  const int tpt = kPrefillTileRows / g;
+  for (int r = 0; r < batch; ++r) {
+    const int nq = qo[r + 1] - qo[r];
+    if (nq < 2) continue;
+    const int np = kv[r + 1] - kv[r];
+    const int kv_len = (np - 1) * P + last[r];
+    for (int t0 = 0; t0 < nq; t0 += 2 * tpt) {
+      PrefillTile t{};
+      t.q_row0 = qo[r];
+      t.qo_len = nq;
+      t.kv_len = kv_len;
+      t.page_base = kv[r];
+      t.tok0 = t0;
+      t.ntok = std::min(tpt, nq - t0);
+      t.ntok1 = t.ntok == tpt ? std::max(0, std::min(tpt, nq - t0 - tpt)) : 0;
+      t.key_lo = 0;
+      t.key_hi = kv_len;
+      t.part = -1;
+      // keys read, counted twice for a pair (both tiles use each key tile)
+      t.work = std::min(kv_len, kv_len - nq + t0 + t.ntok + t.ntok1) * (t.ntok1 > 0 ? 2 : 1);
+      if (!tiles.push_back(t)) return DAA_ERR_WORKSPACE;
+    }
+  }
+  // tensor-core items: most work first
+  std::sort(tiles.data(), tiles.data() + tiles.size(), [](const PrefillTile& x, const PrefillTile& y) {
+    if (x.work != y.work) return x.work > y.work;
+    if (x.q_row0 != y.q_row0) return x.q_row0 < y.q_row0;
+    return x.tok0 != y.tok0 ? x.tok0 < y.tok0 : x.key_lo < y.key_lo;
+  });
+
+  lay.n_units = (int)units.size();
+  lay.n_merges = (int)merges.size();
+  lay.n_tiles = (int)tiles.size();
+  size_t off = 0;
+  lay.off_units = off;
+  off = plan_align_up(off + units.size() * sizeof(DecodeUnit));
+  lay.off_merges = off;
+  off = plan_align_up(off + merges.size() * sizeof(MergeItem));
+  lay.off_tiles = off;
+  off = plan_align_up(off + tiles.size() * sizeof(PrefillTile));
+  lay.plan_bytes = off;
+  lay.off_part_o = off;
+  off = plan_align_up(off + (size_t)lay.n_parts * d.num_qo_heads * d.head_dim * sizeof(float));
+  lay.off_part_lse = off;
+  off = plan_align_up(off + (size_t)lay.n_parts * d.num_qo_heads * sizeof(float));
+  lay.total = (units.size() == 0 && tiles.size() == 0) ? 0 : off;
+  return DAA_OK;
+}
+
+// Copy the plan into a host staging buffer laid out as the workspace head.
+template <class UnitVec, class MergeVec, class TileVec>
+void plan_stage(const PlanLayout& lay, const UnitVec& units, const MergeVec& merges,
+                const TileVec& tiles, uint8_t* host) {
+  std::memset(host, 0, lay.plan_bytes);
+  if (units.size()) std::memcpy(host + lay.off_units, units.data(), units.size() * sizeof(DecodeUnit));
+  if (merges.size()) std::memcpy(host + lay.off_merges, merges.data(), merges.size() * sizeof(MergeItem));
+  if (tiles.size()) std::memcpy(host + lay.off_tiles, tiles.data(), tiles.size() * sizeof(PrefillTile));
+}
+
+}  // namespace daa

@@ -49,6 +49,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 domain
 
 struct __align__(64) PrefillParams {
   CUtensorMap tmap_q;     // q viewed as [nnz_qo][Hq][d], box {64, g, 128/g}
+  CUtensorMap tmap_q1;    // the same view, box {64, g, 1} (one-token decode items)
   CUtensorMap tmap_kv;    // pool viewed as [num_pages*2*Hkv][P][d], box {64, P, 1}
   PrefillArgs a;
 };
@@ -104,18 +105,25 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
   const int kvh = blockIdx.y;
   const int g = a.group;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nq = tile.pad0 > 0 ? 2 : 1;  // Q tiles in this CTA (pad0 = tokens of tile 1)
+  const int nq = tile.ntok1 > 0 ? 2 : 1;  // Q tiles in this CTA
+  const bool one_token = tile.ntok == 1 && nq == 1;
 
-  // keys [0, kv_end) are read; causal rows mask beyond their own position
+  // key tiles kt0 .. kt0 + n_kt - 1 cover keys [key_lo, kend); causal rows mask
+  // beyond their own position
   const int pos_first = tile.kv_len - tile.qo_len + tile.tok0;
-  const int ntok_all = tile.ntok + tile.pad0;
+  const int ntok_all = tile.ntok + tile.ntok1;
   const int kv_end = a.causal ? min(tile.kv_len, pos_first + ntok_all) : tile.kv_len;
-  const int n_kt = (kv_end + kKeys - 1) / kKeys;
+  const int kend = min(kv_end, tile.key_hi);
+  const int kt0 = tile.key_lo / kKeys;
+  const int n_kt = (kend + kKeys - 1) / kKeys - kt0;
   const int npages_req = (tile.kv_len + kP - 1) / kP;
-  const bool last_partial = tile.kv_len - (n_kt - 1) * kKeys < kKeys;
+  const bool last_partial = tile.kv_len - (kt0 + n_kt - 1) * kKeys < kKeys;
+  // warps of each Q tile that hold real rows (the others skip the softmax)
+  const int act0 = (tile.ntok * g + 31) / 32;
+  const int act1 = (tile.ntok1 * g + 31) / 32;
 
   if (tid == 0) {
-    prefetch_tmap(&prm.tmap_q);
+    prefetch_tmap(one_token ? (const void*)&prm.tmap_q1 : (const void*)&prm.tmap_q);
     prefetch_tmap(&prm.tmap_kv);
     mbar_init(q_full, 1);
     for (int i = 0; i < RS; ++i) {
@@ -124,7 +132,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(&s_full[q], 1);
-      mbar_init(&p_full[q], 4);
+      mbar_init(&p_full[q], q == 0 ? act0 : (act1 > 0 ? act1 : 1));
       mbar_init(&o_done[q], 1);
     }
     mbar_init(v_clean, 1);
@@ -142,15 +150,16 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const int tpt = kRows / g;
+      const int tpt = one_token ? 1 : kRows / g;
+      const void* tmap_q = one_token ? (const void*)&prm.tmap_q1 : (const void*)&prm.tmap_q;
       mbar_arrive_expect_tx(q_full, (uint32_t)(nq * tpt * g * D * 2));
       for (int q = 0; q < nq; ++q)
         for (int b = 0; b < L::KB; ++b)
-          tma_load_3d(smem + L::OFF_Q + q * L::Q_BYTES + b * (kRows * 128), &prm.tmap_q, b * 64,
+          tma_load_3d(smem + L::OFF_Q + q * L::Q_BYTES + b * (kRows * 128), tmap_q, b * 64,
                       kvh * g, tile.q_row0 + tile.tok0 + q * tile.ntok, q_full);
       for (int i = 0; i < 2 * n_kt; ++i) {
         const int st = i % RS;
-        const int j = i >> 1;
+        const int j = kt0 + (i >> 1);  // absolute key tile
         const int pg0 = j * kPagesPerTile;
         const int np = min(kPagesPerTile, npages_req - pg0);
         uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
@@ -174,7 +183,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
     if (last_partial) {
       // last V tile: rows past the request's last key must hold finite values
       const int i = 2 * n_kt - 1, st = i % RS;
-      const int tile_keys = tile.kv_len - (n_kt - 1) * kKeys;
+      const int tile_keys = tile.kv_len - (kt0 + n_kt - 1) * kKeys;
       uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
       mbar_wait(&ring_full[st], (i / RS) & 1, a.err);
       const int nz = (kKeys - tile_keys) * 8;  // 16-byte chunks per 64-column block
@@ -242,18 +251,18 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
         if (j + 1 < n_kt) tc_commit(&ring_empty[sk]);
       }
     }
-  } else if (warp / 4 < nq) {
+  } else if (warp / 4 < nq && (warp & 3) < ((warp >> 2) == 0 ? act0 : act1)) {
     // ------------------------------------------------------------- softmax
     const int q = warp >> 2;
     const int row = tid & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tmem_s = tmem + q * 128 + lane_off;
     const uint32_t tmem_o = tmem + 256 + q * 128 + lane_off;
-    const int q_ntok = q == 0 ? tile.ntok : tile.pad0;
+    const int q_ntok = q == 0 ? tile.ntok : tile.ntok1;
     const int q_tok0 = tile.tok0 + q * tile.ntok;  // first token of this Q tile
     const int tl = row / g;
     const int qpos = tile.kv_len - tile.qo_len + q_tok0 + tl;
-    const int row_end = a.causal ? min(qpos + 1, tile.kv_len) : tile.kv_len;  // keys j < row_end
+    const int row_end = min(a.causal ? min(qpos + 1, tile.kv_len) : tile.kv_len, kend);  // keys < row_end
     const float sc = a.sm_scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
 
@@ -262,41 +271,48 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
       tc_fence_after();
       float s[kKeys];
 #pragma unroll
-      for (int c = 0; c < kKeys; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem_s + c, r);
-        tmem_wait_ld();
+      for (int c = 0; c < kKeys; c += 32) tmem_ld32f(tmem_s + c, s + c);
+      tmem_wait_ld();
+      const int lim = row_end - (kt0 + j) * kKeys;  // keys [(kt0+j)*128, .. + lim) are valid
+      if (!__all_sync(0xffffffffu, lim >= kKeys)) {
 #pragma unroll
-        for (int i2 = 0; i2 < 32; ++i2) s[c + i2] = __uint_as_float(r[i2]);
+        for (int c = 0; c < kKeys; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
       }
-      const int lim = row_end - j * kKeys;  // keys [j*128, j*128 + lim) are valid
-      float mt = -INFINITY;
+      // row max of the raw scores (sm_scale > 0, so it commutes with scaling)
+      // (four independent chains over 32 columns each)
+      float mx[4];
 #pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        s[c] = (c < lim) ? s[c] * sc : -INFINITY;
-        mt = fmaxf(mt, s[c]);
+      for (int k = 0; k < 4; ++k) {
+        mx[k] = s[32 * k];
+#pragma unroll
+        for (int i2 = 1; i2 < 31; i2 += 2) mx[k] = fmax3(mx[k], s[32 * k + i2], s[32 * k + i2 + 1]);
+        mx[k] = fmaxf(mx[k], s[32 * k + 31]);
       }
+      const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * sc;
       float m_use = m_run;
       float alpha = 1.f;
       if (mt > m_run + kRescaleThreshold) {
         m_use = mt;
         alpha = ex2_approx(m_run - mt);  // 0 on the first tile
       }
-      // P = 2^(s - m) as bf16 pairs over the first 64 columns of S_q (the A
-      // operand of PV), 32 columns at a time so each chunk of s dies early
-      float sum = 0.f;
+      // P = 2^(s * scale - m) as bf16 pairs over the first 64 columns of S_q
+      // (the A operand of PV), 32 columns at a time so each chunk of s dies early
+      const float2 sc2 = make_float2(sc, sc);
+      const float2 nm2 = make_float2(-m_use, -m_use);
+      float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < kKeys / 2; c += 32) {
         uint32_t r[32];
 #pragma unroll
         for (int i2 = 0; i2 < 32; ++i2) {
-          const float p0 = ex2_approx(s[2 * (c + i2)] - m_use);
-          const float p1 = ex2_approx(s[2 * (c + i2) + 1] - m_use);
-          sum += p0 + p1;
-          r[i2] = pack_bf16x2(p0, p1);
+          const float2 t = __ffma2_rn(make_float2(s[2 * (c + i2)], s[2 * (c + i2) + 1]), sc2, nm2);
+          const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+          sum2 = __fadd2_rn(sum2, pp);
+          r[i2] = pack_bf16x2(pp.x, pp.y);
         }
         tmem_st32(tmem_s + c, r);
       }
+      const float sum = sum2.x + sum2.y;
       l_run = l_run * alpha + sum;
       m_run = m_use;
       const bool warp_rescale = __any_sync(0xffffffffu, alpha != 1.f) && j > 0;
@@ -306,13 +322,18 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
         mbar_wait(&o_done[q], (j - 1) & 1, a.err);
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(tmem_o + c, r);
+        for (int c = 0; c < D; c += 64) {  // two 32-column loads in flight per wait
+          float o[64];
+          tmem_ld32f(tmem_o + c, o);
+          tmem_ld32f(tmem_o + c + 32, o + 32);
           tmem_wait_ld();
+          uint32_t r[32];
 #pragma unroll
-          for (int i2 = 0; i2 < 32; ++i2) r[i2] = __float_as_uint(__uint_as_float(r[i2]) * alpha);
-          tmem_st32(tmem_o + c, r);
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int i2 = 0; i2 < 32; ++i2) r[i2] = __float_as_uint(o[32 * h + i2] * alpha);
+            tmem_st32(tmem_o + c + 32 * h, r);
+          }
         }
       }
       tmem_wait_st();
@@ -329,26 +350,39 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
     const int q_row = tile.q_row0 + q_tok0 + tl;
     const int hq = kvh * g + hg;
     const bool write = row < q_ntok * g;
+    const bool partial = tile.part >= 0;  // one-token split item: fp32 partial for softmax_merge
     uint16_t* dst = a.out + ((int64_t)q_row * a.Hq + hq) * D;
+    float* pdst = a.part_o + ((int64_t)tile.part * a.Hq + hq) * D;
 #pragma unroll
-    for (int c = 0; c < D; c += 32) {
-      uint32_t r[32];
-      tmem_ld32(tmem_o + c, r);
+    for (int c = 0; c < D; c += 64) {  // two 32-column loads in flight per wait
+      float o[64];
+      tmem_ld32f(tmem_o + c, o);
+      tmem_ld32f(tmem_o + c + 32, o + 32);
       tmem_wait_ld();
-      if (write) {
+      if (write && partial) {
 #pragma unroll
-        for (int i2 = 0; i2 < 32; i2 += 8) {
+        for (int i2 = 0; i2 < 64; i2 += 4)
+          *reinterpret_cast<float4*>(pdst + c + i2) =
+              make_float4(o[i2] * inv, o[i2 + 1] * inv, o[i2 + 2] * inv, o[i2 + 3] * inv);
+      } else if (write) {
+#pragma unroll
+        for (int i2 = 0; i2 < 64; i2 += 8) {
           uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(r[i2 + 0]) * inv, __uint_as_float(r[i2 + 1]) * inv);
-          v.y = pack_bf16x2(__uint_as_float(r[i2 + 2]) * inv, __uint_as_float(r[i2 + 3]) * inv);
-          v.z = pack_bf16x2(__uint_as_float(r[i2 + 4]) * inv, __uint_as_float(r[i2 + 5]) * inv);
-          v.w = pack_bf16x2(__uint_as_float(r[i2 + 6]) * inv, __uint_as_float(r[i2 + 7]) * inv);
+          v.x = pack_bf16x2(o[i2 + 0] * inv, o[i2 + 1] * inv);
+          v.y = pack_bf16x2(o[i2 + 2] * inv, o[i2 + 3] * inv);
+          v.z = pack_bf16x2(o[i2 + 4] * inv, o[i2 + 5] * inv);
+          v.w = pack_bf16x2(o[i2 + 6] * inv, o[i2 + 7] * inv);
           *reinterpret_cast<uint4*>(dst + c + i2) = v;
         }
       }
     }
-    if (write && a.lse_out)
-      a.lse_out[(int64_t)q_row * a.Hq + hq] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+    if (write) {
+      const float lse2 = m_run + __log2f(l_run);
+      if (partial)
+        a.part_lse[(int64_t)tile.part * a.Hq + hq] = lse2;
+      else if (a.lse_out)
+        a.lse_out[(int64_t)q_row * a.Hq + hq] = lse2 * 0.69314718055994531f;
+    }
   }
 
   tc_fence_before();
@@ -393,6 +427,16 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
     cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)tpt};
     cuuint32_t es[3] = {1, 1, 1};
     if (enc(&prm.tmap_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.q, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.Hq, (cuuint64_t)a.nnz_qo};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.Hq * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)g, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&prm.tmap_q1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.q, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
