@@ -25,6 +25,9 @@
 // Per key tile the MMA warp issues PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): S_q(j+1)
 // follows PV_q(j) in the tensor pipe, which reads P_q(j) from the columns
 // S_q(j+1) overwrites; the other tile's softmax runs meanwhile (ping-pong).
+// A CTA with a single Q tile (decode splits, a request's last odd tile) instead
+// double-buffers S over both S regions, so S(j+1) is ready while softmax works
+// on tile j, and PV(j) is followed by S(j+2) into the buffer it just read.
 // Softmax keeps a lazily raised running max (raised only when it grows by
 // more than 2^8) and rescales O in TMEM only then.  V rows past the request's
 // last key (stale slots, or pages not loaded) are zeroed by the producer
@@ -82,6 +85,28 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t addr, uint32_t lbo) {
   return smem_desc_sw128(addr, lbo, 1024);
 }
 
+// Ring item order.  Pairs of Q tiles (nq == 2) consume K_0, V_0, K_1, V_1, ...
+// A single Q tile double-buffers S, so S runs one tile ahead of PV and the
+// consumption order is K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}.
+__device__ __forceinline__ int ring_tile(int i, int nq, int n) {
+  if (nq == 2) return i >> 1;
+  if (i == 0) return 0;
+  if (i & 1) {  // i = 2t + 1: K_{t+1}, or V_{n-1} for the last item
+    const int t = i >> 1;
+    return t + 1 < n ? t + 1 : t;
+  }
+  return (i >> 1) - 1;  // i = 2t + 2: V_t
+}
+__device__ __forceinline__ bool ring_is_v(int i, int nq, int n) {
+  if (nq == 2) return i & 1;
+  if (i == 0) return false;
+  if (i & 1) return (i >> 1) + 1 >= n;
+  return true;
+}
+// Ring index of K_j / V_j in the single-tile order above.
+__device__ __forceinline__ int ring_k_index(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int ring_v_index(int j, int n) { return j <= n - 2 ? 2 * j + 2 : 2 * n - 1; }
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
@@ -132,7 +157,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(&s_full[q], 1);
-      mbar_init(&p_full[q], q == 0 ? act0 : (act1 > 0 ? act1 : 1));
+      mbar_init(&p_full[q], q == 0 || nq == 1 ? act0 : act1);
       mbar_init(&o_done[q], 1);
     }
     mbar_init(v_clean, 1);
@@ -159,7 +184,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
                       kvh * g, tile.q_row0 + tile.tok0 + q * tile.ntok, q_full);
       for (int i = 0; i < 2 * n_kt; ++i) {
         const int st = i % RS;
-        const int j = kt0 + (i >> 1);  // absolute key tile
+        const int jr = ring_tile(i, nq, n_kt);  // relative key tile of ring item i
+        const bool is_v = ring_is_v(i, nq, n_kt);
+        const int j = kt0 + jr;                 // absolute key tile
         const int pg0 = j * kPagesPerTile;
         const int np = min(kPagesPerTile, npages_req - pg0);
         uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
@@ -171,7 +198,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
             set_device_error(a.err, kDevErrPageRange);
             page = 0;  // fetch a valid page instead; the output is undefined anyway
           }
-          const int32_t slice = (int32_t)((page * 2 + (i & 1)) * a.Hkv + kvh);
+          const int32_t slice = (int32_t)((page * 2 + (is_v ? 1 : 0)) * a.Hkv + kvh);
 #pragma unroll
           for (int b = 0; b < L::KB; ++b)
             tma_load_3d(buf + b * (kKeys * 128) + pgi * (kP * 128), &prm.tmap_kv, b * 64, 0, slice,
@@ -182,7 +209,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
     __syncwarp();
     if (last_partial) {
       // last V tile: rows past the request's last key must hold finite values
-      const int i = 2 * n_kt - 1, st = i % RS;
+      const int i = 2 * n_kt - 1, st = i % RS;  // V of the last tile is the last ring item
       const int tile_keys = tile.kv_len - (kt0 + n_kt - 1) * kKeys;
       uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
       mbar_wait(&ring_full[st], (i / RS) & 1, a.err);
@@ -226,6 +253,50 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
       mbar_wait(q_full, 0, a.err);
       mbar_wait(&ring_full[0], 0, a.err);
       tc_fence_after();
+      if (nq == 1) {
+        // single Q tile: S double-buffered in TMEM columns [0,128) and [128,256)
+        auto issue_s1 = [&](int b, int st) {
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
+            const uint32_t koff = (k >> 2) * (kKeys * 128) + (k & 3) * 32;
+            tc_mma_ss(tmem + b * 128, desc_kmajor(sQ + off), desc_kmajor(sR + st * L::T_BYTES + koff),
+                      idesc_s, k > 0 ? 1u : 0u);
+          }
+          tc_commit(&s_full[b]);
+        };
+        issue_s1(0, 0);
+        tc_commit(&ring_empty[0]);
+        if (n_kt > 1) {
+          const int ik = ring_k_index(1), sk = ik % RS;
+          mbar_wait(&ring_full[sk], (ik / RS) & 1, a.err);
+          tc_fence_after();
+          issue_s1(1, sk);
+          tc_commit(&ring_empty[sk]);
+        }
+        for (int j = 0; j < n_kt; ++j) {
+          const int b = j & 1;
+          const int iv = ring_v_index(j, n_kt), sv = iv % RS;
+          mbar_wait(&ring_full[sv], (iv / RS) & 1, a.err);
+          if (j == n_kt - 1 && last_partial) mbar_wait(v_clean, 0, a.err);
+          mbar_wait(&p_full[b], (j >> 1) & 1, a.err);
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kKeys / 16; ++k)
+            tc_mma_ts(tmem + 256, tmem + b * 128 + k * 8,
+                      desc_mnmajor(sR + sv * L::T_BYTES + k * (16 * 128), kKeys * 128), idesc_o,
+                      (j > 0 || k > 0) ? 1u : 0u);
+          tc_commit(&o_done[0]);
+          tc_commit(&ring_empty[sv]);
+          if (j + 2 < n_kt) {  // S(j+2) into the buffer PV(j) just read
+            const int ik = ring_k_index(j + 2), sk = ik % RS;
+            mbar_wait(&ring_full[sk], (ik / RS) & 1, a.err);
+            tc_fence_after();
+            issue_s1(b, sk);
+            tc_commit(&ring_empty[sk]);
+          }
+        }
+      } else {
       for (int q = 0; q < nq; ++q) issue_s(q, 0);
       tc_commit(&ring_empty[0]);
       for (int j = 0; j < n_kt; ++j) {
@@ -250,13 +321,13 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
         tc_commit(&ring_empty[sv]);
         if (j + 1 < n_kt) tc_commit(&ring_empty[sk]);
       }
+      }
     }
   } else if (warp / 4 < nq && (warp & 3) < ((warp >> 2) == 0 ? act0 : act1)) {
     // ------------------------------------------------------------- softmax
     const int q = warp >> 2;
     const int row = tid & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tmem_s = tmem + q * 128 + lane_off;
     const uint32_t tmem_o = tmem + 256 + q * 128 + lane_off;
     const int q_ntok = q == 0 ? tile.ntok : tile.ntok1;
     const int q_tok0 = tile.tok0 + q * tile.ntok;  // first token of this Q tile
@@ -267,7 +338,11 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
     float m_run = -INFINITY, l_run = 0.f;
 
     for (int j = 0; j < n_kt; ++j) {
-      mbar_wait(&s_full[q], j & 1, a.err);
+      // S buffer of this tile: the tile's own (pairs) or alternating (single tile)
+      const int b = nq == 2 ? q : (j & 1);
+      const uint32_t ph = nq == 2 ? (j & 1) : ((j >> 1) & 1);
+      const uint32_t tmem_s = tmem + b * 128 + lane_off;
+      mbar_wait(&s_full[b], ph, a.err);
       tc_fence_after();
       float s[kKeys];
 #pragma unroll
@@ -336,10 +411,14 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
           }
         }
       }
+      // o_done must never run two phases ahead of this thread's parity waits:
+      // with S double-buffered, S(j) done only implies PV(j-2) done, so consume
+      // the phase of PV(j-1) before PV(j) can be issued (normally no wait).
+      if (j > 0 && !warp_rescale) mbar_wait(&o_done[q], (j - 1) & 1, a.err);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[q]);
+      if (lane == 0) mbar_arrive(&p_full[b]);
     }
 
     // ---- epilogue: O / l -> bf16 rows of out; lse

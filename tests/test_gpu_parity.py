@@ -102,6 +102,16 @@ def test_edge_cases(dev, case):
     _run_both(wl, dev)
 
 
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 1, 128), (12, 1, 128), (16, 2, 64)])
+def test_tensor_core_decode_tile_counts(dev, Hq, Hkv, d):
+    """GQA decode runs as single-tile tensor-core items with S double-buffered:
+    kv lengths around 128-key tile boundaries give 1..17 tiles per item, odd and
+    even, full and ragged last tiles, split and unsplit requests."""
+    kvs = [1, 2, 127, 128, 129, 200, 255, 256, 257, 384, 385, 1000, 2047, 2048, 2049]
+    wl = make_random_workload(113 + Hq, Hq, Hkv, d, 16, [(1, kv) for kv in kvs], extra_pages=5)
+    _run_both(wl, dev)
+
+
 def test_decode_kv_len_one_returns_v(dev):
     from gpu_support import gpu_fill, gpu_step, new_pool
     wl = make_random_workload(111, 8, 2, 128, 16, [(1, 1), (1, 1)])
