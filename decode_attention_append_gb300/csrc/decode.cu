@@ -141,10 +141,13 @@ decode_splitkv_kernel(const DecodeArgs a) {
   uint8_t* gring = ring + grp * S::NSTAGE * S::STAGE;
   const bool producer = (wh == 0 && lane == 0);
 
-  auto issue = [&](int k) {
+  // page id of the group's k-th page (the producer loads the next one a page
+  // ahead, so the global-load latency is off the refill path)
+  auto page_id = [&](int k) -> int64_t {
+    return k < my_n ? (int64_t)__ldg(a.page_indices + u.page_base + pg_lo + grp + k * S::NPG) : -1;
+  };
+  auto issue = [&](int k, int64_t page) {
     const int stage = k % S::NSTAGE;
-    const int pg = pg_lo + grp + k * S::NPG;
-    const int64_t page = a.page_indices[u.page_base + pg];
     if (page < 0 || page >= a.num_pages) {
       set_device_error(a.err, kDevErrPageRange);
       mbar_arrive(&gfull[stage]);  // completes the phase with no bytes; data is stale
@@ -158,9 +161,14 @@ decode_splitkv_kernel(const DecodeArgs a) {
     bulk_g2s(dst + S::SLICE, vp, S::SLICE, &gfull[stage]);
   };
 
+  int64_t next_page = -1;  // producer: id of page k + NSTAGE
   if (producer) {
     const int n0 = my_n < S::NSTAGE ? my_n : S::NSTAGE;
-    for (int k = 0; k < n0; ++k) issue(k);
+    int64_t ids[S::NSTAGE];
+#pragma unroll
+    for (int k = 0; k < S::NSTAGE; ++k) ids[k] = page_id(k);
+    for (int k = 0; k < n0; ++k) issue(k, ids[k]);
+    next_page = page_id(S::NSTAGE);
   }
 
   // q rows of this warp's heads, scaled into the log2 domain
@@ -285,7 +293,8 @@ decode_splitkv_kernel(const DecodeArgs a) {
     if (lane == 0) mbar_arrive(&gempty[stage]);
     if (producer && k + S::NSTAGE < my_n) {
       mbar_wait(&gempty[stage], parity, a.err);
-      issue(k + S::NSTAGE);
+      issue(k + S::NSTAGE, next_page);
+      next_page = page_id(k + S::NSTAGE + 1);
     }
   }
 

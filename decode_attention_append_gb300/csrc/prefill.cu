@@ -174,6 +174,16 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
+    // Page ids of ring item i: lane l (< 8) holds the id of the item's l-th
+    // page.  Fetched with one coalesced load per item, one item ahead, so its
+    // latency overlaps the wait for a free stage; each lane then issues the
+    // TMA boxes of its own page.
+    auto load_ids = [&](int i) -> int64_t {
+      if (i >= 2 * n_kt) return -1;
+      const int pg0 = (kt0 + ring_tile(i, nq, n_kt)) * kPagesPerTile;
+      const int np = min(kPagesPerTile, npages_req - pg0);
+      return lane < np ? (int64_t)__ldg(a.page_indices + tile.page_base + pg0 + lane) : -1;
+    };
     if (lane == 0) {
       const int tpt = one_token ? 1 : kRows / g;
       const void* tmap_q = one_token ? (const void*)&prm.tmap_q1 : (const void*)&prm.tmap_q;
@@ -182,29 +192,33 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
         for (int b = 0; b < L::KB; ++b)
           tma_load_3d(smem + L::OFF_Q + q * L::Q_BYTES + b * (kRows * 128), tmap_q, b * 64,
                       kvh * g, tile.q_row0 + tile.tok0 + q * tile.ntok, q_full);
-      for (int i = 0; i < 2 * n_kt; ++i) {
-        const int st = i % RS;
-        const int jr = ring_tile(i, nq, n_kt);  // relative key tile of ring item i
-        const bool is_v = ring_is_v(i, nq, n_kt);
-        const int j = kt0 + jr;                 // absolute key tile
-        const int pg0 = j * kPagesPerTile;
-        const int np = min(kPagesPerTile, npages_req - pg0);
-        uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
+    }
+    int64_t pid = load_ids(0);
+    for (int i = 0; i < 2 * n_kt; ++i) {
+      const int64_t pid_next = load_ids(i + 1);
+      const int st = i % RS;
+      const bool is_v = ring_is_v(i, nq, n_kt);
+      const int pg0 = (kt0 + ring_tile(i, nq, n_kt)) * kPagesPerTile;
+      const int np = min(kPagesPerTile, npages_req - pg0);
+      uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
+      if (lane == 0) {
         if (i >= RS) mbar_wait(&ring_empty[st], ((i / RS) - 1) & 1, a.err);
         mbar_arrive_expect_tx(&ring_full[st], (uint32_t)(np * kP * D * 2));
-        for (int pgi = 0; pgi < np; ++pgi) {
-          int64_t page = a.page_indices[tile.page_base + pg0 + pgi];
-          if (page < 0 || page >= a.num_pages) {
-            set_device_error(a.err, kDevErrPageRange);
-            page = 0;  // fetch a valid page instead; the output is undefined anyway
-          }
-          const int32_t slice = (int32_t)((page * 2 + (is_v ? 1 : 0)) * a.Hkv + kvh);
-#pragma unroll
-          for (int b = 0; b < L::KB; ++b)
-            tma_load_3d(buf + b * (kKeys * 128) + pgi * (kP * 128), &prm.tmap_kv, b * 64, 0, slice,
-                        &ring_full[st]);
-        }
       }
+      __syncwarp();
+      if (lane < np) {
+        int64_t page = pid;
+        if (page < 0 || page >= a.num_pages) {
+          set_device_error(a.err, kDevErrPageRange);
+          page = 0;  // fetch a valid page instead; the output is undefined anyway
+        }
+        const int32_t slice = (int32_t)((page * 2 + (is_v ? 1 : 0)) * a.Hkv + kvh);
+#pragma unroll
+        for (int b = 0; b < L::KB; ++b)
+          tma_load_3d(buf + b * (kKeys * 128) + lane * (kP * 128), &prm.tmap_kv, b * 64, 0, slice,
+                      &ring_full[st]);
+      }
+      pid = pid_next;
     }
     __syncwarp();
     if (last_partial) {
