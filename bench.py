@@ -70,7 +70,7 @@ def step_accounting(wl, k=0):
     return dict(decode_bytes=dec_bytes, append_bytes=app_bytes, prefill_flops=pre_flops,
                 prefill_bytes=pre_bytes, nnz_new=nnz_new,
                 # work per kernel
-                tc_flops=pre_flops, tc_bytes=pre_bytes + (dec_bytes if tc_decode else 0),
+                tc_flops=pre_flops, tc_bytes=pre_bytes, tc_decode_bytes=dec_bytes if tc_decode else 0,
                 cuda_decode_bytes=0 if tc_decode else dec_bytes)
 
 
@@ -486,8 +486,7 @@ def main():
         n_launch = len(per_kernel[dom]) / args.steps
         t = mean_ms * 1e-3
         if dom == "prefill_tc":
-            # the tensor-core kernel runs the prefill tiles and (for g >= 4) the
-            # decode splits: its bound is whichever ideal time is larger
+            # the tensor-core prefill kernel: bound by whichever ideal time is larger
             fl, by = acc["tc_flops"] / n_launch, acc["tc_bytes"] / n_launch
             t_tensor, t_hbm = fl / (bf16 * 1e12), by / (hbm * 1e9)
             if t_tensor >= t_hbm:
@@ -499,10 +498,12 @@ def main():
             roof["ideal_fraction"] = (t_tensor + t_hbm) / t
             kfile = "prefill.cu"
         else:
-            kb = {"decode_splitkv": acc["cuda_decode_bytes"], "kv_append": acc["append_bytes"]}.get(dom, 0)
+            kb = {"decode_splitkv": acc["cuda_decode_bytes"], "decode_tc": acc["tc_decode_bytes"],
+                  "kv_append": acc["append_bytes"]}.get(dom, 0)
             roof = {"bound": "hbm", "achieved": kb / n_launch / t / 1e9, "peak": hbm, "unit": "GB/s",
                     "peak_source": f"{peak_src} HBM copy"}
-            kfile = {"decode_splitkv": "decode.cu", "kv_append": "append.cu"}.get(dom, "decode.cu")
+            kfile = {"decode_splitkv": "decode.cu", "decode_tc": "prefill.cu",
+                     "kv_append": "append.cu"}.get(dom, "decode.cu")
         roof["frac"] = roof["achieved"] / roof["peak"]
         roof["kernel"] = dom
         roof["mean_ms"] = mean_ms
@@ -527,8 +528,8 @@ def main():
         pm = float(np.mean(per_kernel["prefill_tc"]))
         line["prefill_tflops"] = acc["prefill_flops"] / (pm * 1e-3) / 1e12
     if acc["decode_bytes"]:
-        kern = "decode_splitkv" if acc["cuda_decode_bytes"] else "prefill_tc"
-        if kern in per_kernel and not acc["prefill_flops"]:
+        kern = "decode_splitkv" if acc["cuda_decode_bytes"] else "decode_tc"
+        if kern in per_kernel:
             dm = float(np.mean(per_kernel[kern]))
             line["decode_gbs"] = acc["decode_bytes"] / (dm * 1e-3) / 1e9
             line["decode_kernel"] = kern

@@ -153,7 +153,9 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
     a.pool = static_cast<const uint16_t*>(ls.kv_pages);
     a.page_indices = ls.page_indices;
     a.tiles = reinterpret_cast<const PrefillTile*>(ws + lay.off_tiles);
-    a.n_tiles = lay.n_tiles;
+    a.n_tiles = lay.n_tiles - lay.n_dec_tiles;
+    a.dec_tiles = a.tiles + a.n_tiles;
+    a.n_dec_tiles = lay.n_dec_tiles;
     a.Hq = dims.num_qo_heads;
     a.Hkv = dims.num_kv_heads;
     a.group = g;
@@ -167,7 +169,12 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
     a.part_o = part_o;
     a.part_lse = part_lse;
     a.err = ls.err;
-    if (run(kKernelPrefill, [&] { return launch_prefill(a, s); }) != cudaSuccess) return DAA_ERR_CUDA;
+    if (a.n_tiles > 0 &&
+        run(kKernelPrefill, [&] { return launch_prefill(a, s); }) != cudaSuccess)
+      return DAA_ERR_CUDA;
+    if (a.n_dec_tiles > 0 &&
+        run(kKernelTcDecode, [&] { return launch_tc_decode(a, s); }) != cudaSuccess)
+      return DAA_ERR_CUDA;
   }
   if (lay.n_units > 0) {
     DecodeArgs a{};

@@ -50,8 +50,10 @@ struct PrefillArgs {
   const uint16_t* q;
   const uint16_t* pool;
   const int32_t* page_indices;
-  const PrefillTile* tiles;     // device
+  const PrefillTile* tiles;     // device: prefill items
   int n_tiles;
+  const PrefillTile* dec_tiles; // device: one-token (decode) items
+  int n_dec_tiles;
   int Hq, Hkv, group, head_dim;
   int64_t num_pages;
   int nnz_qo;
@@ -65,7 +67,10 @@ struct PrefillArgs {
 };
 // Rows of packed (token, head) a prefill tile holds.
 constexpr int kPrefillTileRows = 128;
+// Tensor-core kernel over the prefill items (pairs of 128-row Q tiles) and
+// over the one-token decode items (a smaller instantiation, two CTAs per SM).
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_tc_decode(const PrefillArgs& a, cudaStream_t stream);
 
 // Everything one batch_attention call launches, given its plan in `scratch`
 // (the workspace, or the no-allocation entry point's static array).

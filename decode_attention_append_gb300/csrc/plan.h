@@ -60,6 +60,7 @@ enum KernelId : int32_t {
   kKernelDecode = 2,
   kKernelMerge = 3,
   kKernelPrefill = 4,
+  kKernelTcDecode = 5,
 };
 
 }  // namespace daa

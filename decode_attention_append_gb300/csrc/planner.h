@@ -47,7 +47,7 @@ inline daa_status plan_check_dims(const daa_dims& d) {
 
 // Offsets of the workspace sections (bytes).
 struct PlanLayout {
-  int n_units = 0, n_merges = 0, n_tiles = 0, n_parts = 0;
+  int n_units = 0, n_merges = 0, n_tiles = 0, n_dec_tiles = 0, n_parts = 0;
   size_t off_units = 0, off_merges = 0, off_tiles = 0, plan_bytes = 0;
   size_t off_part_o = 0, off_part_lse = 0, total = 0;
 };
@@ -166,12 +166,16 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
       if (!tiles.push_back(t)) return DAA_ERR_WORKSPACE;
     }
   }
-  // tensor-core items: most work first
+  // tensor-core items: prefill items, then one-token decode items (each group
+  // launches its own instantiation of the kernel), most work first
   std::sort(tiles.data(), tiles.data() + tiles.size(), [](const PrefillTile& x, const PrefillTile& y) {
+    const bool dx = x.qo_len == 1, dy = y.qo_len == 1;
+    if (dx != dy) return dy;
     if (x.work != y.work) return x.work > y.work;
     if (x.q_row0 != y.q_row0) return x.q_row0 < y.q_row0;
     return x.tok0 != y.tok0 ? x.tok0 < y.tok0 : x.key_lo < y.key_lo;
   });
+  for (size_t i = 0; i < tiles.size(); ++i) lay.n_dec_tiles += tiles.data()[i].qo_len == 1 ? 1 : 0;
 
   lay.n_units = (int)units.size();
   lay.n_merges = (int)merges.size();

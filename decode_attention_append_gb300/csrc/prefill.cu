@@ -18,7 +18,7 @@
 //   warp 8           TMA producer: Q tiles, then K_0, V_0, K_1, V_1, ... into a
 //                    ring of RS shared-memory stages (one 128-key tile each)
 //   warp 9           MMA issuer (one lane)
-// Tensor memory (512 columns): S_q / P_q at q*128, O_q at 256 + q*128.
+// Tensor memory: S_q / P_q at q*KT, O_q at 2*KT + q*D (512 columns for pairs).
 //   S_q = Q_q K_j^T      A = Q (smem), B = K (smem), fp32 S in TMEM
 //   P_q (bf16) overwrites the first 64 columns of S_q (softmax, tcgen05.st)
 //   O_q += P_q V_j       A = P (TMEM), B = V (smem, MN-major), fp32 O in TMEM
@@ -41,13 +41,7 @@ namespace daa {
 namespace {
 
 constexpr int kP = 16;
-constexpr int kRows = kPrefillTileRows;  // 128
-constexpr int kKeys = 128;               // keys per K/V tile (8 pages)
-constexpr int kPagesPerTile = kKeys / kP;
-constexpr int kNumWarps = 10;
-constexpr int kThreads = 32 * kNumWarps;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kRows = kPrefillTileRows;  // 128 packed query rows per Q tile
 constexpr float kRescaleThreshold = 8.0f;  // log2 domain
 
 struct __align__(64) PrefillParams {
@@ -55,16 +49,31 @@ struct __align__(64) PrefillParams {
   CUtensorMap tmap_q1;    // the same view, box {64, g, 1} (one-token decode items)
   CUtensorMap tmap_kv;    // pool viewed as [num_pages*2*Hkv][P][d], box {64, P, 1}
   PrefillArgs a;
+  const PrefillTile* tiles;
 };
 
-template <int D>
-struct Smem {
+// One instantiation of the kernel: head dim D, KT keys per K/V tile, at most
+// NQX Q tiles per CTA, MIN_BLOCKS CTAs meant to share an SM.
+//   <D, 128, 2, 1>  prefill pairs: 224 KB of shared memory, 512 TMEM columns
+//   <D,  64, 1, 2>  decode splits: ~100 KB, 256 TMEM columns, two CTAs per SM
+//                   (two independent TMA producers per SM stream K/V faster
+//                   than one)
+template <int D_, int KT_, int NQX_, int MINB_>
+struct TcCfg {
+  static constexpr int D = D_, KT = KT_, NQX = NQX_, MIN_BLOCKS = MINB_;
+  static constexpr int PPT = KT / kP;               // pages per K/V tile
   static constexpr int KB = D / 64;                 // 64-column (128-byte) blocks per row
+  static constexpr int THREADS = 32 * (4 * NQX + 2);
+  static constexpr int PRODUCER = 4 * NQX;          // warp ids
+  static constexpr int MMA = 4 * NQX + 1;
   static constexpr int Q_BYTES = kRows * D * 2;
-  static constexpr int T_BYTES = kKeys * D * 2;     // one K or V tile
-  static constexpr int RS = D == 128 ? 5 : 8;       // ring stages
-  static constexpr int OFF_Q = 0;                   // [2]
-  static constexpr int OFF_RING = OFF_Q + 2 * Q_BYTES;
+  static constexpr int T_BYTES = KT * D * 2;        // one K or V tile
+  static constexpr int BUDGET = MINB_ == 1 ? 231424 : 114688;
+  static constexpr int FIXED = NQX * Q_BYTES + 512 + 1024;
+  static constexpr int RS_FIT = (BUDGET - FIXED) / T_BYTES;
+  static constexpr int RS = RS_FIT < 12 ? RS_FIT : 12;  // ring stages
+  static constexpr int OFF_Q = 0;                   // [NQX]
+  static constexpr int OFF_RING = NQX * Q_BYTES;
   static constexpr int OFF_BAR = OFF_RING + RS * T_BYTES;
   // barriers: q_full, ring_full[RS], ring_empty[RS], s_full[2], p_full[2],
   // o_done[2], v_clean
@@ -72,8 +81,16 @@ struct Smem {
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_TMEM + 16;
   static constexpr int ALLOC = BYTES + 1024;        // slack to align the base to 1024
-  static constexpr int TMEM_COLS = 512;
+  // TMEM: S / P buffers at columns 0 and KT, O_q at O_COL + q * D
+  static constexpr int O_COL = 2 * KT;
+  static constexpr int TMEM_COLS = 2 * KT + NQX * D <= 256 ? 256 : 512;
+  static_assert(RS >= 3, "ring too shallow");
+  static_assert(ALLOC <= (MINB_ == 1 ? 232448 : 115712), "shared memory budget");
 };
+using CfgPrefill128 = TcCfg<128, 128, 2, 1>;
+using CfgPrefill64 = TcCfg<64, 128, 2, 1>;
+using CfgDecode128 = TcCfg<128, 64, 1, 2>;
+using CfgDecode64 = TcCfg<64, 64, 1, 2>;
 
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t addr) {
   // K-major, 128-byte swizzle: 8-row atoms of 1024 bytes stacked along M/N.
@@ -107,11 +124,11 @@ __device__ __forceinline__ bool ring_is_v(int i, int nq, int n) {
 __device__ __forceinline__ int ring_k_index(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int ring_v_index(int j, int n) { return j <= n - 2 ? 2 * j + 2 : 2 * n - 1; }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
-  using L = Smem<D>;
-  constexpr int RS = L::RS;
+  using L = C;
+  constexpr int D = C::D, KT = C::KT, PPT = C::PPT, RS = C::RS;
   const PrefillArgs& a = prm.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -126,11 +143,11 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
   uint64_t* v_clean = o_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
 
-  const PrefillTile tile = a.tiles[blockIdx.x];
+  const PrefillTile tile = prm.tiles[blockIdx.x];
   const int kvh = blockIdx.y;
   const int g = a.group;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nq = tile.ntok1 > 0 ? 2 : 1;  // Q tiles in this CTA
+  const int nq = C::NQX == 2 && tile.ntok1 > 0 ? 2 : 1;  // Q tiles in this CTA
   const bool one_token = tile.ntok == 1 && nq == 1;
 
   // key tiles kt0 .. kt0 + n_kt - 1 cover keys [key_lo, kend); causal rows mask
@@ -139,10 +156,10 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
   const int ntok_all = tile.ntok + tile.ntok1;
   const int kv_end = a.causal ? min(tile.kv_len, pos_first + ntok_all) : tile.kv_len;
   const int kend = min(kv_end, tile.key_hi);
-  const int kt0 = tile.key_lo / kKeys;
-  const int n_kt = (kend + kKeys - 1) / kKeys - kt0;
+  const int kt0 = tile.key_lo / KT;
+  const int n_kt = (kend + KT - 1) / KT - kt0;
   const int npages_req = (tile.kv_len + kP - 1) / kP;
-  const bool last_partial = tile.kv_len - (kt0 + n_kt - 1) * kKeys < kKeys;
+  const bool last_partial = tile.kv_len - (kt0 + n_kt - 1) * KT < KT;
   // warps of each Q tile that hold real rows (the others skip the softmax)
   const int act0 = (tile.ntok * g + 31) / 32;
   const int act1 = (tile.ntok1 * g + 31) / 32;
@@ -163,7 +180,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
     mbar_init(v_clean, 1);
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == C::MMA) {
     tmem_alloc(tmem_slot, L::TMEM_COLS);
     tmem_relinquish();
   }
@@ -172,7 +189,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kProducerWarp) {
+  if (warp == C::PRODUCER) {
     // ------------------------------------------------------------ producer
     // Page ids of ring item i: lane l (< 8) holds the id of the item's l-th
     // page.  Fetched with one coalesced load per item, one item ahead, so its
@@ -180,8 +197,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
     // TMA boxes of its own page.
     auto load_ids = [&](int i) -> int64_t {
       if (i >= 2 * n_kt) return -1;
-      const int pg0 = (kt0 + ring_tile(i, nq, n_kt)) * kPagesPerTile;
-      const int np = min(kPagesPerTile, npages_req - pg0);
+      const int pg0 = (kt0 + ring_tile(i, nq, n_kt)) * PPT;
+      const int np = min(PPT, npages_req - pg0);
       return lane < np ? (int64_t)__ldg(a.page_indices + tile.page_base + pg0 + lane) : -1;
     };
     if (lane == 0) {
@@ -198,8 +215,8 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
       const int64_t pid_next = load_ids(i + 1);
       const int st = i % RS;
       const bool is_v = ring_is_v(i, nq, n_kt);
-      const int pg0 = (kt0 + ring_tile(i, nq, n_kt)) * kPagesPerTile;
-      const int np = min(kPagesPerTile, npages_req - pg0);
+      const int pg0 = (kt0 + ring_tile(i, nq, n_kt)) * PPT;
+      const int np = min(PPT, npages_req - pg0);
       uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
       if (lane == 0) {
         if (i >= RS) mbar_wait(&ring_empty[st], ((i / RS) - 1) & 1, a.err);
@@ -215,7 +232,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
         const int32_t slice = (int32_t)((page * 2 + (is_v ? 1 : 0)) * a.Hkv + kvh);
 #pragma unroll
         for (int b = 0; b < L::KB; ++b)
-          tma_load_3d(buf + b * (kKeys * 128) + lane * (kP * 128), &prm.tmap_kv, b * 64, 0, slice,
+          tma_load_3d(buf + b * (KT * 128) + lane * (kP * 128), &prm.tmap_kv, b * 64, 0, slice,
                       &ring_full[st]);
       }
       pid = pid_next;
@@ -224,23 +241,23 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
     if (last_partial) {
       // last V tile: rows past the request's last key must hold finite values
       const int i = 2 * n_kt - 1, st = i % RS;  // V of the last tile is the last ring item
-      const int tile_keys = tile.kv_len - (kt0 + n_kt - 1) * kKeys;
+      const int tile_keys = tile.kv_len - (kt0 + n_kt - 1) * KT;
       uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
       mbar_wait(&ring_full[st], (i / RS) & 1, a.err);
-      const int nz = (kKeys - tile_keys) * 8;  // 16-byte chunks per 64-column block
+      const int nz = (KT - tile_keys) * 8;  // 16-byte chunks per 64-column block
       for (int idx = lane; idx < nz * L::KB; idx += 32) {
         const int b = idx / nz, rem = idx - b * nz;
         const int r = tile_keys + (rem >> 3), ch = rem & 7;
-        *reinterpret_cast<uint4*>(buf + b * (kKeys * 128) + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(buf + b * (KT * 128) + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(v_clean);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == C::MMA) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0, 0);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, KT, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 0, 1);
       const uint32_t sQ = smem_u32(smem + L::OFF_Q);
       const uint32_t sR = smem_u32(smem + L::OFF_RING);
@@ -248,18 +265,18 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
-          const uint32_t koff = (k >> 2) * (kKeys * 128) + (k & 3) * 32;
-          tc_mma_ss(tmem + q * 128, desc_kmajor(sQ + q * L::Q_BYTES + off),
+          const uint32_t koff = (k >> 2) * (KT * 128) + (k & 3) * 32;
+          tc_mma_ss(tmem + q * KT, desc_kmajor(sQ + q * L::Q_BYTES + off),
                     desc_kmajor(sR + st * L::T_BYTES + koff), idesc_s, k > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[q]);
       };
       auto issue_pv = [&](int q, int st, int j) {
 #pragma unroll
-        for (int k = 0; k < kKeys / 16; ++k) {
+        for (int k = 0; k < KT / 16; ++k) {
           const uint32_t voff = k * (16 * 128);
-          tc_mma_ts(tmem + 256 + q * 128, tmem + q * 128 + k * 8,
-                    desc_mnmajor(sR + st * L::T_BYTES + voff, kKeys * 128), idesc_o,
+          tc_mma_ts(tmem + C::O_COL + q * D, tmem + q * KT + k * 8,
+                    desc_mnmajor(sR + st * L::T_BYTES + voff, KT * 128), idesc_o,
                     (j > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit(&o_done[q]);
@@ -268,13 +285,13 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
       mbar_wait(&ring_full[0], 0, a.err);
       tc_fence_after();
       if (nq == 1) {
-        // single Q tile: S double-buffered in TMEM columns [0,128) and [128,256)
+        // single Q tile: S double-buffered in TMEM columns [0, KT) and [KT, 2 KT)
         auto issue_s1 = [&](int b, int st) {
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
-            const uint32_t koff = (k >> 2) * (kKeys * 128) + (k & 3) * 32;
-            tc_mma_ss(tmem + b * 128, desc_kmajor(sQ + off), desc_kmajor(sR + st * L::T_BYTES + koff),
+            const uint32_t koff = (k >> 2) * (KT * 128) + (k & 3) * 32;
+            tc_mma_ss(tmem + b * KT, desc_kmajor(sQ + off), desc_kmajor(sR + st * L::T_BYTES + koff),
                       idesc_s, k > 0 ? 1u : 0u);
           }
           tc_commit(&s_full[b]);
@@ -296,9 +313,9 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
           mbar_wait(&p_full[b], (j >> 1) & 1, a.err);
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < kKeys / 16; ++k)
-            tc_mma_ts(tmem + 256, tmem + b * 128 + k * 8,
-                      desc_mnmajor(sR + sv * L::T_BYTES + k * (16 * 128), kKeys * 128), idesc_o,
+          for (int k = 0; k < KT / 16; ++k)
+            tc_mma_ts(tmem + C::O_COL, tmem + b * KT + k * 8,
+                      desc_mnmajor(sR + sv * L::T_BYTES + k * (16 * 128), KT * 128), idesc_o,
                       (j > 0 || k > 0) ? 1u : 0u);
           tc_commit(&o_done[0]);
           tc_commit(&ring_empty[sv]);
@@ -310,7 +327,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
             tc_commit(&ring_empty[sk]);
           }
         }
-      } else {
+      } else if constexpr (C::NQX == 2) {
       for (int q = 0; q < nq; ++q) issue_s(q, 0);
       tc_commit(&ring_empty[0]);
       for (int j = 0; j < n_kt; ++j) {
@@ -342,7 +359,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
     const int q = warp >> 2;
     const int row = tid & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tmem_o = tmem + 256 + q * 128 + lane_off;
+    const uint32_t tmem_o = tmem + C::O_COL + q * D + lane_off;
     const int q_ntok = q == 0 ? tile.ntok : tile.ntok1;
     const int q_tok0 = tile.tok0 + q * tile.ntok;  // first token of this Q tile
     const int tl = row / g;
@@ -355,42 +372,45 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
       // S buffer of this tile: the tile's own (pairs) or alternating (single tile)
       const int b = nq == 2 ? q : (j & 1);
       const uint32_t ph = nq == 2 ? (j & 1) : ((j >> 1) & 1);
-      const uint32_t tmem_s = tmem + b * 128 + lane_off;
+      const uint32_t tmem_s = tmem + b * KT + lane_off;
       mbar_wait(&s_full[b], ph, a.err);
       tc_fence_after();
-      float s[kKeys];
+      float s[KT];
 #pragma unroll
-      for (int c = 0; c < kKeys; c += 32) tmem_ld32f(tmem_s + c, s + c);
+      for (int c = 0; c < KT; c += 32) tmem_ld32f(tmem_s + c, s + c);
       tmem_wait_ld();
-      const int lim = row_end - (kt0 + j) * kKeys;  // keys [(kt0+j)*128, .. + lim) are valid
-      if (!__all_sync(0xffffffffu, lim >= kKeys)) {
+      const int lim = row_end - (kt0 + j) * KT;  // keys [(kt0+j)*128, .. + lim) are valid
+      if (!__all_sync(0xffffffffu, lim >= KT)) {
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
+        for (int c = 0; c < KT; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
       }
       // row max of the raw scores (sm_scale > 0, so it commutes with scaling)
-      // (four independent chains over 32 columns each)
-      float mx[4];
+      // (independent chains over 32 columns each)
+      float mx[KT / 32];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < KT / 32; ++k) {
         mx[k] = s[32 * k];
 #pragma unroll
         for (int i2 = 1; i2 < 31; i2 += 2) mx[k] = fmax3(mx[k], s[32 * k + i2], s[32 * k + i2 + 1]);
         mx[k] = fmaxf(mx[k], s[32 * k + 31]);
       }
-      const float mt = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * sc;
+      float mt = mx[0];
+#pragma unroll
+      for (int k = 1; k < KT / 32; ++k) mt = fmaxf(mt, mx[k]);
+      mt *= sc;
       float m_use = m_run;
       float alpha = 1.f;
       if (mt > m_run + kRescaleThreshold) {
         m_use = mt;
         alpha = ex2_approx(m_run - mt);  // 0 on the first tile
       }
-      // P = 2^(s * scale - m) as bf16 pairs over the first 64 columns of S_q
+      // P = 2^(s * scale - m) as bf16 pairs over the first KT/2 columns of S
       // (the A operand of PV), 32 columns at a time so each chunk of s dies early
       const float2 sc2 = make_float2(sc, sc);
       const float2 nm2 = make_float2(-m_use, -m_use);
       float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int c = 0; c < kKeys / 2; c += 32) {
+      for (int c = 0; c < KT / 2; c += 32) {
         uint32_t r[32];
 #pragma unroll
         for (int i2 = 0; i2 < 32; ++i2) {
@@ -480,7 +500,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == C::MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, L::TMEM_COLS);
   }
@@ -505,35 +525,28 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-template <int D>
-cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
-  using L = Smem<D>;
+template <class C>
+cudaError_t launch_tc(const PrefillArgs& a, const PrefillTile* tiles, int n_tiles,
+                      cudaStream_t stream) {
+  if (n_tiles <= 0) return cudaSuccess;
+  constexpr int D = C::D;
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return cudaErrorNotSupported;
   PrefillParams prm;
   prm.a = a;
+  prm.tiles = tiles;
   const int g = a.group;
   const int tpt = kRows / g;
-  {
+  auto encode_q = [&](CUtensorMap* m, int tokens) {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.Hq, (cuuint64_t)a.nnz_qo};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.Hq * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)tpt};
+    cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)tokens};
     cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&prm.tmap_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.q, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.Hq, (cuuint64_t)a.nnz_qo};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.Hq * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)g, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&prm.tmap_q1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.q, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.q, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  if (!encode_q(&prm.tmap_q, tpt) || !encode_q(&prm.tmap_q1, 1)) return cudaErrorInvalidValue;
   {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)kP, (cuuint64_t)a.num_pages * 2 * a.Hkv};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)kP * D * 2};
@@ -544,19 +557,24 @@ cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  auto kern = prefill_tc_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  auto kern = prefill_tc_kernel<C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.n_tiles, a.Hkv);
-  kern<<<grid, kThreads, L::ALLOC, stream>>>(prm);
+  dim3 grid(n_tiles, a.Hkv);
+  kern<<<grid, C::THREADS, C::ALLOC, stream>>>(prm);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-  if (a.n_tiles <= 0) return cudaSuccess;
-  return a.head_dim == 128 ? launch_prefill_d<128>(a, stream) : launch_prefill_d<64>(a, stream);
+  return a.head_dim == 128 ? launch_tc<CfgPrefill128>(a, a.tiles, a.n_tiles, stream)
+                           : launch_tc<CfgPrefill64>(a, a.tiles, a.n_tiles, stream);
+}
+
+cudaError_t launch_tc_decode(const PrefillArgs& a, cudaStream_t stream) {
+  return a.head_dim == 128 ? launch_tc<CfgDecode128>(a, a.dec_tiles, a.n_dec_tiles, stream)
+                           : launch_tc<CfgDecode64>(a, a.dec_tiles, a.n_dec_tiles, stream);
 }
 
 }  // namespace daa

@@ -147,7 +147,7 @@ size_t daa_batch_attention_workspace_size(const int32_t* h_qo_indptr, const int3
  *                 work on the host, so the call never waits on the device
  *  batch          number of requests
  *  causal         1: keys j <= pos; 0: all kv_len keys
- *  sm_scale       score scale, e.g. 1/sqrt(head_dim)
+ *  sm_scale       score scale, e.g. 1/sqrt(head_dim); must be finite and > 0
  *  out            device, bf16 [nnz_qo][Hq][head_dim], written
  *  lse_out        device, fp32 [nnz_qo][Hq] natural-log LSE, or NULL
  *  workspace      device scratch of at least
@@ -223,7 +223,8 @@ daa_status daa_device_error(int32_t* code, int32_t reset);
  * are kept, older ones dropped).  daa_trace_read synchronises on the recorded
  * events and copies out up to `max_records` (kernel id, milliseconds) pairs in
  * launch order, returning how many were written, then clears the record.
- * Kernel ids: 1 kv_append, 2 decode split-KV, 3 softmax_merge, 4 prefill.
+ * Kernel ids: 1 kv_append, 2 decode split-KV (CUDA cores), 3 softmax_merge,
+ * 4 tensor-core prefill, 5 tensor-core decode split-KV.
  */
 daa_status daa_trace_enable(int32_t capacity);
 daa_status daa_trace_disable(void);
