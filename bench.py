@@ -175,9 +175,10 @@ class GpuStep:
     """Device-resident workload: pool with the cached prefixes, page table,
     the step's q / k_new / v_new, outputs and workspace."""
 
-    def __init__(self, wl, device, k=0):
+    def __init__(self, wl, device, k=0, fused=True):
         import decode_attention_append_gb300 as daa
         self.daa = daa
+        self.fused = fused
         self.wl, self.dev = wl, device
         self.pool = torch.full(wl.pool_shape(), 0x7FC1, dtype=torch.int16, device=device).view(torch.bfloat16)
         it = wl.initial_table()
@@ -206,8 +207,11 @@ class GpuStep:
         torch.cuda.synchronize()
 
     def step(self):
-        self.runner.append(self.k_new, self.v_new)
-        self.runner.run(self.q, out=self.out)
+        if self.fused:
+            self.runner.step(self.k_new, self.v_new, self.q, out=self.out)
+        else:
+            self.runner.append(self.k_new, self.v_new)
+            self.runner.run(self.q, out=self.out)
 
     def step_e2e(self, stream):
         """Public API call with host buffers: H2D inputs, append + attention, D2H out."""
@@ -217,11 +221,17 @@ class GpuStep:
         self.k_new.copy_(self.h_k, non_blocking=True)
         self.v_new.copy_(self.h_v, non_blocking=True)
         qo, kv, pi, ll = self.d_ints
-        self.daa.kv_append(self.k_new, self.v_new, self.pool, qo, pi, kv, ll)
-        self.daa.batch_attention(self.q, self.pool, qo, kv, pi, ll, self.wl.causal, self.wl.sm_scale,
-                                 out=self.out, workspace=self.runner.workspace,
-                                 host_indptr=(self.host_table["qo_indptr"], self.host_table["kv_indptr"],
-                                              self.host_table["last_page_len"]))
+        hosts = (self.host_table["qo_indptr"], self.host_table["kv_indptr"],
+                 self.host_table["last_page_len"])
+        if self.fused:
+            self.daa.append_attention(self.k_new, self.v_new, self.q, self.pool, qo, kv, pi, ll,
+                                      self.wl.causal, self.wl.sm_scale, out=self.out,
+                                      workspace=self.runner.workspace, host_indptr=hosts)
+        else:
+            self.daa.kv_append(self.k_new, self.v_new, self.pool, qo, pi, kv, ll)
+            self.daa.batch_attention(self.q, self.pool, qo, kv, pi, ll, self.wl.causal,
+                                     self.wl.sm_scale, out=self.out,
+                                     workspace=self.runner.workspace, host_indptr=hosts)
         self.h_out.copy_(self.out, non_blocking=True)
 
     def e2e_bytes(self):
@@ -350,6 +360,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="mha_decode")
+    ap.add_argument("--api", default="fused", choices=["fused", "two-call"],
+                    help="fused: one append_attention call per step; two-call: kv_append then "
+                         "batch_attention")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="profiling runs: timed steps only (no clock window, no traced or e2e pass)")
@@ -374,7 +387,9 @@ def main():
               "prefill_requests": summary["prefill_requests"], "kv_tokens": summary["kv_tokens"],
               "Hq": wl.num_qo_heads, "Hkv": wl.num_kv_heads, "head_dim": wl.head_dim,
               "page_size": wl.page_size, "num_pages": wl.num_pages,
-              "parallelism": f"replicas{args.gpus}", "compact_pool": bool(args.compact_pool)}
+              "parallelism": f"replicas{args.gpus}", "compact_pool": bool(args.compact_pool),
+              "api": ("append_attention" if args.api == "fused"
+                      else "kv_append + batch_attention")}
 
     if args.impl == "reference":
         if rank != 0:
@@ -412,7 +427,7 @@ def main():
             __graft_entry__.build()
     import decode_attention_append_gb300 as daa
 
-    g = GpuStep(wl, dev)
+    g = GpuStep(wl, dev, fused=args.api == "fused")
     flush_buf = None
     need_flush = algo_bytes < 2 * L2_BYTES
     if need_flush:

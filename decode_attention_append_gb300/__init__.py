@@ -77,6 +77,9 @@ def load_library():
         lib.daa_batch_attention.restype = i32
         lib.daa_batch_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, vp, vp,
                                             vp, sz, _Dims, vp]
+        lib.daa_append_attention.restype = i32
+        lib.daa_append_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32,
+                                             vp, vp, vp, sz, _Dims, vp]
         lib.daa_batch_attention_noalloc.restype = i32
         lib.daa_batch_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32,
                                                     vp, vp, _Dims, vp]
@@ -207,6 +210,51 @@ def batch_attention(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_l
     return out
 
 
+def append_attention(k_new, v_new, q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len,
+                     causal=True, sm_scale=None, out=None, lse=None, workspace=None,
+                     host_indptr=None, stream=None):
+    """``kv_append`` of this step's new K/V (rows laid out like ``q``) followed
+    by ``batch_attention``, in one call: same results, with the attention
+    kernels launched behind the append so that the work that does not read the
+    appended rows overlaps it.  Arguments as ``batch_attention``."""
+    lib = load_library()
+    _dev_bf16(k_new, "k_new"), _dev_bf16(v_new, "v_new")
+    _dev_bf16(q, "q"), _dev_bf16(kv_pages, "kv_pages")
+    for n, t in (("qo_indptr", qo_indptr), ("kv_indptr", kv_indptr), ("page_indices", page_indices),
+                 ("last_page_len", last_page_len)):
+        _dev_i32(t, n)
+    Hq, d = q.shape[1], q.shape[2]
+    dims = _dims(kv_pages, Hq)
+    if k_new.shape != (q.shape[0], dims.num_kv_heads, d) or v_new.shape != k_new.shape:
+        raise ValueError("k_new and v_new must be [nnz_qo, Hkv, head_dim]")
+    if sm_scale is None:
+        sm_scale = 1.0 / float(d) ** 0.5
+    if host_indptr is None:
+        host_indptr = (qo_indptr, kv_indptr, last_page_len)
+    hq, hk, hl = (_host_i32(x) for x in host_indptr)
+    batch = len(hq) - 1
+    if out is None:
+        out = torch.empty_like(q)
+    _dev_bf16(out, "out")
+    if lse is not None and not (lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous()):
+        raise TypeError("lse must be a contiguous fp32 CUDA tensor")
+    if workspace is None:
+        st = ctypes.c_int32(0)
+        need = lib.daa_batch_attention_workspace_size(_ptr(hq), _ptr(hk), _ptr(hl), batch, dims,
+                                                      ctypes.byref(st))
+        _check(st.value, "append_attention")
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.daa_append_attention(_ptr(k_new), _ptr(v_new), _ptr(q), _ptr(kv_pages),
+                                    _ptr(qo_indptr), _ptr(kv_indptr), _ptr(page_indices),
+                                    _ptr(last_page_len), _ptr(hq), _ptr(hk), _ptr(hl), batch,
+                                    int(bool(causal)), float(sm_scale), _ptr(out), _ptr(lse),
+                                    _ptr(workspace), ws_bytes, dims, _stream(stream)),
+           "append_attention")
+    return out
+
+
 def batch_attention_noalloc(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len,
                             host_indptr, causal=True, sm_scale=None, out=None, lse=None,
                             stream=None):
@@ -271,6 +319,15 @@ class BatchAttention:
         t = self.t
         kv_append(k_new, v_new, self.kv_pages, t.qo_indptr, t.page_indices, t.kv_indptr,
                   t.last_page_len, stream=stream)
+
+    def step(self, k_new, v_new, q, out=None, lse=None, stream=None):
+        """append + run in one call (``append_attention``)."""
+        t = self.t
+        return append_attention(k_new, v_new, q, self.kv_pages, t.qo_indptr, t.kv_indptr,
+                                t.page_indices, t.last_page_len, self.causal, self.sm_scale,
+                                out=out, lse=lse, workspace=self.workspace,
+                                host_indptr=(t.h_qo_indptr, t.h_kv_indptr, t.h_last_page_len),
+                                stream=stream)
 
     def run(self, q, out=None, lse=None, stream=None):
         t = self.t

@@ -130,6 +130,12 @@ cudaError_t traced(int32_t kid, cudaStream_t s, F&& launch) {
   return err;
 }
 
+bool tracing() {
+  Tracer& t = tracer();
+  std::lock_guard<std::mutex> g(t.mu);
+  return t.on;
+}
+
 std::vector<uint8_t>& staging() {
   thread_local std::vector<uint8_t> buf;
   return buf;
@@ -137,7 +143,8 @@ std::vector<uint8_t>& staging() {
 
 }  // namespace
 
-daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s, bool trace) {
+daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s, bool trace,
+                      bool after_append) {
   const daa_dims& dims = ls.dims;
   const int g = dims.num_qo_heads / dims.num_kv_heads;
   const float sc = ls.sm_scale * 1.4426950408889634f;
@@ -147,6 +154,9 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
   auto run = [&](int32_t kid, auto&& f) -> cudaError_t {
     return trace ? traced(kid, s, f) : f();
   };
+  // programmatic launches, except while the tracer brackets every launch with
+  // events (each kernel is then timed alone)
+  bool programmatic = after_append && !(trace && tracing());
   if (lay.n_tiles > 0) {
     PrefillArgs a{};
     a.q = static_cast<const uint16_t*>(ls.q);
@@ -169,12 +179,16 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
     a.part_o = part_o;
     a.part_lse = part_lse;
     a.err = ls.err;
-    if (a.n_tiles > 0 &&
-        run(kKernelPrefill, [&] { return launch_prefill(a, s); }) != cudaSuccess)
-      return DAA_ERR_CUDA;
-    if (a.n_dec_tiles > 0 &&
-        run(kKernelTcDecode, [&] { return launch_tc_decode(a, s); }) != cudaSuccess)
-      return DAA_ERR_CUDA;
+    if (a.n_tiles > 0) {
+      if (run(kKernelPrefill, [&] { return launch_prefill(a, s, programmatic); }) != cudaSuccess)
+        return DAA_ERR_CUDA;
+      programmatic = !(trace && tracing());
+    }
+    if (a.n_dec_tiles > 0) {
+      if (run(kKernelTcDecode, [&] { return launch_tc_decode(a, s, programmatic); }) != cudaSuccess)
+        return DAA_ERR_CUDA;
+      programmatic = !(trace && tracing());
+    }
   }
   if (lay.n_units > 0) {
     DecodeArgs a{};
@@ -194,7 +208,9 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
     a.part_o = part_o;
     a.part_lse = part_lse;
     a.err = ls.err;
-    if (run(kKernelDecode, [&] { return launch_decode(a, s); }) != cudaSuccess) return DAA_ERR_CUDA;
+    if (run(kKernelDecode, [&] { return launch_decode(a, s, programmatic); }) != cudaSuccess)
+      return DAA_ERR_CUDA;
+    programmatic = !(trace && tracing());
   }
   if (lay.n_merges > 0) {
     MergeArgs m{};
@@ -206,7 +222,8 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
     m.part_lse = part_lse;
     m.out = static_cast<uint16_t*>(ls.out);
     m.lse_out = ls.lse_out;
-    if (run(kKernelMerge, [&] { return launch_merge(m, s); }) != cudaSuccess) return DAA_ERR_CUDA;
+    if (run(kKernelMerge, [&] { return launch_merge(m, s, programmatic); }) != cudaSuccess)
+      return DAA_ERR_CUDA;
   }
   return DAA_OK;
 }
@@ -264,13 +281,20 @@ size_t daa_batch_attention_workspace_size(const int32_t* h_qo_indptr, const int3
   return st == DAA_OK ? pl.lay.total : 0;
 }
 
-daa_status daa_batch_attention(const void* q, const void* kv_pages, const int32_t* qo_indptr,
-                               const int32_t* kv_indptr, const int32_t* page_indices,
-                               const int32_t* last_page_len, const int32_t* h_qo_indptr,
-                               const int32_t* h_kv_indptr, const int32_t* h_last_page_len,
-                               int32_t batch, int32_t causal, float sm_scale, void* out,
-                               float* lse_out, void* workspace, size_t workspace_bytes,
-                               daa_dims dims, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of daa_batch_attention and daa_append_attention: validate, plan,
+// stage the plan, then (fused call) launch the append, then the attention.
+daa_status attention_call(const void* k_new, const void* v_new, const void* q,
+                          const void* kv_pages, const int32_t* qo_indptr,
+                          const int32_t* kv_indptr, const int32_t* page_indices,
+                          const int32_t* last_page_len, const int32_t* h_qo_indptr,
+                          const int32_t* h_kv_indptr, const int32_t* h_last_page_len,
+                          int32_t batch, int32_t causal, float sm_scale, void* out,
+                          float* lse_out, void* workspace, size_t workspace_bytes,
+                          const daa_dims& dims, void* stream, bool fused) {
   if (!(std::isfinite(sm_scale)) || !(sm_scale > 0.f)) return DAA_ERR_INVALID_ARG;
   HostPlan& pl = host_plan();
   daa_status st = make_plan(h_qo_indptr, h_kv_indptr, h_last_page_len, batch, dims, num_sms(), pl);
@@ -281,6 +305,10 @@ daa_status daa_batch_attention(const void* q, const void* kv_pages, const int32_
     return DAA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv_pages) || !aligned16(out)) return DAA_ERR_ALIGNMENT;
   if ((reinterpret_cast<uintptr_t>(lse_out) & 3) != 0) return DAA_ERR_ALIGNMENT;
+  if (fused) {
+    if (!k_new || !v_new) return DAA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return DAA_ERR_ALIGNMENT;
+  }
   if (!workspace || workspace_bytes < lay.total) return DAA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DAA_ERR_ALIGNMENT;
 
@@ -291,6 +319,16 @@ daa_status daa_batch_attention(const void* q, const void* kv_pages, const int32_
   plan_stage(lay, pl.units, pl.merges, pl.tiles, host.data());
   if (cudaMemcpyAsync(ws, host.data(), lay.plan_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return DAA_ERR_CUDA;
+  const int nnz_qo = h_qo_indptr[batch];
+  if (fused && nnz_qo > 0) {
+    int* err = device_error_word();
+    cudaError_t e = traced(kKernelAppend, s, [&] {
+      return launch_kv_append(k_new, v_new, const_cast<void*>(kv_pages), qo_indptr, page_indices,
+                              kv_indptr, last_page_len, batch, nnz_qo, dims.num_kv_heads,
+                              dims.head_dim, dims.num_pages, num_sms(), err, s);
+    });
+    if (e != cudaSuccess) return DAA_ERR_CUDA;
+  }
   LaunchSet ls{};
   ls.q = q;
   ls.kv_pages = kv_pages;
@@ -298,13 +336,42 @@ daa_status daa_batch_attention(const void* q, const void* kv_pages, const int32_
   ls.dims = dims;
   ls.causal = causal;
   ls.sm_scale = sm_scale;
-  ls.nnz_qo = h_qo_indptr[batch];
+  ls.nnz_qo = nnz_qo;
   ls.out = out;
   ls.lse_out = lse_out;
   ls.scratch = ws;
   ls.err = device_error_word();
   ls.sms = num_sms();
-  return launch_all(ls, lay, s, /*trace=*/true);
+  return launch_all(ls, lay, s, /*trace=*/true, /*after_append=*/fused && nnz_qo > 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+daa_status daa_batch_attention(const void* q, const void* kv_pages, const int32_t* qo_indptr,
+                               const int32_t* kv_indptr, const int32_t* page_indices,
+                               const int32_t* last_page_len, const int32_t* h_qo_indptr,
+                               const int32_t* h_kv_indptr, const int32_t* h_last_page_len,
+                               int32_t batch, int32_t causal, float sm_scale, void* out,
+                               float* lse_out, void* workspace, size_t workspace_bytes,
+                               daa_dims dims, void* stream) {
+  return attention_call(nullptr, nullptr, q, kv_pages, qo_indptr, kv_indptr, page_indices,
+                        last_page_len, h_qo_indptr, h_kv_indptr, h_last_page_len, batch, causal,
+                        sm_scale, out, lse_out, workspace, workspace_bytes, dims, stream, false);
+}
+
+daa_status daa_append_attention(const void* k_new, const void* v_new, const void* q,
+                                void* kv_pages, const int32_t* qo_indptr,
+                                const int32_t* kv_indptr, const int32_t* page_indices,
+                                const int32_t* last_page_len, const int32_t* h_qo_indptr,
+                                const int32_t* h_kv_indptr, const int32_t* h_last_page_len,
+                                int32_t batch, int32_t causal, float sm_scale, void* out,
+                                float* lse_out, void* workspace, size_t workspace_bytes,
+                                daa_dims dims, void* stream) {
+  return attention_call(k_new, v_new, q, kv_pages, qo_indptr, kv_indptr, page_indices,
+                        last_page_len, h_qo_indptr, h_kv_indptr, h_last_page_len, batch, causal,
+                        sm_scale, out, lse_out, workspace, workspace_bytes, dims, stream, true);
 }
 
 daa_status daa_device_error(int32_t* code, int32_t reset) {

@@ -43,6 +43,10 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
   constexpr int CH = D / 8;  // 16-byte chunks per (head, slot) row
   __shared__ int64_t s_dst[kAppendMaxRows];  // chunk index of (page, K, head 0, slot, 0); -1 = skip
 
+  // the attention kernels of a fused call may start their CTAs now: the ones
+  // that read appended rows wait for this grid to complete
+  if (threadIdx.x == 0) grid_dep_launch();
+
   const int per_row = 2 * Hkv * CH;
   const int64_t total = (int64_t)nnz_new * per_row;
   const int64_t first = (int64_t)blockIdx.x * chunks_per_cta;

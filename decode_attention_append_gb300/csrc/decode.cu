@@ -128,6 +128,7 @@ decode_splitkv_kernel(const DecodeArgs a) {
   const int my_n = npg_unit > grp ? (npg_unit - grp + S::NPG - 1) / S::NPG : 0;
 
   if (threadIdx.x == 0) {
+    grid_dep_launch();  // the merge pass may launch; it waits for this grid
     for (int i = 0; i < S::NPG * S::NSTAGE; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], S::NWH);
@@ -167,6 +168,9 @@ decode_splitkv_kernel(const DecodeArgs a) {
     int64_t ids[S::NSTAGE];
 #pragma unroll
     for (int k = 0; k < S::NSTAGE; ++k) ids[k] = page_id(k);
+    // only the split holding the request's last page reads a row appended in
+    // this step: it alone waits for the kernel launched before this one
+    if (u.tok_end >= u.kv_len) grid_dep_wait();
     for (int k = 0; k < n0; ++k) issue(k, ids[k]);
     next_page = page_id(S::NSTAGE);
   }
@@ -363,32 +367,32 @@ decode_splitkv_kernel(const DecodeArgs a) {
 }
 
 template <int D, int G>
-cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream, bool programmatic) {
   using S = DecodeShape<D, G>;
   auto kern = decode_splitkv_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.n_units, a.Hkv);
-  kern<<<grid, S::THREADS, S::SMEM, stream>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(a.n_units, a.Hkv), dim3(S::THREADS), S::SMEM, stream,
+                       programmatic, a);
 }
 
 template <int D>
-cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream, bool pr) {
   const int g = a.group;
-  if (g <= 1) return launch_decode_t<D, 1>(a, stream);
-  if (g <= 2) return launch_decode_t<D, 2>(a, stream);
-  if (g <= 4) return launch_decode_t<D, 4>(a, stream);
-  if (g <= 8) return launch_decode_t<D, 8>(a, stream);
-  if (g <= 12) return launch_decode_t<D, 12>(a, stream);
-  return launch_decode_t<D, 16>(a, stream);
+  if (g <= 1) return launch_decode_t<D, 1>(a, stream, pr);
+  if (g <= 2) return launch_decode_t<D, 2>(a, stream, pr);
+  if (g <= 4) return launch_decode_t<D, 4>(a, stream, pr);
+  if (g <= 8) return launch_decode_t<D, 8>(a, stream, pr);
+  if (g <= 12) return launch_decode_t<D, 12>(a, stream, pr);
+  return launch_decode_t<D, 16>(a, stream, pr);
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream, bool programmatic) {
   if (a.n_units <= 0) return cudaSuccess;
-  return a.head_dim == 128 ? launch_decode_d<128>(a, stream) : launch_decode_d<64>(a, stream);
+  return a.head_dim == 128 ? launch_decode_d<128>(a, stream, programmatic)
+                           : launch_decode_d<64>(a, stream, programmatic);
 }
 
 }  // namespace daa

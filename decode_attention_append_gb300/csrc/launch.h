@@ -11,6 +11,25 @@ namespace daa {
 // Address of this library's device error word on the current device.
 int* device_error_word();
 
+// Launch `kern` on `s`; with `programmatic`, as a programmatic dependent launch
+// (its CTAs may start while the previous kernel on the stream is still running
+// and must call grid_dep_wait before reading what that kernel writes).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, bool programmatic, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = programmatic ? attr : nullptr;
+  cfg.numAttrs = programmatic ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* pool,
                              const int32_t* append_indptr, const int32_t* page_indices,
                              const int32_t* kv_indptr, const int32_t* last_page_len, int batch,
@@ -33,7 +52,7 @@ struct DecodeArgs {
   float* part_lse;              // [n_parts][Hq] (log2 domain)
   int* err;
 };
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream, bool programmatic);
 
 struct MergeArgs {
   const MergeItem* items;       // device
@@ -44,7 +63,7 @@ struct MergeArgs {
   uint16_t* out;
   float* lse_out;
 };
-cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream, bool programmatic);
 
 struct PrefillArgs {
   const uint16_t* q;
@@ -69,8 +88,8 @@ struct PrefillArgs {
 constexpr int kPrefillTileRows = 128;
 // Tensor-core kernel over the prefill items (pairs of 128-row Q tiles) and
 // over the one-token decode items (a smaller instantiation, two CTAs per SM).
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
-cudaError_t launch_tc_decode(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, bool programmatic);
+cudaError_t launch_tc_decode(const PrefillArgs& a, cudaStream_t stream, bool programmatic);
 
 // Everything one batch_attention call launches, given its plan in `scratch`
 // (the workspace, or the no-allocation entry point's static array).
@@ -89,6 +108,18 @@ struct LaunchSet {
   int sms;
 };
 struct PlanLayout;
-daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s, bool trace);
+// The kernels run in the order prefill, decode, softmax_merge; each after the
+// first is a programmatic dependent launch, and so is the first when
+// `after_append` (this call's own kv_append kernel precedes it on the stream).
+// Ordering contract, kept by the kernels:
+//  * every CTA that reads rows the append wrote (all prefill CTAs, the last
+//    key split of each decode request) calls grid_dep_wait first; so does
+//    every softmax_merge CTA.  The completion of a kernel therefore implies the
+//    completion of the kernel before it, and the last kernel's completion (what
+//    later stream work waits for) implies that of the whole chain;
+//  * the other decode splits read only cached rows and overlap the kernel
+//    before them.
+daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s, bool trace,
+                      bool after_append);
 
 }  // namespace daa

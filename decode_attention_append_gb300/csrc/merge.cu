@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) softmax_merge_kernel(const M
   constexpr int EPL = D / 32;  // elements per lane
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = blockIdx.y * kMergeWarps + warp;
+  grid_dep_wait();  // the partials come from the decode kernel launched before
   if (hq >= a.Hq) return;
   const MergeItem it = a.items[blockIdx.x];
   const float* lse = a.part_lse + (int64_t)it.part_begin * a.Hq + hq;
@@ -62,14 +63,12 @@ __global__ void __launch_bounds__(32 * kMergeWarps) softmax_merge_kernel(const M
 
 }  // namespace
 
-cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream, bool programmatic) {
   if (a.n_items <= 0) return cudaSuccess;
-  dim3 grid(a.n_items, (a.Hq + kMergeWarps - 1) / kMergeWarps);
-  if (a.head_dim == 128)
-    softmax_merge_kernel<128><<<grid, 32 * kMergeWarps, 0, stream>>>(a);
-  else
-    softmax_merge_kernel<64><<<grid, 32 * kMergeWarps, 0, stream>>>(a);
-  return cudaGetLastError();
+  const dim3 grid(a.n_items, (a.Hq + kMergeWarps - 1) / kMergeWarps), block(32 * kMergeWarps);
+  return a.head_dim == 128
+             ? launch_kernel(softmax_merge_kernel<128>, grid, block, 0, stream, programmatic, a)
+             : launch_kernel(softmax_merge_kernel<64>, grid, block, 0, stream, programmatic, a);
 }
 
 }  // namespace daa

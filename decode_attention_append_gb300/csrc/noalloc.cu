@@ -120,5 +120,5 @@ extern "C" daa_status daa_batch_attention_noalloc(
   ls.scratch = scratch;
   ls.err = device_error_word();
   ls.sms = sms;
-  return launch_all(ls, lay, s, /*trace=*/false);
+  return launch_all(ls, lay, s, /*trace=*/false, /*after_append=*/false);
 }

@@ -187,6 +187,7 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (tid == 0) grid_dep_launch();  // the next kernel may start its CTAs
 
   if (warp == C::PRODUCER) {
     // ------------------------------------------------------------ producer
@@ -210,6 +211,10 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
                       kvh * g, tile.q_row0 + tile.tok0 + q * tile.ntok, q_full);
     }
     int64_t pid = load_ids(0);
+    // items whose keys reach the request's end read rows appended in this step
+    // (every prefill item; the last split of a decode request): they wait for
+    // the kernel launched before this one
+    if (tile.key_hi >= tile.kv_len) grid_dep_wait();
     for (int i = 0; i < 2 * n_kt; ++i) {
       const int64_t pid_next = load_ids(i + 1);
       const int st = i % RS;
@@ -538,7 +543,7 @@ EncodeTiledFn get_encode_fn() {
 
 template <class C, bool kDecode>
 cudaError_t launch_tc(const PrefillArgs& a, const PrefillTile* tiles, int n_tiles,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool programmatic) {
   if (n_tiles <= 0) return cudaSuccess;
   constexpr int D = C::D;
   EncodeTiledFn enc = get_encode_fn();
@@ -571,21 +576,20 @@ cudaError_t launch_tc(const PrefillArgs& a, const PrefillTile* tiles, int n_tile
   auto kern = kDecode ? decode_tc_kernel<C> : prefill_tc_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC);
   if (e != cudaSuccess) return e;
-  dim3 grid(n_tiles, a.Hkv);
-  kern<<<grid, C::THREADS, C::ALLOC, stream>>>(prm);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(n_tiles, a.Hkv), dim3(C::THREADS), C::ALLOC, stream, programmatic,
+                       prm);
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-  return a.head_dim == 128 ? launch_tc<CfgPrefill128, false>(a, a.tiles, a.n_tiles, stream)
-                           : launch_tc<CfgPrefill64, false>(a, a.tiles, a.n_tiles, stream);
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, bool pr) {
+  return a.head_dim == 128 ? launch_tc<CfgPrefill128, false>(a, a.tiles, a.n_tiles, stream, pr)
+                           : launch_tc<CfgPrefill64, false>(a, a.tiles, a.n_tiles, stream, pr);
 }
 
-cudaError_t launch_tc_decode(const PrefillArgs& a, cudaStream_t stream) {
-  return a.head_dim == 128 ? launch_tc<CfgDecode128, true>(a, a.dec_tiles, a.n_dec_tiles, stream)
-                           : launch_tc<CfgDecode64, true>(a, a.dec_tiles, a.n_dec_tiles, stream);
+cudaError_t launch_tc_decode(const PrefillArgs& a, cudaStream_t stream, bool pr) {
+  return a.head_dim == 128 ? launch_tc<CfgDecode128, true>(a, a.dec_tiles, a.n_dec_tiles, stream, pr)
+                           : launch_tc<CfgDecode64, true>(a, a.dec_tiles, a.n_dec_tiles, stream, pr);
 }
 
 }  // namespace daa

@@ -117,6 +117,17 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// Programmatic dependent launch (griddepcontrol, sm_90 and later).
+// grid_dep_wait: block the calling thread until the grid this one was launched
+// behind has completed and its writes are visible (immediate when the launch
+// was not programmatic).  grid_dep_launch: let the next programmatic launch on
+// the stream start its CTAs once every CTA of this grid has issued it (or
+// exited).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (TMA / tensor core reads of shared memory).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -135,9 +135,11 @@ size_t daa_batch_attention_workspace_size(const int32_t* h_qo_indptr, const int3
  *   out[row][h][:] = sum_{j in J} softmax_J(s)_j * V_r[j][hk][:]      (bf16, RNE)
  *   lse_out[row][h] = ln sum_{j in J} exp(s_j)                          (fp32)
  * where row = qo_indptr[r] + i and K_r / V_r are read from the request's pages.
- * Requests with qo_len = 1 run the split-KV decode kernel followed by the
- * softmax_merge pass; requests with qo_len > 1 run the tensor-core prefill
- * kernel.  Rows of requests with qo_len = 0 do not exist; nothing is written.
+ * Requests with qo_len > 1 run the tensor-core prefill kernel; requests with
+ * qo_len = 1 run a split-KV decode kernel (CUDA cores when a kv head serves
+ * fewer than 4 query heads, tensor cores otherwise) followed by the
+ * softmax_merge pass for the requests it split.  Rows of requests with
+ * qo_len = 0 do not exist; nothing is written.
  *
  *  q              device, bf16 [nnz_qo][Hq][head_dim]
  *  kv_pages       device, bf16 pool (read only)
@@ -164,6 +166,37 @@ daa_status daa_batch_attention(const void* q, const void* kv_pages, const int32_
                                int32_t batch, int32_t causal, float sm_scale, void* out,
                                float* lse_out, void* workspace, size_t workspace_bytes,
                                daa_dims dims, void* stream);
+
+/*
+ * daa_kv_append followed by daa_batch_attention in one call, on one plan
+ * ("Disaggregated prefill and decode", section "KV Messenger": entries are
+ * valid after the append and before attention; "Chunked prefill", #correctness:
+ * each chunk's new k, v are appended and attended to in the same step).
+ *
+ * The new tokens of request r are its query rows: k_new, v_new are
+ * [nnz_qo][Hkv][head_dim] with the row layout of q (append_indptr = qo_indptr,
+ * nnz_new = h_qo_indptr[batch]).  The result -- pool bytes, out, lse_out -- is
+ * exactly that of the two calls in sequence on the same stream.  What differs
+ * is the schedule: the plan copy is issued before the append, and the
+ * attention kernels are launched behind the append as programmatic dependent
+ * launches, so their set-up and the key splits that read only cached rows
+ * overlap the append (the CTAs that read an appended row wait for it).
+ *
+ *  k_new, v_new   device, bf16 [nnz_qo][Hkv][head_dim]
+ *  kv_pages       device, bf16 pool, written (the appended rows) and read
+ *  other arguments as daa_batch_attention, with the same workspace size
+ *  (daa_batch_attention_workspace_size).
+ * Errors: those of both calls, all checked on the host before anything is
+ * enqueued.
+ */
+daa_status daa_append_attention(const void* k_new, const void* v_new, const void* q,
+                                void* kv_pages, const int32_t* qo_indptr,
+                                const int32_t* kv_indptr, const int32_t* page_indices,
+                                const int32_t* last_page_len, const int32_t* h_qo_indptr,
+                                const int32_t* h_kv_indptr, const int32_t* h_last_page_len,
+                                int32_t batch, int32_t causal, float sm_scale, void* out,
+                                float* lse_out, void* workspace, size_t workspace_bytes,
+                                daa_dims dims, void* stream);
 
 /* Size of the device scratch array behind daa_batch_attention_noalloc (48 MiB). */
 #define DAA_NOALLOC_SCRATCH_BYTES (48u * 1024u * 1024u)

@@ -26,19 +26,23 @@ def gpu_fill(wl, pool, device):
                   t.last_page_len)
 
 
-def gpu_step(wl, pool, k, device, with_lse=True):
-    """Append step k's new K/V and run attention: (out bf16 cpu, lse fp32 cpu)."""
+def gpu_step(wl, pool, k, device, with_lse=True, fused=False):
+    """Append step k's new K/V and run attention: (out bf16 cpu, lse fp32 cpu).
+    fused: one append_attention call instead of kv_append + batch_attention."""
     st = wl.step_table(k)
     q, kn, vn = wl.step_inputs(k)
     tab = daa.PageTable.from_host(st["qo_indptr"], st["kv_indptr"], st["page_indices"],
                                   st["last_page_len"], device)
     runner = daa.BatchAttention(tab, wl.num_qo_heads, pool, causal=wl.causal, sm_scale=wl.sm_scale)
-    if kn.shape[0]:
-        runner.append(kn.to(device), vn.to(device))
     qd = q.to(device)
     lse = torch.full((q.shape[0], wl.num_qo_heads), float("nan"), device=device) if with_lse else None
     out = torch.full_like(qd, float("nan"))
-    runner.run(qd, out=out, lse=lse)
+    if fused:
+        runner.step(kn.to(device), vn.to(device), qd, out=out, lse=lse)
+    else:
+        if kn.shape[0]:
+            runner.append(kn.to(device), vn.to(device))
+        runner.run(qd, out=out, lse=lse)
     torch.cuda.synchronize()
     return out.cpu(), (lse.cpu() if lse is not None else None)
 

@@ -29,7 +29,8 @@ def _declared_symbols():
 def test_header_declares_the_boundary():
     syms = _declared_symbols()
     for s in ("daa_kv_append", "daa_batch_attention", "daa_batch_attention_workspace_size",
-              "daa_status_string", "daa_device_error", "daa_trace_enable", "daa_trace_read"):
+              "daa_append_attention", "daa_status_string", "daa_device_error", "daa_trace_enable",
+              "daa_trace_read"):
         assert s in syms
 
 
@@ -121,6 +122,26 @@ def test_null_pointers_rejected_before_any_launch(lib):
                                  float("nan"), None, None, None, 0, d, None)
     assert st == -1
     assert daa.STATUS[-1] == "invalid argument"
+
+
+def test_append_attention_rejects_before_any_launch(lib):
+    """The fused call validates both halves on the host: missing or misaligned
+    k_new / v_new, and everything batch_attention rejects."""
+    d = _dims()
+    qo = np.asarray([0, 1], np.int32)
+    kv = np.asarray([0, 1], np.int32)
+    last = np.asarray([1], np.int32)
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+    dev = lambda x: ctypes.c_void_p(x)  # noqa: E731  (never dereferenced: rejected first)
+    args = [dev(0x10000), dev(0x20000), dev(0x30000), dev(0x40000), dev(0x50000)]
+    ws = dev(0x100000)
+    call = lambda kn, vn, scale=0.125, lastp=last: lib.daa_append_attention(  # noqa: E731
+        kn, vn, dev(0x1000), *args, p(qo), p(kv), p(lastp), 1, 1, scale, dev(0x70000), None, ws,
+        1 << 20, d, None)
+    assert call(None, dev(0x2000)) == -1
+    assert call(dev(0x2008), dev(0x3000)) == -7
+    assert call(dev(0x2000), dev(0x3000), scale=0.0) == -1
+    assert call(dev(0x2000), dev(0x3000), lastp=np.asarray([0], np.int32)) == -2
 
 
 def test_misaligned_pointers_rejected(lib):

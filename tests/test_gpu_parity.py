@@ -42,7 +42,7 @@ def _check(out, lse, ref, ref_lse, what):
     return mx, mean, rel
 
 
-def _run_both(wl, dev, sel_rows=None, compare_pool=True):
+def _run_both(wl, dev, sel_rows=None, compare_pool=True, fused=False):
     from gpu_support import compact, gpu_fill, gpu_step, new_pool, pool_bits
     cw, mapping = compact(wl)
     opool = oracle_pool(cw)
@@ -50,7 +50,7 @@ def _run_both(wl, dev, sel_rows=None, compare_pool=True):
     gpu_fill(wl, gpool, dev)
     stats = []
     for k in range(len(wl.steps)):
-        out, lse = gpu_step(wl, gpool, k, dev)
+        out, lse = gpu_step(wl, gpool, k, dev, fused=fused)
         ref, ref_lse, _ = oracle_step(cw, opool, k, sel_rows=sel_rows)
         if sel_rows is not None:
             out, lse = out[sel_rows], lse[sel_rows]
@@ -159,6 +159,34 @@ def test_chunked_vs_one_shot_gpu(dev):
     assert np.array_equal(pool_bits(pc[pages]), pool_bits(po[pages]))
     diff = (torch.cat(chunks, 0).double() - one.double()).abs().max().item()
     assert diff <= 1e-2, diff
+
+
+@pytest.mark.parametrize("name", ["tiny_mixed", "mha_decode", "chunked_prefill_mixed",
+                                  "gqa_decode_shard"])
+def test_append_attention_against_oracle(dev, name):
+    """The fused call (append, then attention launched behind it as
+    programmatic dependent launches) against the oracle: pool bytes bit-exact,
+    outputs within the attention tolerance, every step."""
+    _run_both(make_workload(name), dev, fused=True)
+
+
+@pytest.mark.parametrize("case", [EDGE[1], EDGE[4], EDGE[7], EDGE[8]], ids=lambda c: f"seed{c[0]}")
+def test_append_attention_equals_two_calls(dev, case):
+    """Same kernels, same plan: the fused call and kv_append + batch_attention
+    give bit-identical pools, outputs and LSE (only the schedule differs)."""
+    from gpu_support import gpu_fill, gpu_step, new_pool, pool_bits
+    seed, Hq, Hkv, d, reqs, causal = case
+    wl = make_random_workload(seed, Hq, Hkv, d, 16, reqs, extra_pages=7)
+    wl.causal = causal
+    pa, pb = new_pool(wl, dev), new_pool(wl, dev)
+    gpu_fill(wl, pa, dev)
+    gpu_fill(wl, pb, dev)
+    for k in range(len(wl.steps)):
+        oa, la = gpu_step(wl, pa, k, dev, fused=True)
+        ob, lb = gpu_step(wl, pb, k, dev, fused=False)
+        assert torch.equal(oa.view(torch.int16), ob.view(torch.int16)), f"step {k}: out differs"
+        assert torch.equal(la, lb), f"step {k}: lse differs"
+    assert np.array_equal(pool_bits(pa), pool_bits(pb))
 
 
 def test_no_device_error_recorded(dev):
