@@ -194,7 +194,8 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
     // Page ids of ring item i: lane l (< 8) holds the id of the item's l-th
     // page.  Fetched with one coalesced load per item, one item ahead, so its
     // latency overlaps the wait for a free stage; each lane then issues the
-    // TMA boxes of its own page.
+    // TMA boxes of its own page (issue spread over lanes runs faster than
+    // from one lane; either way, 2 KB page boxes cap the per-SM load rate).
     auto load_ids = [&](int i) -> int64_t {
       if (i >= 2 * n_kt) return -1;
       const int pg0 = (kt0 + ring_tile(i, nq, n_kt)) * PPT;
@@ -260,102 +261,106 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
     }
   } else if (warp == C::MMA) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, KT, 0, 0);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 0, 1);
-      const uint32_t sQ = smem_u32(smem + L::OFF_Q);
-      const uint32_t sR = smem_u32(smem + L::OFF_RING);
-      auto issue_s = [&](int q, int st) {
+    // The whole warp runs this converged; one elected lane issues each MMA and
+    // commit (waits are taken by every lane, then the warp reconverges).
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, KT, 0, 0);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 0, 1);
+    const uint32_t sQ = smem_u32(smem + L::OFF_Q);
+    const uint32_t sR = smem_u32(smem + L::OFF_RING);
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      mbar_wait(bar, parity, a.err);
+      __syncwarp();
+    };
+    auto commit = [&](uint64_t* bar) {
+      if (elect_one()) tc_commit(bar);
+      __syncwarp();
+    };
+    // S = Q K^T into TMEM columns [col, col + KT): Q tile at sq, K tile in ring stage st
+    auto issue_s = [&](uint32_t col, uint32_t sq, int st) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
-          const uint32_t koff = (k >> 2) * (KT * 128) + (k & 3) * 32;
-          tc_mma_ss(tmem + q * KT, desc_kmajor(sQ + q * L::Q_BYTES + off),
-                    desc_kmajor(sR + st * L::T_BYTES + koff), idesc_s, k > 0 ? 1u : 0u);
-        }
-        tc_commit(&s_full[q]);
-      };
-      auto issue_pv = [&](int q, int st, int j) {
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
+        const uint32_t koff = (k >> 2) * (KT * 128) + (k & 3) * 32;
+        const uint64_t da = desc_kmajor(sq + off);
+        const uint64_t db = desc_kmajor(sR + st * L::T_BYTES + koff);
+        if (elect_one()) tc_mma_ss(tmem + col, da, db, idesc_s, k > 0 ? 1u : 0u);
+      }
+      __syncwarp();
+    };
+    // O (columns [ocol, ocol + D)) += P (bf16 in columns [pcol, pcol + KT/2)) V (ring stage st)
+    auto issue_pv = [&](uint32_t ocol, uint32_t pcol, int st, bool accumulate) {
 #pragma unroll
-        for (int k = 0; k < KT / 16; ++k) {
-          const uint32_t voff = k * (16 * 128);
-          tc_mma_ts(tmem + C::O_COL + q * D, tmem + q * KT + k * 8,
-                    desc_mnmajor(sR + st * L::T_BYTES + voff, KT * 128), idesc_o,
-                    (j > 0 || k > 0) ? 1u : 0u);
-        }
-        tc_commit(&o_done[q]);
-      };
-      mbar_wait(q_full, 0, a.err);
-      mbar_wait(&ring_full[0], 0, a.err);
-      tc_fence_after();
-      if (nq == 1) {
-        // single Q tile: S double-buffered in TMEM columns [0, KT) and [KT, 2 KT)
-        auto issue_s1 = [&](int b, int st) {
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
-            const uint32_t koff = (k >> 2) * (KT * 128) + (k & 3) * 32;
-            tc_mma_ss(tmem + b * KT, desc_kmajor(sQ + off), desc_kmajor(sR + st * L::T_BYTES + koff),
-                      idesc_s, k > 0 ? 1u : 0u);
-          }
-          tc_commit(&s_full[b]);
-        };
-        issue_s1(0, 0);
-        tc_commit(&ring_empty[0]);
-        if (n_kt > 1) {
-          const int ik = ring_k_index(1), sk = ik % RS;
-          mbar_wait(&ring_full[sk], (ik / RS) & 1, a.err);
+      for (int k = 0; k < KT / 16; ++k) {
+        const uint64_t db = desc_mnmajor(sR + st * L::T_BYTES + k * (16 * 128), KT * 128);
+        if (elect_one())
+          tc_mma_ts(tmem + ocol, tmem + pcol + k * 8, db, idesc_o, (accumulate || k > 0) ? 1u : 0u);
+      }
+      __syncwarp();
+    };
+    wait(q_full, 0);
+    wait(&ring_full[0], 0);
+    tc_fence_after();
+    if (nq == 1) {
+      // single Q tile: S double-buffered in TMEM columns [0, KT) and [KT, 2 KT)
+      issue_s(0, sQ, 0);
+      commit(&s_full[0]);
+      commit(&ring_empty[0]);
+      if (n_kt > 1) {
+        const int ik = ring_k_index(1), sk = ik % RS;
+        wait(&ring_full[sk], (ik / RS) & 1);
+        tc_fence_after();
+        issue_s(KT, sQ, sk);
+        commit(&s_full[1]);
+        commit(&ring_empty[sk]);
+      }
+      for (int j = 0; j < n_kt; ++j) {
+        const int b = j & 1;
+        const int iv = ring_v_index(j, n_kt), sv = iv % RS;
+        wait(&ring_full[sv], (iv / RS) & 1);
+        if (j == n_kt - 1 && last_partial) wait(v_clean, 0);
+        wait(&p_full[b], (j >> 1) & 1);
+        tc_fence_after();
+        issue_pv(C::O_COL, b * KT, sv, j > 0);
+        commit(&o_done[0]);
+        commit(&ring_empty[sv]);
+        if (j + 2 < n_kt) {  // S(j+2) into the buffer PV(j) just read
+          const int ik = ring_k_index(j + 2), sk = ik % RS;
+          wait(&ring_full[sk], (ik / RS) & 1);
           tc_fence_after();
-          issue_s1(1, sk);
-          tc_commit(&ring_empty[sk]);
+          issue_s(b * KT, sQ, sk);
+          commit(&s_full[b]);
+          commit(&ring_empty[sk]);
         }
-        for (int j = 0; j < n_kt; ++j) {
-          const int b = j & 1;
-          const int iv = ring_v_index(j, n_kt), sv = iv % RS;
-          mbar_wait(&ring_full[sv], (iv / RS) & 1, a.err);
-          if (j == n_kt - 1 && last_partial) mbar_wait(v_clean, 0, a.err);
-          mbar_wait(&p_full[b], (j >> 1) & 1, a.err);
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < KT / 16; ++k)
-            tc_mma_ts(tmem + C::O_COL, tmem + b * KT + k * 8,
-                      desc_mnmajor(sR + sv * L::T_BYTES + k * (16 * 128), KT * 128), idesc_o,
-                      (j > 0 || k > 0) ? 1u : 0u);
-          tc_commit(&o_done[0]);
-          tc_commit(&ring_empty[sv]);
-          if (j + 2 < n_kt) {  // S(j+2) into the buffer PV(j) just read
-            const int ik = ring_k_index(j + 2), sk = ik % RS;
-            mbar_wait(&ring_full[sk], (ik / RS) & 1, a.err);
-            tc_fence_after();
-            issue_s1(b, sk);
-            tc_commit(&ring_empty[sk]);
-          }
-        }
-      } else if constexpr (C::NQX == 2) {
-      for (int q = 0; q < nq; ++q) issue_s(q, 0);
-      tc_commit(&ring_empty[0]);
+      }
+    } else if constexpr (C::NQX == 2) {
+      for (int q = 0; q < nq; ++q) {
+        issue_s(q * KT, sQ + q * L::Q_BYTES, 0);
+        commit(&s_full[q]);
+      }
+      commit(&ring_empty[0]);
       for (int j = 0; j < n_kt; ++j) {
         const int iv = 2 * j + 1, sv = iv % RS;
         const int ik = 2 * j + 2, sk = ik % RS;
-        mbar_wait(&ring_full[sv], (iv / RS) & 1, a.err);
-        if (j == n_kt - 1 && last_partial) mbar_wait(v_clean, 0, a.err);
+        wait(&ring_full[sv], (iv / RS) & 1);
+        if (j == n_kt - 1 && last_partial) wait(v_clean, 0);
         bool k_ready = false;
         for (int q = 0; q < nq; ++q) {
-          mbar_wait(&p_full[q], j & 1, a.err);
+          wait(&p_full[q], j & 1);
           tc_fence_after();
-          issue_pv(q, sv, j);
+          issue_pv(C::O_COL + q * D, q * KT, sv, j > 0);
+          commit(&o_done[q]);
           if (j + 1 < n_kt) {
             if (!k_ready) {
-              mbar_wait(&ring_full[sk], (ik / RS) & 1, a.err);
+              wait(&ring_full[sk], (ik / RS) & 1);
               tc_fence_after();
               k_ready = true;
             }
-            issue_s(q, sk);
+            issue_s(q * KT, sQ + q * L::Q_BYTES, sk);
+            commit(&s_full[q]);
           }
         }
-        tc_commit(&ring_empty[sv]);
-        if (j + 1 < n_kt) tc_commit(&ring_empty[sk]);
-      }
+        commit(&ring_empty[sv]);
+        if (j + 1 < n_kt) commit(&ring_empty[sk]);
       }
     }
   } else if (warp / 4 < nq && (warp & 3) < ((warp >> 2) == 0 ? act0 : act1)) {

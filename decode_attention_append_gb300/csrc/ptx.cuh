@@ -169,6 +169,22 @@ __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// One lane of a converged warp (the same lane at every call while all 32 lanes
+// are active).  tcgen05.mma and tcgen05.commit are single-thread instructions;
+// issuing them as `if (elect_one()) ...` from a warp that runs the issue loop
+// converged keeps the loop and the operand descriptors in warp-uniform code.
+// Issued instead from a branch taken by one lane, with descriptors computed at
+// run time, the same MMA stream measured about half the tensor-pipe rate.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc], kind::f16.  A (M x 16 per MMA) sits in
 // TMEM as M lanes x 8 columns, two bf16 per 32-bit column (lower half first).
 __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
