@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libdaa.so")
-SOURCES = ["api.cu", "append.cu", "decode.cu", "merge.cu", "prefill.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "append.cu", "decode.cu", "merge.cu", "prefill.cu", "prefill_pair.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]

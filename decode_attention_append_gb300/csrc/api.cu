@@ -180,7 +180,10 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
     a.part_lse = part_lse;
     a.err = ls.err;
     if (a.n_tiles > 0) {
-      if (run(kKernelPrefill, [&] { return launch_prefill(a, s, programmatic); }) != cudaSuccess)
+      const bool quads = plan_prefill_quads(dims);
+      if (run(kKernelPrefill, [&] {
+            return quads ? launch_prefill_pair(a, s, programmatic) : launch_prefill(a, s, programmatic);
+          }) != cudaSuccess)
         return DAA_ERR_CUDA;
       programmatic = !(trace && tracing());
     }

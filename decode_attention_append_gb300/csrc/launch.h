@@ -89,6 +89,9 @@ constexpr int kPrefillTileRows = 128;
 // Tensor-core kernel over the prefill items (pairs of 128-row Q tiles) and
 // over the one-token decode items (a smaller instantiation, two CTAs per SM).
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, bool programmatic);
+// head_dim 128: prefill items of four Q tiles on clusters of two CTAs
+// (tcgen05 cta_group::2); grid (2 * n_tiles, Hkv).
+cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream, bool programmatic);
 cudaError_t launch_tc_decode(const PrefillArgs& a, cudaStream_t stream, bool programmatic);
 
 // Everything one batch_attention call launches, given its plan in `scratch`

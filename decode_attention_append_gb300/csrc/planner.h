@@ -11,9 +11,10 @@
 //    at memory rate while the CUDA cores only run the softmax;
 //  * other decode requests go to the CUDA-core split-KV kernel as page-aligned
 //    key splits;
-//  * prefill requests (qo_len > 1) become pairs of 128-row tiles of packed
-//    (token, query head) rows for the tensor-core kernel, longest key range
-//    first.
+//  * prefill requests (qo_len > 1) become items of 128-row tiles of packed
+//    (token, query head) rows for the tensor-core kernels -- four tiles on a
+//    pair of SMs for head_dim 128, two tiles on one SM otherwise -- longest
+//    key range first.
 // Split decode requests get consecutive partial slots and one softmax_merge
 // item ("Chunked prefill" (k4i.top), #correctness).
 #pragma once
@@ -31,6 +32,10 @@ constexpr int kTcDecodeMinGroup = 4;
 constexpr size_t kPlanAlign = 256;
 
 inline size_t plan_align_up(size_t x) { return (x + kPlanAlign - 1) & ~(kPlanAlign - 1); }
+
+// Prefill items span four Q tiles and run on CTA pairs (head_dim 128), else two
+// Q tiles on one CTA.
+inline bool plan_prefill_quads(const daa_dims& d) { return d.head_dim == 128; }
 
 inline daa_status plan_check_dims(const daa_dims& d) {
   if (d.num_qo_heads <= 0 || d.num_kv_heads <= 0 || d.head_dim <= 0 || d.page_size <= 0 ||
@@ -142,27 +147,39 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
     return a != b ? a > b : (x.q_row != y.q_row ? x.q_row < y.q_row : x.tok_begin < y.tok_begin);
   });
 
-  // prefill: pairs of 128-row tiles (ntok * g <= 128 packed rows each)
+  // prefill: 128-row Q tiles of packed (token, query head) rows (tpt tokens
+  // each).  head_dim 128: items of four tiles for a CTA pair (ntok = the item's
+  // tokens); otherwise pairs of tiles for one CTA (ntok, ntok1 per tile).
   const int tpt = kPrefillTileRows / g;
+  const bool quads = plan_prefill_quads(d);
   for (int r = 0; r < batch; ++r) {
     const int nq = qo[r + 1] - qo[r];
     if (nq < 2) continue;
     const int np = kv[r + 1] - kv[r];
     const int kv_len = (np - 1) * P + last[r];
-    for (int t0 = 0; t0 < nq; t0 += 2 * tpt) {
+    for (int t0 = 0; t0 < nq; t0 += (quads ? 4 : 2) * tpt) {
       PrefillTile t{};
       t.q_row0 = qo[r];
       t.qo_len = nq;
       t.kv_len = kv_len;
       t.page_base = kv[r];
       t.tok0 = t0;
-      t.ntok = std::min(tpt, nq - t0);
-      t.ntok1 = t.ntok == tpt ? std::max(0, std::min(tpt, nq - t0 - tpt)) : 0;
+      int ntiles;
+      if (quads) {
+        t.ntok = std::min(4 * tpt, nq - t0);
+        t.ntok1 = 0;
+        ntiles = (t.ntok + tpt - 1) / tpt;
+      } else {
+        t.ntok = std::min(tpt, nq - t0);
+        t.ntok1 = t.ntok == tpt ? std::max(0, std::min(tpt, nq - t0 - tpt)) : 0;
+        ntiles = t.ntok1 > 0 ? 2 : 1;
+      }
       t.key_lo = 0;
       t.key_hi = kv_len;
       t.part = -1;
-      // keys read, counted twice for a pair (both tiles use each key tile)
-      t.work = std::min(kv_len, kv_len - nq + t0 + t.ntok + t.ntok1) * (t.ntok1 > 0 ? 2 : 1);
+      // keys read by the item's last token, counted once per Q tile
+      const int toks = quads ? t.ntok : t.ntok + t.ntok1;
+      t.work = std::min(kv_len, kv_len - nq + t0 + toks) * ntiles;
       if (!tiles.push_back(t)) return DAA_ERR_WORKSPACE;
     }
   }

@@ -36,13 +36,13 @@
 
 #include "launch.h"
 #include "ptx.cuh"
+#include "softmax_tc.cuh"
 
 namespace daa {
 namespace {
 
 constexpr int kP = 16;
 constexpr int kRows = kPrefillTileRows;  // 128 packed query rows per Q tile
-constexpr float kRescaleThreshold = 8.0f;  // log2 domain
 
 struct __align__(64) PrefillParams {
   CUtensorMap tmap_q;     // q viewed as [nnz_qo][Hq][d], box {64, g, 128/g}
@@ -368,143 +368,20 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
     const int q = warp >> 2;
     const int row = tid & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tmem_o = tmem + C::O_COL + q * D + lane_off;
     const int q_ntok = q == 0 ? tile.ntok : tile.ntok1;
     const int q_tok0 = tile.tok0 + q * tile.ntok;  // first token of this Q tile
     const int tl = row / g;
     const int qpos = tile.kv_len - tile.qo_len + q_tok0 + tl;
     const int row_end = min(a.causal ? min(qpos + 1, tile.kv_len) : tile.kv_len, kend);  // keys < row_end
-    const float sc = a.sm_scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
-
-    for (int j = 0; j < n_kt; ++j) {
-      // S buffer of this tile: the tile's own (pairs) or alternating (single tile)
-      const int b = nq == 2 ? q : (j & 1);
-      const uint32_t ph = nq == 2 ? (j & 1) : ((j >> 1) & 1);
-      const uint32_t tmem_s = tmem + b * KT + lane_off;
-      mbar_wait(&s_full[b], ph, a.err);
-      tc_fence_after();
-      float s[KT];
-#pragma unroll
-      for (int c = 0; c < KT; c += 32) tmem_ld32f(tmem_s + c, s + c);
-      tmem_wait_ld();
-      const int lim = row_end - (kt0 + j) * KT;  // keys [(kt0+j)*128, .. + lim) are valid
-      if (!__all_sync(0xffffffffu, lim >= KT)) {
-#pragma unroll
-        for (int c = 0; c < KT; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
-      }
-      // row max of the raw scores (sm_scale > 0, so it commutes with scaling)
-      // (independent chains over 32 columns each)
-      float mx[KT / 32];
-#pragma unroll
-      for (int k = 0; k < KT / 32; ++k) {
-        mx[k] = s[32 * k];
-#pragma unroll
-        for (int i2 = 1; i2 < 31; i2 += 2) mx[k] = fmax3(mx[k], s[32 * k + i2], s[32 * k + i2 + 1]);
-        mx[k] = fmaxf(mx[k], s[32 * k + 31]);
-      }
-      float mt = mx[0];
-#pragma unroll
-      for (int k = 1; k < KT / 32; ++k) mt = fmaxf(mt, mx[k]);
-      mt *= sc;
-      float m_use = m_run;
-      float alpha = 1.f;
-      if (mt > m_run + kRescaleThreshold) {
-        m_use = mt;
-        alpha = ex2_approx(m_run - mt);  // 0 on the first tile
-      }
-      // P = 2^(s * scale - m) as bf16 pairs over the first KT/2 columns of S
-      // (the A operand of PV), 32 columns at a time so each chunk of s dies early
-      const float2 sc2 = make_float2(sc, sc);
-      const float2 nm2 = make_float2(-m_use, -m_use);
-      float2 sum2 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < KT / 2; c += 32) {
-        uint32_t r[32];
-#pragma unroll
-        for (int i2 = 0; i2 < 32; ++i2) {
-          const float2 t = __ffma2_rn(make_float2(s[2 * (c + i2)], s[2 * (c + i2) + 1]), sc2, nm2);
-          const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-          sum2 = __fadd2_rn(sum2, pp);
-          r[i2] = pack_bf16x2(pp.x, pp.y);
-        }
-        tmem_st32(tmem_s + c, r);
-      }
-      const float sum = sum2.x + sum2.y;
-      l_run = l_run * alpha + sum;
-      m_run = m_use;
-      const bool warp_rescale = __any_sync(0xffffffffu, alpha != 1.f) && j > 0;
-
-      // O (TMEM) is rescaled once PV of the previous tile is done with it
-      if (warp_rescale) {
-        mbar_wait(&o_done[q], (j - 1) & 1, a.err);
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D; c += 64) {  // two 32-column loads in flight per wait
-          float o[64];
-          tmem_ld32f(tmem_o + c, o);
-          tmem_ld32f(tmem_o + c + 32, o + 32);
-          tmem_wait_ld();
-          uint32_t r[32];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-#pragma unroll
-            for (int i2 = 0; i2 < 32; ++i2) r[i2] = __float_as_uint(o[32 * h + i2] * alpha);
-            tmem_st32(tmem_o + c + 32 * h, r);
-          }
-        }
-      }
-      // o_done must never run two phases ahead of this thread's parity waits:
-      // with S double-buffered, S(j) done only implies PV(j-2) done, so consume
-      // the phase of PV(j-1) before PV(j) can be issued (normally no wait).
-      if (j > 0 && !warp_rescale) mbar_wait(&o_done[q], (j - 1) & 1, a.err);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[b]);
-    }
-
-    // ---- epilogue: O / l -> bf16 rows of out; lse
-    mbar_wait(&o_done[q], (n_kt - 1) & 1, a.err);
-    tc_fence_after();
-    const float inv = 1.f / l_run;
-    const int hg = row - tl * g;
-    const int q_row = tile.q_row0 + q_tok0 + tl;
-    const int hq = kvh * g + hg;
-    const bool write = row < q_ntok * g;
-    const bool partial = tile.part >= 0;  // one-token split item: fp32 partial for softmax_merge
-    uint16_t* dst = a.out + ((int64_t)q_row * a.Hq + hq) * D;
-    float* pdst = a.part_o + ((int64_t)tile.part * a.Hq + hq) * D;
-#pragma unroll
-    for (int c = 0; c < D; c += 64) {  // two 32-column loads in flight per wait
-      float o[64];
-      tmem_ld32f(tmem_o + c, o);
-      tmem_ld32f(tmem_o + c + 32, o + 32);
-      tmem_wait_ld();
-      if (write && partial) {
-#pragma unroll
-        for (int i2 = 0; i2 < 64; i2 += 4)
-          *reinterpret_cast<float4*>(pdst + c + i2) =
-              make_float4(o[i2] * inv, o[i2 + 1] * inv, o[i2 + 2] * inv, o[i2 + 3] * inv);
-      } else if (write) {
-#pragma unroll
-        for (int i2 = 0; i2 < 64; i2 += 8) {
-          uint4 v;
-          v.x = pack_bf16x2(o[i2 + 0] * inv, o[i2 + 1] * inv);
-          v.y = pack_bf16x2(o[i2 + 2] * inv, o[i2 + 3] * inv);
-          v.z = pack_bf16x2(o[i2 + 4] * inv, o[i2 + 5] * inv);
-          v.w = pack_bf16x2(o[i2 + 6] * inv, o[i2 + 7] * inv);
-          *reinterpret_cast<uint4*>(dst + c + i2) = v;
-        }
-      }
-    }
-    if (write) {
-      const float lse2 = m_run + __log2f(l_run);
-      if (partial)
-        a.part_lse[(int64_t)tile.part * a.Hq + hq] = lse2;
-      else if (a.lse_out)
-        a.lse_out[(int64_t)q_row * a.Hq + hq] = lse2 * 0.69314718055994531f;
-    }
+    SoftmaxRowOut ro;
+    ro.q_row = tile.q_row0 + q_tok0 + tl;
+    ro.hq = kvh * g + (row - tl * g);
+    ro.write = row < q_ntok * g;
+    ro.part = tile.part;
+    tc_softmax_rows<D, KT>(a, tmem + lane_off, tmem + C::O_COL + q * D + lane_off, s_full, &o_done[q],
+                           q, nq == 1, n_kt, kt0, row_end, ro, [&](int b) {
+                             if (lane == 0) mbar_arrive(&p_full[b]);
+                           });
   }
 
   tc_fence_before();

@@ -1,0 +1,473 @@
+// Prefill-chunk attention (qo_len > 1) on pairs of SMs: tcgen05 with
+// cta_group::2, head_dim 128.
+//
+// "Chunked prefill" (k4i.top), #correctness / #flops: the same computation as
+// the single-CTA tensor-core kernel (one online softmax over the cached prefix
+// and the causal part of the chunk).  What changes is how K/V reach the tensor
+// cores.  With 16-token pages a K or V tile is assembled from 2 KB TMA boxes
+// (one per page and 64-column half), and one SM takes in such boxes at about
+// 20 bytes per clock -- below the ~30 bytes per clock two 128-row Q tiles need
+// at the tensor-core rate.  A cluster of two CTAs issues each MMA once for
+// M = 256 rows (128 in each CTA) and splits the B operand between them, so each
+// SM loads only half of every K tile (64 keys) and half of every V tile (64 of
+// the 128 columns): half the boxes and bytes per SM for the same work.
+//
+// Cluster = (CTA 0, CTA 1), one work item = up to four 128-row Q tiles of one
+// request and kv head; CTA r holds tiles r and 2 + r (local tiles 0 and 1), so
+// the M = 256 MMA of local tile q covers the adjacent tiles 2q and 2q + 1.
+// Per CTA the warp roles are those of the single-CTA kernel:
+//   warps 0-3 / 4-7  softmax of local Q tile 0 / 1 (thread = row = TMEM lane)
+//   warp 8           TMA producer of this CTA's halves: Q tiles, then K_0, V_0,
+//                    K_1, V_1, ... into a ring of RS half-tile stages (16 KB)
+//   warp 9           CTA 0: MMA issuer for the pair; CTA 1: relays "my half of
+//                    stage s has landed" to CTA 0 (remote mbarrier arrive)
+// Tensor memory per CTA: S_q / P_q at q*128, O_q at 256 + q*128 (512 columns).
+// Completion of the pair's MMAs is committed to the barriers of both CTAs
+// (multicast); both CTAs' softmax warps hand P to CTA 0's issuer by arriving on
+// its p_full barrier.  Every tcgen05 instruction of this kernel uses
+// cta_group::2, as the instruction set requires within one kernel.
+#include <cuda.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+#include "softmax_tc.cuh"
+
+namespace daa {
+namespace {
+
+constexpr int kP = 16;
+constexpr int kRows = kPrefillTileRows;
+
+struct __align__(64) PairParams {
+  CUtensorMap tmap_q;   // q viewed as [nnz_qo][Hq][d], box {64, g, 128/g}
+  CUtensorMap tmap_kv;  // pool viewed as [num_pages*2*Hkv][P][d], box {64, P, 1}
+  PrefillArgs a;
+  const PrefillTile* tiles;
+};
+
+// ------------------------------------------------- cluster / cta_group::2 ops
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Arrive once on the mbarrier at the same shared-memory offset in CTA `rank`
+// of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+// The same without release semantics.  Used to hand P (in this CTA's tensor
+// memory) to CTA 0's issuer: the stores are already complete
+// (tcgen05.wait::st, then tcgen05.fence::before_thread_sync), and the release
+// form measured ~800 clocks per arrive on this critical path.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint64_t* bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(rank));
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(smem_slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// D (TMEM of both CTAs) (+)= A (M = 256: 128 rows in each CTA's smem) * B
+// (N split in half between the two CTAs' smem).
+__device__ __forceinline__ void mma_pair_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The same with A read from each CTA's own TMEM (its 128 rows).
+__device__ __forceinline__ void mma_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the barrier at this offset in both CTAs once the pair's previously
+// issued MMAs complete.
+__device__ __forceinline__ void commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+struct PairCfg {
+  static constexpr int D = 128, KT = 128, PPT = KT / kP;
+  static constexpr int THREADS = 320;
+  static constexpr int PRODUCER = 8, MMA = 9;
+  static constexpr int Q_BYTES = kRows * D * 2;           // one 128-row Q tile (32 KB)
+  static constexpr int H_BYTES = KT * D;                  // half of a K or V tile (16 KB)
+  static constexpr int BUDGET = 231424;
+  static constexpr int FIXED = 2 * Q_BYTES + 512 + 1024;
+  static constexpr int RS_FIT = (BUDGET - FIXED) / H_BYTES;
+  static constexpr int RS = RS_FIT < 12 ? RS_FIT : 12;    // ring stages (half tiles)
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_RING = 2 * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_RING + RS * H_BYTES;
+  // q_full, q_peer, ring_full[RS], ring_empty[RS], peer_full[RS], s_full[2],
+  // p_full[2], o_done[2], v_clean
+  static constexpr int NBAR = 2 + 3 * RS + 7;
+  static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_TMEM + 16;
+  static constexpr int ALLOC = BYTES + 1024;
+  static constexpr int O_COL = 2 * KT;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(RS >= 6, "ring too shallow");
+  static_assert(ALLOC <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ uint64_t desc_kmajor_p(uint32_t addr) { return smem_desc_sw128(addr, 16, 1024); }
+__device__ __forceinline__ uint64_t desc_mnmajor_p(uint32_t addr) {
+  // one 64-column N block per CTA: LBO is not used
+  return smem_desc_sw128(addr, PairCfg::KT * 128, 1024);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::THREADS, 1)
+prefill_pair_kernel(const __grid_constant__ PairParams prm) {
+  using C = PairCfg;
+  constexpr int D = C::D, KT = C::KT, PPT = C::PPT, RS = C::RS;
+  const PrefillArgs& a = prm.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* q_peer = bars + 1;
+  uint64_t* ring_full = bars + 2;
+  uint64_t* ring_empty = ring_full + RS;
+  uint64_t* peer_full = ring_empty + RS;
+  uint64_t* s_full = peer_full + RS;  // [2]
+  uint64_t* p_full = s_full + 2;      // [2]
+  uint64_t* o_done = p_full + 2;      // [2]
+  uint64_t* v_clean = o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
+
+  const uint32_t rank = cluster_ctarank();
+  const PrefillTile tile = prm.tiles[blockIdx.x >> 1];
+  const int kvh = blockIdx.y;
+  const int g = a.group;
+  const int tpt = kRows / g;  // tokens per Q tile
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_tiles = (tile.ntok + tpt - 1) / tpt;  // Q tiles of the item (1..4)
+  const int nq = (n_tiles + 1) >> 1;                 // M = 256 tile pairs (1 or 2)
+
+  // key tiles 0 .. n_kt - 1 cover keys [0, kend); causal rows mask beyond their
+  // own position
+  const int pos_first = tile.kv_len - tile.qo_len + tile.tok0;
+  const int kv_end = a.causal ? min(tile.kv_len, pos_first + tile.ntok) : tile.kv_len;
+  const int kend = min(kv_end, tile.key_hi);
+  const int kt0 = tile.key_lo / KT;
+  const int n_kt = (kend + KT - 1) / KT - kt0;
+  const int npages_req = (tile.kv_len + kP - 1) / kP;
+  const bool last_partial = tile.kv_len - (kt0 + n_kt - 1) * KT < KT;
+
+  if (tid == 0) {
+    prefetch_tmap(&prm.tmap_q);
+    prefetch_tmap(&prm.tmap_kv);
+    mbar_init(q_full, 1);
+    mbar_init(q_peer, 1);
+    for (int i = 0; i < RS; ++i) {
+      mbar_init(&ring_full[i], 1);
+      mbar_init(&ring_empty[i], 1);
+      mbar_init(&peer_full[i], 1);
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&s_full[q], 1);
+      mbar_init(&p_full[q], 8);  // the tile pair's 4 + 4 softmax warps
+      mbar_init(&o_done[q], 1);
+    }
+    mbar_init(v_clean, 2);
+    fence_mbar_init();
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == C::MMA) {
+    tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote arrive or commit
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (tid == 0) grid_dep_launch();
+
+  if (warp == C::PRODUCER) {
+    // ------------------------------------------------------------ producer
+    // This CTA's half of K tile j: keys [64 r, 64 r + 64) = pages 4r .. 4r+3,
+    // both 64-column blocks, as two [64 rows][128 B] panels.  Its half of V tile
+    // j: all 8 pages, column block r, as one [128 rows][128 B] panel.
+    auto load_ids = [&](int i) -> int64_t {
+      if (i >= 2 * n_kt) return -1;
+      const int pg0 = (kt0 + (i >> 1)) * PPT;
+      const int np = min(PPT, npages_req - pg0);
+      return lane < np ? (int64_t)__ldg(a.page_indices + tile.page_base + pg0 + lane) : -1;
+    };
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, (uint32_t)(nq * tpt * g * D * 2));
+      for (int q = 0; q < nq; ++q) {
+        const int t = 2 * q + (int)rank;  // tile of the item held in local slot q
+        for (int b = 0; b < 2; ++b)
+          tma_load_3d(smem + C::OFF_Q + q * C::Q_BYTES + b * (kRows * 128), &prm.tmap_q, b * 64,
+                      kvh * g, tile.q_row0 + tile.tok0 + t * tpt, q_full);
+      }
+    }
+    int64_t pid = load_ids(0);
+    if (tile.key_hi >= tile.kv_len) grid_dep_wait();  // reads rows appended in this step
+    for (int i = 0; i < 2 * n_kt; ++i) {
+      const int64_t pid_next = load_ids(i + 1);
+      const int st = i % RS;
+      const bool is_v = i & 1;
+      const int pg0 = (kt0 + (i >> 1)) * PPT;
+      const int np = min(PPT, npages_req - pg0);
+      const int kp = max(0, min(4, np - 4 * (int)rank));  // pages of this CTA's K half
+      uint8_t* buf = smem + C::OFF_RING + st * C::H_BYTES;
+      if (lane == 0) {
+        if (i >= RS) mbar_wait(&ring_empty[st], ((i / RS) - 1) & 1, a.err);
+        mbar_arrive_expect_tx(&ring_full[st], (uint32_t)((is_v ? np : 2 * kp) * kP * 128));
+      }
+      __syncwarp();
+      const bool mine = is_v ? lane < np : (lane >= 4 * (int)rank && lane < 4 * (int)rank + kp);
+      if (mine) {
+        int64_t page = pid;
+        if (page < 0 || page >= a.num_pages) {
+          set_device_error(a.err, kDevErrPageRange);
+          page = 0;  // fetch a valid page instead; the output is undefined anyway
+        }
+        const int32_t slice = (int32_t)((page * 2 + (is_v ? 1 : 0)) * a.Hkv + kvh);
+        if (is_v) {
+          tma_load_3d(buf + lane * (kP * 128), &prm.tmap_kv, (int)rank * 64, 0, slice, &ring_full[st]);
+        } else {
+          const int p = lane - 4 * (int)rank;
+#pragma unroll
+          for (int b = 0; b < 2; ++b)
+            tma_load_3d(buf + b * (64 * 128) + p * (kP * 128), &prm.tmap_kv, b * 64, 0, slice,
+                        &ring_full[st]);
+        }
+      }
+      pid = pid_next;
+    }
+    __syncwarp();
+    if (last_partial) {
+      // this CTA's half of the last V tile: rows past the request's last key
+      // must hold finite values
+      const int i = 2 * n_kt - 1, st = i % RS;
+      const int tile_keys = tile.kv_len - (kt0 + n_kt - 1) * KT;
+      uint8_t* buf = smem + C::OFF_RING + st * C::H_BYTES;
+      mbar_wait(&ring_full[st], (i / RS) & 1, a.err);
+      for (int idx = lane; idx < (KT - tile_keys) * 8; idx += 32) {
+        const int r = tile_keys + (idx >> 3), ch = idx & 7;
+        *reinterpret_cast<uint4*>(buf + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(v_clean);
+        else
+          mbar_arrive_cluster(v_clean, 0);
+      }
+    }
+  } else if (warp == C::MMA && rank == 1) {
+    // ------------------------------------------------------ relay (CTA 1)
+    // CTA 0 issues MMAs that read this CTA's shared memory: tell it when each
+    // of this CTA's Q tiles and ring stages has landed.
+    mbar_wait(q_full, 0, a.err);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(q_peer, 0);
+    for (int i = 0; i < 2 * n_kt; ++i) {
+      const int st = i % RS;
+      mbar_wait(&ring_full[st], (i / RS) & 1, a.err);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(&peer_full[st], 0);
+    }
+  } else if (warp == C::MMA) {
+    // ------------------------------------------------- MMA issuer (CTA 0)
+    // Converged warp, one elected lane issues (see elect_one).
+    constexpr uint32_t idesc_s = idesc_bf16_f32(2 * kRows, KT, 0, 0);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(2 * kRows, D, 0, 1);
+    const uint32_t sQ = smem_u32(smem + C::OFF_Q);
+    const uint32_t sR = smem_u32(smem + C::OFF_RING);
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      mbar_wait(bar, parity, a.err);
+      __syncwarp();
+    };
+    auto commit = [&](uint64_t* bar) {
+      if (elect_one()) commit_pair(bar);
+      __syncwarp();
+    };
+    auto wait_stage = [&](int i) {  // both CTAs' halves of ring item i
+      const int st = i % RS;
+      wait(&ring_full[st], (i / RS) & 1);
+      wait(&peer_full[st], (i / RS) & 1);
+      tc_fence_after();
+    };
+    auto issue_s = [&](int q, int st) {  // S_q = Q_q K^T (N = 128 keys, 64 per CTA)
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint64_t da = desc_kmajor_p(sQ + q * C::Q_BYTES + (k >> 2) * (kRows * 128) + (k & 3) * 32);
+        const uint64_t db = desc_kmajor_p(sR + st * C::H_BYTES + (k >> 2) * (64 * 128) + (k & 3) * 32);
+        if (elect_one()) mma_pair_ss(tmem + q * KT, da, db, idesc_s, k > 0 ? 1u : 0u);
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int q, int st, bool accumulate) {  // O_q += P_q V (N = 128, 64 per CTA)
+#pragma unroll
+      for (int k = 0; k < KT / 16; ++k) {
+        const uint64_t db = desc_mnmajor_p(sR + st * C::H_BYTES + k * (16 * 128));
+        if (elect_one())
+          mma_pair_ts(tmem + C::O_COL + q * D, tmem + q * KT + k * 8, db, idesc_o,
+                      (accumulate || k > 0) ? 1u : 0u);
+      }
+      __syncwarp();
+    };
+    wait(q_full, 0);
+    wait(q_peer, 0);
+    wait_stage(0);
+    for (int q = 0; q < nq; ++q) {
+      issue_s(q, 0);
+      commit(&s_full[q]);
+    }
+    commit(&ring_empty[0]);
+    for (int j = 0; j < n_kt; ++j) {
+      const int iv = 2 * j + 1, sv = iv % RS;
+      const int ik = 2 * j + 2, sk = ik % RS;
+      wait_stage(iv);
+      if (j == n_kt - 1 && last_partial) wait(v_clean, 0);
+      bool k_ready = false;
+      for (int q = 0; q < nq; ++q) {
+        wait(&p_full[q], j & 1);
+        tc_fence_after();
+        issue_pv(q, sv, j > 0);
+        commit(&o_done[q]);
+        if (j + 1 < n_kt) {
+          if (!k_ready) {
+            wait_stage(ik);
+            k_ready = true;
+          }
+          issue_s(q, sk);
+          commit(&s_full[q]);
+        }
+      }
+      commit(&ring_empty[sv]);
+      if (j + 1 < n_kt) commit(&ring_empty[sk]);
+    }
+  } else if (warp / 4 < nq) {
+    // ------------------------------------------------------------- softmax
+    // Every warp of a live tile pair runs (rows past the item's tokens compute
+    // values that are not written): CTA 0's issuer counts 8 arrivals per P.
+    const int q = warp >> 2;
+    const int row = tid & 127;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int t = 2 * q + (int)rank;
+    const int q_tok0 = tile.tok0 + t * tpt;  // first token of this Q tile
+    const int q_ntok = max(0, min(tpt, tile.ntok - t * tpt));
+    const int tl = row / g;
+    const int qpos = tile.kv_len - tile.qo_len + q_tok0 + tl;
+    const int row_end = min(a.causal ? min(qpos + 1, tile.kv_len) : tile.kv_len, kend);
+    SoftmaxRowOut ro;
+    ro.q_row = tile.q_row0 + q_tok0 + tl;
+    ro.hq = kvh * g + (row - tl * g);
+    ro.write = row < q_ntok * g;
+    ro.part = -1;
+    tc_softmax_rows<D, KT>(a, tmem + lane_off, tmem + C::O_COL + q * D + lane_off, s_full, &o_done[q],
+                           q, false, n_kt, kt0, row_end, ro, [&](int b) {
+                             if (lane == 0) {
+                               if (rank == 0)
+                                 mbar_arrive(&p_full[b]);
+                               else
+                                 mbar_arrive_cluster_relaxed(&p_full[b], 0);
+                             }
+                           });
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // neither CTA leaves while the pair's MMAs or arrives may reach it
+  if (warp == C::MMA) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::TMEM_COLS);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream, bool programmatic) {
+  if (a.n_tiles <= 0) return cudaSuccess;
+  if (a.head_dim != 128) return cudaErrorInvalidValue;
+  constexpr int D = 128;
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  PairParams prm;
+  prm.a = a;
+  prm.tiles = a.tiles;
+  const int g = a.group;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.Hq, (cuuint64_t)a.nnz_qo};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.Hq * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)(kRows / g)};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&prm.tmap_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.q, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)kP, (cuuint64_t)a.num_pages * 2 * a.Hkv};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)kP * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kP, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&prm.tmap_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.pool, dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       PairCfg::ALLOC);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(prefill_pair_kernel, dim3(2 * a.n_tiles, a.Hkv), dim3(PairCfg::THREADS),
+                       PairCfg::ALLOC, stream, programmatic, prm);
+}
+
+}  // namespace daa

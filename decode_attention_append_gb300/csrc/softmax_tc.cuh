@@ -1,0 +1,167 @@
+// Softmax warps of the tensor-core attention kernels: one thread per packed
+// query row (its TMEM lane), a warpgroup per 128-row Q tile.
+//
+// "Chunked prefill" (k4i.top), #correctness: token i of a chunk attends to the
+// keys j <= its absolute position, cached prefix and chunk alike, through one
+// online softmax.  Per key tile the thread loads its row of S from TMEM, masks
+// keys at or past row_end, raises a lazily kept running max (only when it
+// grows by more than 2^8, so O is rescaled in TMEM rarely), writes
+// P = 2^(s * scale - m) as bf16 over the first KT/2 columns of S (the A
+// operand of PV), and hands P to the MMA issuer through release_p.  The
+// epilogue divides O by the running sum and writes bf16 rows (or, for a key
+// split, fp32 partial rows in the log2 domain for softmax_merge).
+#pragma once
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace daa {
+
+constexpr float kRescaleThreshold = 8.0f;  // log2 domain
+
+// Per-row output target of the epilogue.
+struct SoftmaxRowOut {
+  int q_row;     // token row of q / out / lse_out
+  int hq;        // query head
+  bool write;    // the row holds a real (token, head)
+  int part;      // partial slot (key split) or -1
+};
+
+// tmem_s0: TMEM address (lane field = this warp's 32 lanes) of S buffer 0; S
+// buffer b sits at tmem_s0 + b * KT.  tmem_o: this warp's lanes of O.
+// dbuf: S alternates between buffers 0 and 1 per key tile (single Q tile);
+// otherwise buffer `sbuf` is used for every tile.
+template <int D, int KT, class ReleaseP>
+__device__ __forceinline__ void tc_softmax_rows(const PrefillArgs& a, uint32_t tmem_s0,
+                                                uint32_t tmem_o, uint64_t* s_full,
+                                                uint64_t* o_done_q, int sbuf, bool dbuf,
+                                                int n_kt, int kt0, int row_end,
+                                                const SoftmaxRowOut& ro, ReleaseP&& release_p) {
+  const float sc = a.sm_scale_log2;
+  float m_run = -INFINITY, l_run = 0.f;
+
+  for (int j = 0; j < n_kt; ++j) {
+    const int b = dbuf ? (j & 1) : sbuf;
+    const uint32_t ph = dbuf ? ((j >> 1) & 1) : (j & 1);
+    const uint32_t tmem_s = tmem_s0 + b * KT;
+    mbar_wait(&s_full[b], ph, a.err);
+    tc_fence_after();
+    float s[KT];
+#pragma unroll
+    for (int c = 0; c < KT; c += 32) tmem_ld32f(tmem_s + c, s + c);
+    tmem_wait_ld();
+    const int lim = row_end - (kt0 + j) * KT;  // keys [(kt0+j)*KT, .. + lim) are valid
+    if (!__all_sync(0xffffffffu, lim >= KT)) {
+#pragma unroll
+      for (int c = 0; c < KT; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
+    }
+    // row max of the raw scores (sm_scale > 0, so it commutes with scaling),
+    // as independent chains over 32 columns each
+    float mx[KT / 32];
+#pragma unroll
+    for (int k = 0; k < KT / 32; ++k) {
+      mx[k] = s[32 * k];
+#pragma unroll
+      for (int i2 = 1; i2 < 31; i2 += 2) mx[k] = fmax3(mx[k], s[32 * k + i2], s[32 * k + i2 + 1]);
+      mx[k] = fmaxf(mx[k], s[32 * k + 31]);
+    }
+    float mt = mx[0];
+#pragma unroll
+    for (int k = 1; k < KT / 32; ++k) mt = fmaxf(mt, mx[k]);
+    mt *= sc;
+    float m_use = m_run;
+    float alpha = 1.f;
+    if (mt > m_run + kRescaleThreshold) {
+      m_use = mt;
+      alpha = ex2_approx(m_run - mt);  // 0 on the first tile
+    }
+    // P = 2^(s * scale - m) as bf16 pairs over the first KT/2 columns of S
+    // (the A operand of PV), 32 columns at a time so each chunk of s dies early
+    const float2 sc2 = make_float2(sc, sc);
+    const float2 nm2 = make_float2(-m_use, -m_use);
+    float2 sum2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < KT / 2; c += 32) {
+      uint32_t r[32];
+#pragma unroll
+      for (int i2 = 0; i2 < 32; ++i2) {
+        const float2 t = __ffma2_rn(make_float2(s[2 * (c + i2)], s[2 * (c + i2) + 1]), sc2, nm2);
+        const float2 pp = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+        sum2 = __fadd2_rn(sum2, pp);
+        r[i2] = pack_bf16x2(pp.x, pp.y);
+      }
+      tmem_st32(tmem_s + c, r);
+    }
+    const float sum = sum2.x + sum2.y;
+    l_run = l_run * alpha + sum;
+    m_run = m_use;
+    const bool warp_rescale = __any_sync(0xffffffffu, alpha != 1.f) && j > 0;
+
+    // O (TMEM) is rescaled once PV of the previous tile is done with it
+    if (warp_rescale) {
+      mbar_wait(o_done_q, (j - 1) & 1, a.err);
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < D; c += 64) {  // two 32-column loads in flight per wait
+        float o[64];
+        tmem_ld32f(tmem_o + c, o);
+        tmem_ld32f(tmem_o + c + 32, o + 32);
+        tmem_wait_ld();
+        uint32_t r[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int i2 = 0; i2 < 32; ++i2) r[i2] = __float_as_uint(o[32 * h + i2] * alpha);
+          tmem_st32(tmem_o + c + 32 * h, r);
+        }
+      }
+    }
+    // o_done must never run two phases ahead of this thread's parity waits:
+    // with S double-buffered, S(j) done only implies PV(j-2) done, so consume
+    // the phase of PV(j-1) before PV(j) can be issued (normally no wait).
+    if (j > 0 && !warp_rescale) mbar_wait(o_done_q, (j - 1) & 1, a.err);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    release_p(b);
+  }
+
+  // ---- epilogue: O / l -> bf16 rows of out; lse
+  mbar_wait(o_done_q, (n_kt - 1) & 1, a.err);
+  tc_fence_after();
+  const float inv = 1.f / l_run;
+  const bool partial = ro.part >= 0;  // key split: fp32 partial for softmax_merge
+  uint16_t* dst = a.out + ((int64_t)ro.q_row * a.Hq + ro.hq) * D;
+  float* pdst = a.part_o + ((int64_t)ro.part * a.Hq + ro.hq) * D;
+#pragma unroll
+  for (int c = 0; c < D; c += 64) {  // two 32-column loads in flight per wait
+    float o[64];
+    tmem_ld32f(tmem_o + c, o);
+    tmem_ld32f(tmem_o + c + 32, o + 32);
+    tmem_wait_ld();
+    if (ro.write && partial) {
+#pragma unroll
+      for (int i2 = 0; i2 < 64; i2 += 4)
+        *reinterpret_cast<float4*>(pdst + c + i2) =
+            make_float4(o[i2] * inv, o[i2 + 1] * inv, o[i2 + 2] * inv, o[i2 + 3] * inv);
+    } else if (ro.write) {
+#pragma unroll
+      for (int i2 = 0; i2 < 64; i2 += 8) {
+        uint4 v;
+        v.x = pack_bf16x2(o[i2 + 0] * inv, o[i2 + 1] * inv);
+        v.y = pack_bf16x2(o[i2 + 2] * inv, o[i2 + 3] * inv);
+        v.z = pack_bf16x2(o[i2 + 4] * inv, o[i2 + 5] * inv);
+        v.w = pack_bf16x2(o[i2 + 6] * inv, o[i2 + 7] * inv);
+        *reinterpret_cast<uint4*>(dst + c + i2) = v;
+      }
+    }
+  }
+  if (ro.write) {
+    const float lse2 = m_run + __log2f(l_run);
+    if (partial)
+      a.part_lse[(int64_t)ro.part * a.Hq + ro.hq] = lse2;
+    else if (a.lse_out)
+      a.lse_out[(int64_t)ro.q_row * a.Hq + ro.hq] = lse2 * 0.69314718055994531f;
+  }
+}
+
+}  // namespace daa
