@@ -220,9 +220,12 @@ prefill_pair_kernel(const __grid_constant__ PairParams prm) {
     // This CTA's half of K tile j: keys [64 r, 64 r + 64) = pages 4r .. 4r+3,
     // both 64-column blocks, as two [64 rows][128 B] panels.  Its half of V tile
     // j: all 8 pages, column block r, as one [128 rows][128 B] panel.
-    auto load_ids = [&](int i) -> int64_t {
-      if (i >= 2 * n_kt) return -1;
-      const int pg0 = (kt0 + (i >> 1)) * PPT;
+    // Page ids of key tile j: lane l (< 8) holds the id of the tile's l-th
+    // page (K_j and V_j share them).  Loaded coalesced, four tiles ahead, in a
+    // register pipeline, so the id latency never stalls the issue loop.
+    auto load_ids = [&](int j) -> int64_t {
+      if (j >= n_kt) return -1;
+      const int pg0 = (kt0 + j) * PPT;
       const int np = min(PPT, npages_req - pg0);
       return lane < np ? (int64_t)__ldg(a.page_indices + tile.page_base + pg0 + lane) : -1;
     };
@@ -235,10 +238,9 @@ prefill_pair_kernel(const __grid_constant__ PairParams prm) {
                       kvh * g, tile.q_row0 + tile.tok0 + t * tpt, q_full);
       }
     }
-    int64_t pid = load_ids(0);
+    int64_t id0 = load_ids(0), id1 = load_ids(1), id2 = load_ids(2), id3 = load_ids(3);
     if (tile.key_hi >= tile.kv_len) grid_dep_wait();  // reads rows appended in this step
     for (int i = 0; i < 2 * n_kt; ++i) {
-      const int64_t pid_next = load_ids(i + 1);
       const int st = i % RS;
       const bool is_v = i & 1;
       const int pg0 = (kt0 + (i >> 1)) * PPT;
@@ -252,7 +254,7 @@ prefill_pair_kernel(const __grid_constant__ PairParams prm) {
       __syncwarp();
       const bool mine = is_v ? lane < np : (lane >= 4 * (int)rank && lane < 4 * (int)rank + kp);
       if (mine) {
-        int64_t page = pid;
+        int64_t page = id0;
         if (page < 0 || page >= a.num_pages) {
           set_device_error(a.err, kDevErrPageRange);
           page = 0;  // fetch a valid page instead; the output is undefined anyway
@@ -268,7 +270,12 @@ prefill_pair_kernel(const __grid_constant__ PairParams prm) {
                         &ring_full[st]);
         }
       }
-      pid = pid_next;
+      if (is_v) {  // tile done: shift the id pipeline
+        id0 = id1;
+        id1 = id2;
+        id2 = id3;
+        id3 = load_ids((i >> 1) + 4);
+      }
     }
     __syncwarp();
     if (last_partial) {
