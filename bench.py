@@ -75,10 +75,11 @@ def step_accounting(wl, k=0):
 
 
 def kernel_source_hash(name):
-    src = os.path.join(ROOT, "decode_attention_append_gb300", "csrc", name)
+    """Hash of a kernel's source file and the device headers it shares."""
+    csrc = os.path.join(ROOT, "decode_attention_append_gb300", "csrc")
     h = hashlib.sha256()
-    for f in (src, os.path.join(ROOT, "decode_attention_append_gb300", "csrc", "ptx.cuh")):
-        with open(f, "rb") as fh:
+    for f in (name, "ptx.cuh", "softmax_tc.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -515,13 +516,16 @@ def main():
             fl, by = acc["tc_flops"] / n_launch, acc["tc_bytes"] / n_launch
             t_tensor, t_hbm = fl / (bf16 * 1e12), by / (hbm * 1e9)
             if t_tensor >= t_hbm:
-                roof = {"bound": "tensor", "achieved": fl / t / 1e12, "peak": bf16, "unit": "TFLOP/s",
-                        "peak_source": f"{peak_src} bf16 dense (burst)"}
+                # the kernel runs back to back for seconds (clock window + timed
+                # steps) under the power cap: the sustained GEMM rate is its peak
+                roof = {"bound": "tensor", "achieved": fl / t / 1e12, "peak": bf16_sus, "unit": "TFLOP/s",
+                        "peak_source": f"{peak_src} bf16 dense, sustained (burst {bf16:.1f})",
+                        "frac_of_burst": fl / t / 1e12 / bf16}
             else:
                 roof = {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm, "unit": "GB/s",
                         "peak_source": f"{peak_src} HBM copy"}
             roof["ideal_fraction"] = (t_tensor + t_hbm) / t
-            kfile = "prefill.cu"
+            kfile = "prefill_pair.cu" if wl.head_dim == 128 else "prefill.cu"
         else:
             kb = {"decode_splitkv": acc["cuda_decode_bytes"], "decode_tc": acc["tc_decode_bytes"],
                   "kv_append": acc["append_bytes"]}.get(dom, 0)
