@@ -32,9 +32,10 @@ struct MergeItem {
 // ntok1 > 0) the next ntok1 tokens; each token brings all g query heads of a
 // kv head, packed token-major into ntok * g <= 128 rows per tile.  One CTA per
 // (item, kv head); both tiles share every K/V tile the CTA loads.  Prefill
-// pairs cover all keys and write the output; a decode request (qo_len == 1,
-// ntok == 1) may be split over 128-key-aligned key ranges, each writing a
-// partial (o, lse) to slot `part` for softmax_merge.
+// pairs cover all keys and write the output; a decode or verify request (all
+// its qo_len tokens in tile 0) may be split over 128-key-aligned key ranges,
+// each writing partial (o, lse) rows to slots part + t * part_stride for
+// softmax_merge.
 struct PrefillTile {
   int32_t q_row0;     // row of the request's first new token
   int32_t qo_len;
@@ -47,7 +48,7 @@ struct PrefillTile {
   int32_t key_hi;     // one past the last key
   int32_t part;       // partial slot, or -1: write out / lse_out directly
   int32_t work;       // planner's sort key (keys read)
-  int32_t pad;
+  int32_t part_stride;  // key-split multi-token item: token t's partial slot is part + t * part_stride
 };
 
 static_assert(sizeof(DecodeUnit) == 32, "DecodeUnit layout");

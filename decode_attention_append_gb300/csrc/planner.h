@@ -6,8 +6,9 @@
 // performance": attention parallelises over requests and over kv_len.  Work is
 // split three ways:
 //  * decode requests (qo_len == 1) whose kv head serves g >= kTcDecodeMinGroup
-//    query heads go to the tensor-core kernel as key-split work items (the g
-//    query heads are the rows of one M = 128 tile); the K/V bytes then stream
+//    query heads, and small multi-token requests (verify batches, qo_len up to
+//    plan_verify_max), go to the tensor-core kernel as key-split work items
+//    (their qo_len x g rows fill one M = 128 tile); the K/V bytes then stream
 //    at memory rate while the CUDA cores only run the softmax;
 //  * other decode requests go to the CUDA-core split-KV kernel as page-aligned
 //    key splits;
@@ -29,6 +30,13 @@ namespace daa {
 
 constexpr int kPlanPageSize = 16;
 constexpr int kTcDecodeMinGroup = 4;
+// Requests with 2 <= qo_len <= this many tokens (and qo_len * g <= 128) -- e.g.
+// the draft tokens of a speculative-decoding verify step -- are memory bound
+// like decode: they run as key-split items of the tensor-core decode kernel
+// (all their rows in one 128-row tile, K/V read once per split).
+constexpr int kVerifyMaxTokens = 16;
+
+inline int plan_verify_max(int g) { return std::min(kVerifyMaxTokens, kPrefillTileRows / g); }
 constexpr size_t kPlanAlign = 256;
 
 inline size_t plan_align_up(size_t x) { return (x + kPlanAlign - 1) & ~(kPlanAlign - 1); }
@@ -75,6 +83,7 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
   const int P = d.page_size;
   const int g = d.num_qo_heads / d.num_kv_heads;
   const bool tc_decode = g >= kTcDecodeMinGroup;
+  const int verify_max = plan_verify_max(g);
 
   int64_t dec_pages = 0;
   for (int r = 0; r < batch; ++r) {
@@ -84,49 +93,57 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
     if (np > 0 && (last[r] < 1 || last[r] > P)) return DAA_ERR_SHAPE;
     const int64_t kv_len = np > 0 ? (np - 1) * P + last[r] : 0;
     if (nq > kv_len || kv_len > INT32_MAX / 2) return DAA_ERR_SHAPE;
-    if (nq == 1) dec_pages += np;
+    if (nq >= 1 && nq <= verify_max) dec_pages += np;
   }
   const int64_t page_heads = dec_pages * d.num_kv_heads;
 
   // split sizes (pages).  CUDA-core splits: enough CTAs that the longest split
   // is a small fraction of the pass.  Tensor-core splits: whole 128-key tiles,
-  // about four items per SM (one 224 KB CTA per SM at a time).
-  int64_t split;
-  if (tc_decode) {
-    split = (page_heads + (int64_t)sms * 4 - 1) / ((int64_t)sms * 4);
-    split = (split + 7) / 8 * 8;
-    split = std::max<int64_t>(32, std::min<int64_t>(2048, split));
-  } else {
-    split = (page_heads + (int64_t)sms * 40 - 1) / ((int64_t)sms * 40);
-    split = std::max<int64_t>(16, std::min<int64_t>(1024, split));
-  }
+  // about four items per SM.
+  int64_t split_tc = (page_heads + (int64_t)sms * 4 - 1) / ((int64_t)sms * 4);
+  split_tc = (split_tc + 7) / 8 * 8;
+  split_tc = std::max<int64_t>(32, std::min<int64_t>(2048, split_tc));
+  int64_t split_cc = (page_heads + (int64_t)sms * 40 - 1) / ((int64_t)sms * 40);
+  split_cc = std::max<int64_t>(16, std::min<int64_t>(1024, split_cc));
 
+  // decode (qo_len 1) and verify (qo_len 2 .. verify_max) requests
   for (int r = 0; r < batch; ++r) {
-    if (qo[r + 1] - qo[r] != 1) continue;
+    const int nq = qo[r + 1] - qo[r];
+    if (nq < 1 || nq > verify_max) continue;
+    const bool on_tc = tc_decode || nq > 1;
+    const int64_t split = on_tc ? split_tc : split_cc;
     const int np = kv[r + 1] - kv[r];
     const int kv_len = (np - 1) * P + last[r];
-    const int nsplit = (int)((np + split - 1) / split);
+    // splits cut the keys token 0 can see, [0, kv_len - nq], so every split
+    // starts at a key each token sees; the last split also takes the tail
+    const int64_t vis = (int64_t)kv_len - nq + 1;
+    const int nsplit = (int)((vis + split * P - 1) / (split * P));
+    // partial slots: token t of split s at part0 + t * nsplit + s, so each
+    // token's splits are consecutive for its softmax_merge item
     int part0 = -1;
     if (nsplit > 1) {
-      if (!merges.push_back(MergeItem{qo[r], lay.n_parts, nsplit, 0})) return DAA_ERR_WORKSPACE;
+      for (int t = 0; t < nq; ++t)
+        if (!merges.push_back(MergeItem{qo[r] + t, lay.n_parts + t * nsplit, nsplit, 0}))
+          return DAA_ERR_WORKSPACE;
       part0 = lay.n_parts;
-      lay.n_parts += nsplit;
+      lay.n_parts += nsplit * nq;
     }
     for (int s = 0; s < nsplit; ++s) {
       const int lo = (int)(s * split * P);
-      const int hi = std::min<int>(kv_len, (int)((s + 1) * split * P));
-      if (tc_decode) {
+      const int hi = s == nsplit - 1 ? kv_len : (int)((s + 1) * split * P);
+      if (on_tc) {
         PrefillTile t{};
         t.q_row0 = qo[r];
-        t.qo_len = 1;
+        t.qo_len = nq;
         t.kv_len = kv_len;
         t.page_base = kv[r];
         t.tok0 = 0;
-        t.ntok = 1;
+        t.ntok = nq;
         t.ntok1 = 0;
         t.key_lo = lo;
         t.key_hi = hi;
         t.part = part0 >= 0 ? part0 + s : -1;
+        t.part_stride = nsplit;
         t.work = hi - lo;
         if (!tiles.push_back(t)) return DAA_ERR_WORKSPACE;
       } else {
@@ -154,7 +171,7 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
   const bool quads = plan_prefill_quads(d);
   for (int r = 0; r < batch; ++r) {
     const int nq = qo[r + 1] - qo[r];
-    if (nq < 2) continue;
+    if (nq <= verify_max) continue;
     const int np = kv[r + 1] - kv[r];
     const int kv_len = (np - 1) * P + last[r];
     for (int t0 = 0; t0 < nq; t0 += (quads ? 4 : 2) * tpt) {
@@ -183,16 +200,16 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
       if (!tiles.push_back(t)) return DAA_ERR_WORKSPACE;
     }
   }
-  // tensor-core items: prefill items, then one-token decode items (each group
-  // launches its own instantiation of the kernel), most work first
-  std::sort(tiles.data(), tiles.data() + tiles.size(), [](const PrefillTile& x, const PrefillTile& y) {
-    const bool dx = x.qo_len == 1, dy = y.qo_len == 1;
+  // tensor-core items: prefill items, then decode / verify items (each group
+  // launches its own kernel), most work first
+  std::sort(tiles.data(), tiles.data() + tiles.size(), [verify_max](const PrefillTile& x, const PrefillTile& y) {
+    const bool dx = x.qo_len <= verify_max, dy = y.qo_len <= verify_max;
     if (dx != dy) return dy;
     if (x.work != y.work) return x.work > y.work;
     if (x.q_row0 != y.q_row0) return x.q_row0 < y.q_row0;
     return x.tok0 != y.tok0 ? x.tok0 < y.tok0 : x.key_lo < y.key_lo;
   });
-  for (size_t i = 0; i < tiles.size(); ++i) lay.n_dec_tiles += tiles.data()[i].qo_len == 1 ? 1 : 0;
+  for (size_t i = 0; i < tiles.size(); ++i) lay.n_dec_tiles += tiles.data()[i].qo_len <= verify_max ? 1 : 0;
 
   lay.n_units = (int)units.size();
   lay.n_merges = (int)merges.size();

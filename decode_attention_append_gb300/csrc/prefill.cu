@@ -212,10 +212,10 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
                       kvh * g, tile.q_row0 + tile.tok0 + q * tile.ntok, q_full);
     }
     int64_t pid = load_ids(0);
-    // items whose keys reach the request's end read rows appended in this step
-    // (every prefill item; the last split of a decode request): they wait for
-    // the kernel launched before this one
-    if (tile.key_hi >= tile.kv_len) grid_dep_wait();
+    // items whose keys reach the rows appended in this step (the request's
+    // last qo_len keys: every prefill item, the split(s) holding them for a
+    // decode or verify request) wait for the kernel launched before this one
+    if (tile.key_hi > tile.kv_len - tile.qo_len) grid_dep_wait();
     for (int i = 0; i < 2 * n_kt; ++i) {
       const int64_t pid_next = load_ids(i + 1);
       const int st = i % RS;
@@ -377,7 +377,7 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
     ro.q_row = tile.q_row0 + q_tok0 + tl;
     ro.hq = kvh * g + (row - tl * g);
     ro.write = row < q_ntok * g;
-    ro.part = tile.part;
+    ro.part = tile.part >= 0 ? tile.part + tl * tile.part_stride : -1;
     tc_softmax_rows<D, KT>(a, tmem + lane_off, tmem + C::O_COL + q * D + lane_off, s_full, &o_done[q],
                            q, nq == 1, n_kt, kt0, row_end, ro, [&](int b) {
                              if (lane == 0) mbar_arrive(&p_full[b]);

@@ -239,7 +239,7 @@ prefill_pair_kernel(const __grid_constant__ PairParams prm) {
       }
     }
     int64_t id0 = load_ids(0), id1 = load_ids(1), id2 = load_ids(2), id3 = load_ids(3);
-    if (tile.key_hi >= tile.kv_len) grid_dep_wait();  // reads rows appended in this step
+    if (tile.key_hi > tile.kv_len - tile.qo_len) grid_dep_wait();  // reads rows appended in this step
     for (int i = 0; i < 2 * n_kt; ++i) {
       const int st = i % RS;
       const bool is_v = i & 1;

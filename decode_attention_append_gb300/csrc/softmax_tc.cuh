@@ -76,8 +76,11 @@ __device__ __forceinline__ void tc_softmax_rows(const PrefillArgs& a, uint32_t t
     }
     // P = 2^(s * scale - m) as bf16 pairs over the first KT/2 columns of S
     // (the A operand of PV), 32 columns at a time so each chunk of s dies early
+    // a row with no visible key yet (possible in a key split) keeps m = -inf:
+    // subtract 0 instead so its masked scores give p = 0, not NaN
+    const float m_sub = m_use == -INFINITY ? 0.f : m_use;
     const float2 sc2 = make_float2(sc, sc);
-    const float2 nm2 = make_float2(-m_use, -m_use);
+    const float2 nm2 = make_float2(-m_sub, -m_sub);
     float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < KT / 2; c += 32) {
@@ -128,7 +131,7 @@ __device__ __forceinline__ void tc_softmax_rows(const PrefillArgs& a, uint32_t t
   // ---- epilogue: O / l -> bf16 rows of out; lse
   mbar_wait(o_done_q, (n_kt - 1) & 1, a.err);
   tc_fence_after();
-  const float inv = 1.f / l_run;
+  const float inv = l_run > 0.f ? 1.f / l_run : 0.f;  // no visible key: o = 0, lse = -inf
   const bool partial = ro.part >= 0;  // key split: fp32 partial for softmax_merge
   uint16_t* dst = a.out + ((int64_t)ro.q_row * a.Hq + ro.hq) * D;
   float* pdst = a.part_o + ((int64_t)ro.part * a.Hq + ro.hq) * D;

@@ -135,11 +135,14 @@ size_t daa_batch_attention_workspace_size(const int32_t* h_qo_indptr, const int3
  *   out[row][h][:] = sum_{j in J} softmax_J(s)_j * V_r[j][hk][:]      (bf16, RNE)
  *   lse_out[row][h] = ln sum_{j in J} exp(s_j)                          (fp32)
  * where row = qo_indptr[r] + i and K_r / V_r are read from the request's pages.
- * Requests with qo_len > 1 run the tensor-core prefill kernel; requests with
- * qo_len = 1 run a split-KV decode kernel (CUDA cores when a kv head serves
- * fewer than 4 query heads, tensor cores otherwise) followed by the
- * softmax_merge pass for the requests it split.  Rows of requests with
- * qo_len = 0 do not exist; nothing is written.
+ * Routing (results do not depend on it): requests with qo_len = 1 run a
+ * split-KV decode kernel (CUDA cores when a kv head serves fewer than 4 query
+ * heads, tensor cores otherwise); requests with 2 <= qo_len <= min(16, 128 / g)
+ * (g = Hq / Hkv; e.g. speculative-decoding verify steps) run as key-split
+ * items of the tensor-core decode kernel; longer requests run the tensor-core
+ * prefill kernel.  Split requests are combined by the softmax_merge pass, one
+ * merge per token.  Rows of requests with qo_len = 0 do not exist; nothing is
+ * written.
  *
  *  q              device, bf16 [nnz_qo][Hq][head_dim]
  *  kv_pages       device, bf16 pool (read only)

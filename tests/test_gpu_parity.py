@@ -112,6 +112,32 @@ def test_tensor_core_decode_tile_counts(dev, Hq, Hkv, d):
     _run_both(wl, dev)
 
 
+VERIFY = [
+    # (Hq, Hkv, d, causal): verify batches (qo 2..16) mixed with decodes; long kv
+    # forces many key splits, kv = 128k + small puts a split boundary inside
+    # the last qo keys
+    (32, 32, 128, True),
+    (8, 2, 64, True),
+    (32, 4, 128, True),
+    (12, 1, 128, True),
+    (16, 1, 128, False),
+]
+
+
+@pytest.mark.parametrize("case", VERIFY, ids=lambda c: f"Hq{c[0]}_Hkv{c[1]}_d{c[2]}_{'c' if c[3] else 'nc'}")
+def test_verify_batches(dev, case):
+    """Small multi-token requests (speculative-decoding verify) run as key-split
+    items of the tensor-core decode kernel with one softmax_merge per token."""
+    Hq, Hkv, d, causal = case
+    vmax = min(16, 128 // (Hq // Hkv))
+    qos = [q for q in (2, 3, 4, 7, 8, 16) if q <= vmax]
+    reqs = [(q, kv) for q, kv in zip(qos * 2, [20000, 4097, 129, 3000, 8195, 640, 17, 20483, 2051, 520, 16, 12000])]
+    reqs += [(1, 9000), (1, 130)]
+    wl = make_random_workload(131 + Hq + d, Hq, Hkv, d, 16, reqs, extra_pages=9)
+    wl.causal = causal
+    _run_both(wl, dev)
+
+
 def test_decode_kv_len_one_returns_v(dev):
     from gpu_support import gpu_fill, gpu_step, new_pool
     wl = make_random_workload(111, 8, 2, 128, 16, [(1, 1), (1, 1)])
