@@ -51,20 +51,29 @@ TC_DECODE_MIN_GROUP = 4
 
 
 def step_accounting(wl, k=0):
-    """Algorithmic bytes / FLOPs of one step, split by kernel class."""
+    """Algorithmic bytes / FLOPs of one step, split by kernel class.  K/V bytes
+    count each request's keys once; keys of a prefix shared by several requests
+    (pages read in place) count once per step, under the first request."""
     Hq, Hkv, d, P = wl.num_qo_heads, wl.num_kv_heads, wl.head_dim, wl.page_size
     dec_bytes = pre_flops = pre_bytes = 0
     nnz_new = 0
+    seen_prefix = set()
     for r in wl.steps[k].requests:
         nnz_new += r.qo_len
+        sq = wl.seqs[r.seq]
+        kv_read = r.kv_len
+        if sq.prefix >= 0:
+            if sq.prefix in seen_prefix:
+                kv_read -= sq.prefix_len
+            seen_prefix.add(sq.prefix)
         npages = -(-r.kv_len // P)
         if r.qo_len == 1:
-            dec_bytes += r.kv_len * Hkv * d * 2 * 2 + 2 * Hq * d * 2 + npages * 4
+            dec_bytes += kv_read * Hkv * d * 2 * 2 + 2 * Hq * d * 2 + npages * 4
         elif r.qo_len > 1:
             cached = r.kv_len - r.qo_len
             pairs = r.qo_len * cached + r.qo_len * (r.qo_len + 1) // 2 if wl.causal else r.qo_len * r.kv_len
             pre_flops += 4 * d * Hq * pairs
-            pre_bytes += r.kv_len * Hkv * d * 2 * 2 + 2 * r.qo_len * Hq * d * 2 + npages * 4
+            pre_bytes += kv_read * Hkv * d * 2 * 2 + 2 * r.qo_len * Hq * d * 2 + npages * 4
     app_bytes = nnz_new * Hkv * d * 2 * 2 * 2
     tc_decode = wl.group_size >= TC_DECODE_MIN_GROUP
     return dict(decode_bytes=dec_bytes, append_bytes=app_bytes, prefill_flops=pre_flops,
@@ -306,14 +315,26 @@ class OracleSample:
             picked.append(i)
             est += cost
         sw = copy.copy(wl)
-        seqs, sreqs, nxt, orig = [], [], 0, []
-        for j, i in enumerate(picked):
+        seqs, sreqs, nxt, orig, owners = [], [], 0, [], {}
+        for i in picked:
             r = reqs[i]
-            n = -(-r.kv_len // P)
-            seqs.append(type(wl.seqs[r.seq])(wl.seqs[r.seq].length, np.arange(nxt, nxt + n, dtype=np.int32)))
-            nxt += n
-            sreqs.append(Request(j, r.qo_len, r.kv_len))
+            src = wl.seqs[r.seq]
+            shared, head = 0, np.zeros(0, np.int32)
+            if src.prefix >= 0:
+                # a shared prefix keeps one copy, read by every sampled request
+                if src.prefix not in owners:
+                    n = src.prefix_len // P
+                    owners[src.prefix] = len(seqs)
+                    seqs.append(type(src)(src.prefix_len, np.arange(nxt, nxt + n, dtype=np.int32)))
+                    orig.append(src.prefix)
+                    nxt += n
+                shared, head = src.prefix_len, seqs[owners[src.prefix]].pages
+            n = -(-r.kv_len // P) - shared // P
+            pages = np.concatenate([head, np.arange(nxt, nxt + n, dtype=np.int32)])
+            sreqs.append(Request(len(seqs), r.qo_len, r.kv_len))
+            seqs.append(type(src)(src.length, pages, owners.get(src.prefix, -1), shared))
             orig.append(r.seq)
+            nxt += n
         sw.seqs, sw.steps, sw.num_pages = seqs, [Step(sreqs)], max(1, nxt)
         # the sampled sequences keep their original values
         sw._block = lambda seq, kind, block, _w=wl, _o=orig: _w._block(_o[seq], kind, block)
@@ -352,14 +373,17 @@ def cpu_baseline(wl, budget_s=12.0, reps=None):
 
 
 def compact_pool(wl):
-    """Same workload with pages renumbered 0..n-1 in order of use."""
+    """Same workload with pages renumbered 0..n-1 in order of first use (a page
+    shared by several sequences stays shared)."""
     import copy
     w = copy.copy(wl)
-    nxt, seqs = 0, []
+    mapping, seqs = {}, []
     for s in wl.seqs:
-        seqs.append(type(s)(s.length, np.arange(nxt, nxt + len(s.pages), dtype=np.int32)))
-        nxt += len(s.pages)
-    w.seqs, w.num_pages = seqs, max(1, nxt)
+        for a in s.pages:
+            mapping.setdefault(int(a), len(mapping))
+        seqs.append(type(s)(s.length, np.asarray([mapping[int(a)] for a in s.pages], np.int32),
+                            s.prefix, s.prefix_len))
+    w.seqs, w.num_pages = seqs, max(1, len(mapping))
     return w
 
 

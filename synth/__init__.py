@@ -11,8 +11,10 @@ from .workloads import (  # noqa: F401
     Step,
     Workload,
     CONFIG_NAMES,
+    EXTRA_NAMES,
     chunk_schedule,
     make_workload,
     make_prompt_workload,
     make_random_workload,
+    make_shared_prefix_workload,
 )

@@ -49,6 +49,8 @@ _BLOCK = 256  # tokens per independently seeded block
 class Seq:
     length: int                 # final number of tokens of the sequence
     pages: np.ndarray           # int32 page ids reserved, ceil(length / page_size) of them
+    prefix: int = -1            # sequence whose first prefix_len tokens (and pages) this one shares
+    prefix_len: int = 0         # shared tokens, a multiple of page_size
 
 
 @dataclass
@@ -128,9 +130,27 @@ class Workload:
                     seen[r.seq] = r.kv_len - r.qo_len
         return sorted(seen.items())
 
+    def initial_spans(self) -> List[Tuple[int, int, int]]:
+        """(seq, lo, hi): token ranges written before the first step.  A shared
+        prefix is written once, under the sequence that owns it; a sequence that
+        shares it writes only its own tokens [prefix_len, cached)."""
+        spans, owners = [], {}
+        for s, c in self.initial_entries():
+            q = self.seqs[s]
+            lo = 0
+            if q.prefix >= 0:
+                owners[q.prefix] = max(owners.get(q.prefix, 0), q.prefix_len)
+                lo = q.prefix_len
+            if c > lo:
+                spans.append((s, lo, c))
+        for p, n in sorted(owners.items()):
+            if all(x[0] != p for x in spans):
+                spans.insert(0, (p, 0, n))
+        return spans
+
     def initial_table(self):
         """Page table that appends every sequence's initially cached prefix."""
-        return self._table([(s, c, c) for s, c in self.initial_entries()])
+        return self._table([(s, hi - lo, hi) for s, lo, hi in self.initial_spans()])
 
     # ------------------------------------------------------------------- values
     def _block(self, seq: int, kind: int, block: int) -> torch.Tensor:
@@ -143,6 +163,14 @@ class Workload:
 
     def rows_into(self, out: torch.Tensor, seq: int, kind: int, lo: int, hi: int) -> None:
         """Write bf16 rows [lo, hi) of tensor ``kind`` of sequence ``seq`` into out[:hi-lo]."""
+        q = self.seqs[seq] if seq < len(self.seqs) else None
+        if q is not None and q.prefix >= 0 and lo < q.prefix_len and kind != _KIND_Q:
+            # the shared tokens are the prefix owner's
+            n = min(hi, q.prefix_len) - lo
+            self.rows_into(out[:n], q.prefix, kind, lo, lo + n)
+            if hi > q.prefix_len:
+                self.rows_into(out[n:], seq, kind, q.prefix_len, hi)
+            return
         at = 0
         b = lo // _BLOCK
         while lo + at < hi:
@@ -183,7 +211,7 @@ class Workload:
 
     def initial_kv(self) -> Tuple[torch.Tensor, torch.Tensor]:
         """K and V of every sequence's initially cached prefix, concatenated."""
-        spans = [(s, 0, c) for s, c in self.initial_entries()]
+        spans = self.initial_spans()
         return self._gather(_KIND_K, spans), self._gather(_KIND_V, spans)
 
     def step_inputs(self, k: int) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
@@ -206,13 +234,17 @@ class Workload:
         )
 
 
-def chunk_schedule(L: int, C: int) -> List[Tuple[int, int]]:
-    """0-based token ranges [start, end) of the ceil(L/C) chunks of an L-token prompt.
+def chunk_schedule(L: int, C: int, cached: int = 0) -> List[Tuple[int, int]]:
+    """0-based token ranges [start, end) of the chunks of an L-token prompt.
 
     "Chunked prefill" (k4i.top), #core-idea and #correctness: chunk s (1-based)
     covers tokens (s-1)C+1 .. sC; in 0-based half-open form [(s-1)C, min(sC, L)).
+    Section "Relation to prefix caching" (#prefix-cache-interaction): when the
+    first `cached` tokens hit the prefix cache they are skipped, and only the
+    uncached suffix is cut into chunks of C.
     """
-    return [(s * C, min((s + 1) * C, L)) for s in range(-(-L // C))]
+    n = L - cached
+    return [(cached + s * C, cached + min((s + 1) * C, n)) for s in range(-(-n // C))]
 
 
 def _alloc_pages(gen: torch.Generator, num_pages: int, lengths: Sequence[int], P: int) -> List[np.ndarray]:
@@ -247,7 +279,32 @@ def _single_step(name, Hq, Hkv, d, P, seed, prompts, decodes, num_pages=None, de
     return Workload(name, Hq, Hkv, d, P, num_pages, seed, seqs, [Step(reqs)], description=description)
 
 
+def make_shared_prefix_workload(name, Hq, Hkv, d, P, seed, prefix_len, prompts, decodes, description=""):
+    """One step over a prefix shared by every request (a prefix-cache hit).
+
+    Sequence 0 owns the shared prefix (prefix_len tokens, whole pages) and is
+    not itself a request.  prompts: (qo_len, kv_len) chunks of prompts whose
+    first prefix_len tokens are the shared prefix; decodes: kv_len of decode
+    requests that share it too.  Each request's page list is the prefix's
+    pages followed by pages of its own."""
+    assert prefix_len % P == 0
+    lengths = [kv for _, kv in prompts] + list(decodes)
+    own = [L - prefix_len for L in lengths]
+    used = prefix_len // P + sum(-(-x // P) for x in own)
+    num_pages = _pool_pages(used)
+    gen = torch.Generator().manual_seed(seed + 7919)
+    pages = _alloc_pages(gen, num_pages, [prefix_len] + own, P)
+    seqs = [Seq(prefix_len, pages[0])]
+    for L, pg in zip(lengths, pages[1:]):
+        seqs.append(Seq(L, np.concatenate([pages[0], pg]).astype(np.int32), 0, prefix_len))
+    reqs = [Request(1 + i, qo, kv) for i, (qo, kv) in enumerate(prompts)]
+    reqs += [Request(1 + len(prompts) + j, 1, kv) for j, kv in enumerate(decodes)]
+    return Workload(name, Hq, Hkv, d, P, num_pages, seed, seqs, [Step(reqs)], description=description)
+
+
 CONFIG_NAMES = ["tiny_mixed", "mha_decode", "chunked_prefill_mixed", "gqa_decode_shard", "long_prefill"]
+# further workloads beyond the five configurations
+EXTRA_NAMES = ["prefix_shared"]
 
 
 def make_workload(name: str) -> Workload:
@@ -295,6 +352,20 @@ def make_workload(name: str) -> Workload:
         return _single_step(name, 64, 8, 128, 16, seed, [(8192, 16384)] * 4, kv,
                             description="4 prompts of 16384 at chunk 2 of 2 (8192 new over 8192 "
                                         "cached) + 64 decodes kv ~ U[2048,16384]; Hq 64 / Hkv 8, d 128")
+    if name == "prefix_shared":
+        # "Chunked prefill", #prefix-cache-interaction: a 1024-token system
+        # prompt hits the prefix cache, so a 2048-token prompt needs only its
+        # two 512-token suffix chunks.  One prompt at each of those chunks, and
+        # 64 decode requests that share the same system prompt, all reading its
+        # 64 pages in place.
+        seed = 1006
+        g = torch.Generator().manual_seed(seed)
+        kv = (1024 + torch.randint(512, 3072 + 1, (64,), generator=g)).tolist()
+        return make_shared_prefix_workload(name, 32, 8, 128, 16, seed, 1024, [(512, 1536), (512, 2048)], kv,
+                                   description="1024-token system prompt shared by every request "
+                                               "(64 pages read in place): prompts at suffix chunks "
+                                               "[1024,1536) and [1536,2048) + 64 decodes kv = 1024 + "
+                                               "U[512,3072]; Hq 32 / Hkv 8, d 128, P 16")
     raise KeyError(name)
 
 

@@ -52,17 +52,16 @@ def pool_bits(pool: torch.Tensor) -> np.ndarray:
 
 
 def compact(wl):
-    """Copy of wl whose pages are renumbered 0..n-1 in order of use (so the
-    oracle's pool holds only the pages the workload touches)."""
+    """Copy of wl whose pages are renumbered 0..n-1 in order of first use (so
+    the oracle's pool holds only the pages the workload touches; a page shared
+    by several sequences stays shared)."""
     w = copy.copy(wl)
     w.seqs = []
     mapping = {}
-    nxt = 0
     for s in wl.seqs:
-        new = np.arange(nxt, nxt + len(s.pages), dtype=np.int32)
-        for a, b in zip(s.pages, new):
-            mapping[int(a)] = int(b)
-        nxt += len(s.pages)
-        w.seqs.append(type(s)(s.length, new))
-    w.num_pages = max(1, nxt)
+        for a in s.pages:
+            mapping.setdefault(int(a), len(mapping))
+        new = np.asarray([mapping[int(a)] for a in s.pages], np.int32)
+        w.seqs.append(type(s)(s.length, new, s.prefix, s.prefix_len))
+    w.num_pages = max(1, len(mapping))
     return w, mapping

@@ -14,7 +14,8 @@ import pytest
 import torch
 
 import oracle
-from synth import SENTINEL_BF16, make_prompt_workload, make_random_workload, make_workload
+from synth import (SENTINEL_BF16, make_prompt_workload, make_random_workload,
+                   make_shared_prefix_workload, make_workload)
 from support import err_stats, oracle_pool, oracle_step
 
 pytestmark = pytest.mark.gpu
@@ -150,7 +151,8 @@ def test_decode_kv_len_one_returns_v(dev):
         assert torch.equal(out[r], expect)
 
 
-@pytest.mark.parametrize("name", ["mha_decode", "chunked_prefill_mixed", "gqa_decode_shard"])
+@pytest.mark.parametrize("name", ["mha_decode", "chunked_prefill_mixed", "gqa_decode_shard",
+                                  "prefix_shared"])
 def test_config_full_rows(dev, name):
     _run_both(make_workload(name), dev)
 
@@ -188,7 +190,7 @@ def test_chunked_vs_one_shot_gpu(dev):
 
 
 @pytest.mark.parametrize("name", ["tiny_mixed", "mha_decode", "chunked_prefill_mixed",
-                                  "gqa_decode_shard"])
+                                  "gqa_decode_shard", "prefix_shared"])
 def test_append_attention_against_oracle(dev, name):
     """The fused call (append, then attention launched behind it as
     programmatic dependent launches) against the oracle: pool bytes bit-exact,
@@ -213,6 +215,28 @@ def test_append_attention_equals_two_calls(dev, case):
         assert torch.equal(oa.view(torch.int16), ob.view(torch.int16)), f"step {k}: out differs"
         assert torch.equal(la, lb), f"step {k}: lse differs"
     assert np.array_equal(pool_bits(pa), pool_bits(pb))
+
+
+SHARED = [
+    # (seed, Hq, Hkv, d, prefix_len, prompt chunks (qo, kv), decode kv_lens)
+    # g = 2: CUDA-core decode splits, a 7-token verify request, pair prefill
+    (91, 8, 4, 128, 48, [(40, 100), (7, 60)], [49, 120, 300]),
+    # g = 4, head_dim 64: tensor-core decode and the single-CTA prefill kernel
+    (92, 16, 4, 64, 64, [(100, 250)], [65, 1000, 77]),
+    # g = 12: twenty decodes over one 256-token prefix, a chunk right after it
+    (93, 12, 1, 128, 256, [(12, 268), (300, 556)], [257 + 37 * i for i in range(20)]),
+]
+
+
+@pytest.mark.parametrize("case", SHARED, ids=lambda c: f"seed{c[0]}")
+@pytest.mark.parametrize("fused", [False, True])
+def test_shared_prefix_pages(dev, case, fused):
+    """Prefix-cache hits ("Chunked prefill", #prefix-cache-interaction): every
+    request reads the same physical prefix pages; outputs match the oracle and
+    the append leaves the shared pages untouched (pool bit-exact)."""
+    seed, Hq, Hkv, d, sp, prompts, decodes = case
+    wl = make_shared_prefix_workload(f"shared_{seed}", Hq, Hkv, d, 16, seed, sp, prompts, decodes)
+    _run_both(wl, dev, fused=fused)
 
 
 def test_no_device_error_recorded(dev):

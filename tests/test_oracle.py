@@ -7,6 +7,7 @@ properties, dense brute force, page-permutation invariance), a dropped term in
 the softmax or its log-sum-exp (merge identity, special cases, library
 log-sum-exp), a wrong append byte count (the IO-overhead worked example).
 """
+import copy
 import json
 import math
 import os
@@ -17,8 +18,8 @@ import torch
 
 import oracle
 from oracle import dense
-from synth import (SENTINEL_BF16, chunk_schedule, make_prompt_workload, make_random_workload,
-                   make_workload)
+from synth import (SENTINEL_BF16, Request, Step, chunk_schedule, make_prompt_workload,
+                   make_random_workload, make_shared_prefix_workload, make_workload)
 from support import oracle_pool, oracle_step
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -374,3 +375,115 @@ def test_sampled_rows_match_full_run():
     part, plse, _ = oracle.attention(q, pool, t["qo_indptr"], t["kv_indptr"], t["page_indices"],
                                      t["last_page_len"], True, wl.sm_scale, 4, sel_rows=sel)
     assert np.array_equal(part, full[sel]) and np.array_equal(plse, lse[sel])
+
+
+# ------------------------------------------------------------- prefix caching
+def test_prefix_cache_schedule_worked_example():
+    """#prefix-cache-interaction: with the 1024-token system prompt cached, the
+    2048-token prompt runs 2 chunks of 512 (user query 0-511, 512-1023)
+    instead of 4."""
+    g = _golden("prefix_cache_schedule.json")
+    L, sp, C = g["system_prompt"] + g["user_query"], g["system_prompt"], g["C"]
+    assert len(chunk_schedule(L, C)) == g["chunks_without_cache"]
+    hit = chunk_schedule(L, C, cached=sp)
+    assert [[a - sp, b - 1 - sp] for a, b in hit] == g["user_chunks_inclusive"]
+
+
+def _shared_tiny(seed=61, Hq=4, Hkv=2, d=16, P=4):
+    # prefix of 12 tokens (3 pages) shared by a prompt chunk, a longer prompt
+    # chunk with cached tokens of its own, and three decodes
+    return make_shared_prefix_workload("shared_tiny", Hq, Hkv, d, P, seed, 12,
+                                       [(5, 17), (6, 27)], [13, 20, 31])
+
+
+def test_shared_prefix_pages_equal_private_copies():
+    """#prefix-cache-interaction: a prefix-cache hit only changes where the
+    cached keys come from.  Requests that read one physical copy of the prefix
+    pages give exactly the outputs of requests that each hold a private copy
+    of the same values, and the step's append leaves the shared pages as they
+    were."""
+    ws = _shared_tiny()
+    pool = oracle_pool(ws)
+    shared_pages = ws.seqs[0].pages
+    before = pool[shared_pages].copy()
+    out_s, lse_s, _ = oracle_step(ws, pool, 0)
+    assert np.array_equal(pool[shared_pages], before)
+    # private copies: same values, each request's prefix in pages of its own
+    wp = copy.copy(ws)
+    wp.seqs = [type(s)(s.length, s.pages.copy(), s.prefix, s.prefix_len) for s in ws.seqs]
+    nxt = ws.num_pages
+    for s in wp.seqs[1:]:
+        n = len(shared_pages)
+        s.pages[:n] = np.arange(nxt, nxt + n)
+        nxt += n
+    wp.num_pages = nxt
+    ppool = oracle.new_pool(wp.pool_shape(), SENTINEL_BF16)
+    for i in range(1, len(wp.seqs)):   # each private copy gets the prefix rows
+        n = wp.seqs[i].prefix_len
+        t = wp._table([(i, n, n)])
+        oracle.kv_append(ppool, ws.k_rows(0, 0, n), ws.v_rows(0, 0, n), t["qo_indptr"],
+                         t["page_indices"], t["kv_indptr"], t["last_page_len"])
+    it = ws.initial_table()
+    k0, v0 = ws.initial_kv()
+    nprefix = ws.seqs[1].prefix_len
+    # the sequences' own cached tokens (after the prefix owner's span)
+    own = wp._table([(s, hi - lo, hi) for s, lo, hi in ws.initial_spans() if s != 0])
+    oracle.kv_append(ppool, k0[nprefix:], v0[nprefix:], own["qo_indptr"], own["page_indices"],
+                     own["kv_indptr"], own["last_page_len"])
+    assert it["qo_indptr"][1] == nprefix
+    out_p, lse_p, _ = oracle_step(wp, ppool, 0)
+    assert np.array_equal(out_s, out_p) and np.array_equal(lse_s, lse_p)
+
+
+def test_shared_prefix_matches_torch_sdpa():
+    """Library attention on K/V taken from the generator (shared prefix rows,
+    then each request's own rows), not from the pool: pins the gather of
+    shared pages and the causal offset of a chunk after a prefix hit."""
+    ws = _shared_tiny(seed=62, Hq=6, Hkv=2, d=32, P=4)
+    pool = oracle_pool(ws)
+    out, lse, _ = oracle_step(ws, pool, 0)
+    q, _, _ = ws.step_inputs(0)
+    g = ws.group_size
+    row = 0
+    for r in ws.steps[0].requests:
+        K, V = ws.k_rows(r.seq, 0, r.kv_len), ws.v_rows(r.seq, 0, r.kv_len)
+        Qt = torch.from_numpy(_f64(q[row:row + r.qo_len]).transpose(1, 0, 2).copy())
+        Kt = torch.from_numpy(np.repeat(_f64(K), g, axis=1).transpose(1, 0, 2).copy())
+        Vt = torch.from_numpy(np.repeat(_f64(V), g, axis=1).transpose(1, 0, 2).copy())
+        mask = torch.ones(r.qo_len, r.kv_len, dtype=torch.bool).tril(diagonal=r.kv_len - r.qo_len)
+        ref = torch.nn.functional.scaled_dot_product_attention(Qt, Kt, Vt, attn_mask=mask,
+                                                               scale=ws.sm_scale)
+        np.testing.assert_allclose(out[row:row + r.qo_len], ref.numpy().transpose(1, 0, 2),
+                                   rtol=0, atol=1e-12)
+        row += r.qo_len
+    assert row == out.shape[0]
+
+
+def test_prefix_hit_equals_recompute():
+    """#prefix-cache-interaction with #correctness: the 2 suffix chunks run
+    after a prefix hit give the same outputs as the last 2 of the 4 chunks of
+    the same prompt computed from scratch, and the pages end up holding the
+    same bytes."""
+    L, C, sp, Hq, Hkv, d, P = 64, 16, 32, 4, 2, 16, 4
+    # A: prefix hit -- the system prompt (seq 0) is cached and shared; the
+    # prompt (seq 1) runs its two suffix chunks as two steps
+    wa = make_shared_prefix_workload("hit", Hq, Hkv, d, P, 71, sp, [(C, sp + C)], [])
+    wa.seqs[1].length = L
+    extra = np.arange(wa.num_pages, wa.num_pages + (L - sp - C) // P, dtype=np.int32)
+    wa.seqs[1].pages = np.concatenate([wa.seqs[1].pages, extra])
+    wa.num_pages += len(extra)
+    wa.steps = [Step([Request(1, b - a, b)]) for a, b in chunk_schedule(L, C, cached=sp)]
+    pa = oracle_pool(wa)
+    outs_a = [oracle_step(wa, pa, k) for k in range(len(wa.steps))]
+    # B: the same prompt values from scratch, 4 chunks, private pages
+    wb = make_prompt_workload(L, C, Hq, Hkv, d, P, 71, num_pages=wa.num_pages)
+    wb.seqs[0].pages = wa.seqs[1].pages.copy()
+    wb.rows_into = lambda out, seq, kind, lo, hi: wa.rows_into(out, 1, kind, lo, hi)
+    pb = oracle_pool(wb)
+    outs_b = [oracle_step(wb, pb, k) for k in range(len(wb.steps))]
+    assert len(outs_a) == 2 and len(outs_b) == 4
+    for (oa, la, na), (ob, lb, nb) in zip(outs_a, outs_b[2:]):
+        np.testing.assert_allclose(oa, ob, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(la, lb, rtol=0, atol=1e-12)
+        assert na == nb
+    assert np.array_equal(pa[wa.seqs[1].pages], pb[wb.seqs[0].pages])
