@@ -55,7 +55,7 @@ def _load():
         lib.oracle_kv_append.argtypes = [P, i64, P, P, P, P, P, P, i32, i32, i32, i32]
         lib.oracle_attention.restype = i32
         lib.oracle_attention.argtypes = [P, P, i64, P, P, P, P, i32, i32, i32, i32, i32, i32,
-                                         dbl, P, i64, P, P, P]
+                                         P, i32, dbl, P, i64, P, P, P]
         lib.oracle_attention_keyrange.restype = i32
         lib.oracle_attention_keyrange.argtypes = [P, P, i64, P, P, P, P, i32, i32, i32, i32, i32,
                                                   dbl, i64, i32, i64, i64, P, P, P]
@@ -117,8 +117,9 @@ def kv_append(pool: np.ndarray, k_new, v_new, append_indptr, page_indices, kv_in
 
 
 def attention(q, pool: np.ndarray, qo_indptr, kv_indptr, page_indices, last_page_len,
-              causal: bool, sm_scale: float, num_qo_heads: int, sel_rows=None):
-    """Returns (out fp64 [rows, Hq, d], lse fp64 [rows, Hq], attended pairs)."""
+              causal: bool, sm_scale: float, num_qo_heads: int, sel_rows=None, tree_mask=None):
+    """Returns (out fp64 [rows, Hq, d], lse fp64 [rows, Hq], attended pairs).
+    tree_mask: optional uint32 [nnz_qo, words] draft-tree mask rows."""
     num_pages, _, Hkv, P, d = pool.shape
     qq = _u16(q)
     qi, ki, pi, ll = _i32(qo_indptr), _i32(kv_indptr), _i32(page_indices), _i32(last_page_len)
@@ -129,8 +130,13 @@ def attention(q, pool: np.ndarray, qo_indptr, kv_indptr, page_indices, last_page
     out = np.zeros((rows, num_qo_heads, d), np.float64)
     lse = np.zeros((rows, num_qo_heads), np.float64)
     pairs = ctypes.c_int64(0)
+    tm = None
+    if tree_mask is not None:
+        tm = np.ascontiguousarray(np.asarray(tree_mask, np.uint32))
+        assert tm.ndim == 2 and tm.shape[0] == nnz
     _check(_load().oracle_attention(_ptr(qq), _ptr(pool), num_pages, _ptr(qi), _ptr(ki), _ptr(pi),
                                     _ptr(ll), batch, num_qo_heads, Hkv, d, P, int(bool(causal)),
+                                    _ptr(tm), 0 if tm is None else tm.shape[1],
                                     float(sm_scale), _ptr(sel), 0 if sel is None else len(sel),
                                     _ptr(out), _ptr(lse), ctypes.addressof(pairs)))
     return out, lse, int(pairs.value)

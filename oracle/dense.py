@@ -27,8 +27,13 @@ def request_kv(pool_bits: np.ndarray, page_ids: np.ndarray, kv_len: int):
 
 
 def attention(q_bits, pool_bits, qo_indptr, kv_indptr, page_indices, last_page_len,
-              causal, sm_scale, num_qo_heads):
-    """(out [nnz, Hq, d], lse [nnz, Hq], weights: list per request [Hq, qo, kv])."""
+              causal, sm_scale, num_qo_heads, tree_mask=None):
+    """(out [nnz, Hq, d], lse [nnz, Hq], weights: list per request [Hq, qo, kv]).
+
+    tree_mask: optional uint32 [nnz, words] rows ("Accelerating Sonar through
+    speculation", EAGLE: tree verification under a custom mask): the allowed
+    matrix of a request is all cached columns, plus, over its new-token
+    columns, the lower triangle of the unpacked mask bits with the diagonal."""
     q = bf16_bits_to_f64(q_bits)
     P = pool_bits.shape[3]
     Hkv = pool_bits.shape[2]
@@ -50,7 +55,13 @@ def attention(q_bits, pool_bits, qo_indptr, kv_indptr, page_indices, last_page_l
         if causal:
             i = np.arange(qo)[:, None]
             j = np.arange(kv_len)[None, :]
-            S = np.where(j <= (kv_len - qo) + i, S, -np.inf)
+            allowed = j <= (kv_len - qo) + i
+            if tree_mask is not None:
+                bits = np.unpackbits(np.ascontiguousarray(tree_mask[q0:q1]).view(np.uint8), axis=1,
+                                     bitorder="little")[:, :qo].astype(bool)
+                new = np.tril(bits, -1) | np.eye(qo, dtype=bool)
+                allowed = np.concatenate([np.ones((qo, kv_len - qo), bool), new], axis=1)
+            S = np.where(allowed, S, -np.inf)
         m = S.max(axis=2, keepdims=True)
         E = np.exp(S - m)
         Z = E.sum(axis=2, keepdims=True)

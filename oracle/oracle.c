@@ -15,6 +15,9 @@
  *    (K_cache += [k_{(s-1)C+1} .. k_{sC}]).
  *  - same page, "IO overhead" (#io-overhead): the append writes C x 2 (K and V)
  *    x n_h x d_h x 2 bytes per layer.
+ *  - "Accelerating Sonar through speculation" (Perplexity), section EAGLE:
+ *    verifying a tree of draft tokens needs a custom attention mask; each
+ *    draft token is scored against the accepted prefix and its own branch.
  *  - "Disaggregated prefill and decode" (Perplexity), section "Sharded KV cache
  *    transfers" and its figure "NHD and HND KV cache layouts": in the HND
  *    layout the head dimension precedes the token dimension inside a page, so
@@ -150,26 +153,47 @@ static const uint16_t *paged_row(const uint16_t *pool, const int32_t *page_indic
 }
 
 /*
- * softmax(q . K^T * sm_scale) V over keys [lo, hi) of request r, kv head h:
+ * Visibility of key j under a draft-tree mask (EAGLE section: tree
+ * verification uses a custom attention mask).  The request's new tokens
+ * t = 0 .. qo_len-1 sit at absolute positions draft0 + t.  New token `tok`
+ * sees every cached key (j < draft0), itself, and each earlier new token
+ * t < tok whose bit is set in its mask row (word t / 32, bit t % 32), and no
+ * later new token.  mrow == NULL: every key is visible.
+ */
+static int tree_visible(const uint32_t *mrow, int64_t draft0, int64_t tok, int64_t j)
+{
+    if (!mrow || j < draft0)
+        return 1;
+    int64_t t = j - draft0;
+    if (t == tok)
+        return 1;
+    if (t > tok)
+        return 0;
+    return (int)((mrow[t / 32] >> (t % 32)) & 1u);
+}
+
+/*
+ * softmax(q . K^T * sm_scale) V over the visible keys in [lo, hi) of request
+ * r, kv head h (all of them when mrow is NULL; see tree_visible):
  *   s_j = sm_scale * sum_c q_c K[j][c]
  *   w_j = exp(s_j - max s) / sum_j' exp(s_j' - max s)
  *   o   = sum_j w_j V[j]          lse = max s + ln sum_j exp(s_j - max s)
- * An empty range gives o = 0 and lse = -inf (the identity of softmax_merge).
- * When w is non-NULL the weights are stored at w[j - lo].
+ * An empty set gives o = 0 and lse = -inf (the identity of softmax_merge).
+ * When w is non-NULL the weights are stored at w[j - lo] (0 for hidden keys).
  */
 static void attend(const double *qv, const uint16_t *pool, const int32_t *page_indices,
                    const int32_t *kv_indptr, int r, int h_kv, int64_t lo, int64_t hi,
-                   double sm_scale, int Hkv, int P, int d, double *o, double *lse,
-                   double *w, double *scratch)
+                   double sm_scale, int Hkv, int P, int d, const uint32_t *mrow,
+                   int64_t draft0, int64_t tok, double *o, double *lse, double *w,
+                   double *scratch)
 {
     for (int c = 0; c < d; ++c)
         o[c] = 0.0;
-    if (hi <= lo) {
-        *lse = -INFINITY;
-        return;
-    }
     double m = -INFINITY;
+    int64_t seen = 0;
     for (int64_t j = lo; j < hi; ++j) {
+        if (!tree_visible(mrow, draft0, tok, j))
+            continue;
         const uint16_t *k = paged_row(pool, page_indices, kv_indptr, r, j, 0, h_kv, Hkv, P, d);
         double s = 0.0;
         for (int c = 0; c < d; ++c)
@@ -178,14 +202,28 @@ static void attend(const double *qv, const uint16_t *pool, const int32_t *page_i
         scratch[j - lo] = s;
         if (s > m)
             m = s;
+        ++seen;
+    }
+    if (seen == 0) {
+        *lse = -INFINITY;
+        for (int64_t j = lo; w && j < hi; ++j)
+            w[j - lo] = 0.0;
+        return;
     }
     double z = 0.0;
     for (int64_t j = lo; j < hi; ++j) {
+        if (!tree_visible(mrow, draft0, tok, j))
+            continue;
         double e = exp(scratch[j - lo] - m);
         scratch[j - lo] = e;
         z += e;
     }
     for (int64_t j = lo; j < hi; ++j) {
+        if (!tree_visible(mrow, draft0, tok, j)) {
+            if (w)
+                w[j - lo] = 0.0;
+            continue;
+        }
         double wj = scratch[j - lo] / z;
         if (w)
             w[j - lo] = wj;
@@ -217,11 +255,14 @@ static int row_request(const int32_t *qo_indptr, int batch, int64_t row)
  * outputs are then packed [n_sel][Hq][d].  pairs_out (may be NULL) receives the
  * number of (query token, key) pairs attended, summed over the computed rows
  * (per query head group, i.e. not multiplied by Hq).
+ * tree_mask (may be NULL): uint32 [nnz_qo][mask_words] draft-tree mask rows
+ * (see tree_visible); it needs causal = 1 and qo_len <= 32 * mask_words.
  */
 int oracle_attention(const uint16_t *q, const uint16_t *pool, int64_t num_pages,
                      const int32_t *qo_indptr, const int32_t *kv_indptr,
                      const int32_t *page_indices, const int32_t *last_page_len,
                      int batch, int Hq, int Hkv, int d, int P, int causal,
+                     const uint32_t *tree_mask, int mask_words,
                      double sm_scale, const int64_t *sel_rows, int64_t n_sel,
                      double *out, double *lse, int64_t *pairs_out)
 {
@@ -231,6 +272,13 @@ int oracle_attention(const uint16_t *q, const uint16_t *pool, int64_t num_pages,
                          num_pages, P);
     if (st != OR_OK)
         return st;
+    if (tree_mask) {
+        if (!causal || mask_words < 1)
+            return OR_ERR_ARG;
+        for (int r = 0; r < batch; ++r)
+            if ((int64_t)qo_indptr[r + 1] - qo_indptr[r] > 32 * (int64_t)mask_words)
+                return OR_ERR_SHAPE;
+    }
     int64_t nnz = batch > 0 ? qo_indptr[batch] : 0;
     int64_t nrows = sel_rows ? n_sel : nnz;
     int64_t max_kv = 0;
@@ -261,13 +309,16 @@ int oracle_attention(const uint16_t *q, const uint16_t *pool, int64_t num_pages,
             int h_kv = (int)((int64_t)h * Hkv / Hq);
             for (int c = 0; c < d; ++c)
                 qv[c] = bf16_to_f64(q[(row * Hq + h) * (int64_t)d + c]);
+            const uint32_t *mrow = tree_mask ? tree_mask + row * (int64_t)mask_words : NULL;
             double l;
             attend(qv, pool, page_indices, kv_indptr, r, h_kv, 0, hi, sm_scale, Hkv, P, d,
-                   out + (idx * Hq + h) * (int64_t)d, &l, NULL, scratch);
+                   mrow, kv_len - qo_len, i, out + (idx * Hq + h) * (int64_t)d, &l, NULL,
+                   scratch);
             if (lse)
                 lse[idx * Hq + h] = l;
             if (h == 0)
-                pairs += hi;
+                for (int64_t j = 0; j < hi; ++j)
+                    pairs += tree_visible(mrow, kv_len - qo_len, i, j);
         }
         free(scratch);
         free(qv);
@@ -307,7 +358,7 @@ int oracle_attention_keyrange(const uint16_t *q, const uint16_t *pool, int64_t n
     for (int c = 0; c < d; ++c)
         qv[c] = bf16_to_f64(q[(row * Hq + h) * (int64_t)d + c]);
     attend(qv, pool, page_indices, kv_indptr, r, (int)((int64_t)h * Hkv / Hq), lo, hi,
-           sm_scale, Hkv, P, d, o, lse, w, scratch);
+           sm_scale, Hkv, P, d, NULL, 0, 0, o, lse, w, scratch);
     free(qv);
     free(scratch);
     return OR_OK;

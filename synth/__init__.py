@@ -17,4 +17,7 @@ from .workloads import (  # noqa: F401
     make_prompt_workload,
     make_random_workload,
     make_shared_prefix_workload,
+    make_tree_workload,
+    random_tree,
+    tree_mask_rows,
 )

@@ -30,7 +30,7 @@ from __future__ import annotations
 
 import math
 from dataclasses import dataclass
-from typing import Dict, List, Sequence, Tuple
+from typing import Dict, List, Optional, Sequence, Tuple
 
 import numpy as np
 import torch
@@ -58,6 +58,7 @@ class Request:
     seq: int                    # index into Workload.seqs
     qo_len: int                 # new tokens appended and attended this step
     kv_len: int                 # tokens attended after the append (cached + new)
+    parents: Optional[np.ndarray] = None  # draft tree over the new tokens: parent index or -1
 
 
 @dataclass
@@ -219,6 +220,21 @@ class Workload:
         spans = [(r.seq, r.kv_len - r.qo_len, r.kv_len) for r in self.steps[k].requests]
         return self._gather(_KIND_Q, spans), self._gather(_KIND_K, spans), self._gather(_KIND_V, spans)
 
+    # ------------------------------------------------------------ tree masks
+    def has_tree(self, k: int = 0) -> bool:
+        return any(r.parents is not None for r in self.steps[k].requests)
+
+    def tree_mask(self, k: int = 0, words: Optional[int] = None) -> np.ndarray:
+        """uint32 [nnz_qo, words] mask rows of step k (see ``tree_mask_rows``);
+        requests without a tree get the chain (every earlier new token)."""
+        reqs = self.steps[k].requests
+        W = words or max(1, -(-max(r.qo_len for r in reqs) // 32))
+        rows = []
+        for r in reqs:
+            par = r.parents if r.parents is not None else np.arange(r.qo_len) - 1
+            rows.append(tree_mask_rows(par, W))
+        return np.concatenate(rows, 0) if rows else np.zeros((0, W), np.uint32)
+
     # ------------------------------------------------------------- accounting
     def summary(self, k: int = 0) -> Dict:
         reqs = self.steps[k].requests
@@ -245,6 +261,33 @@ def chunk_schedule(L: int, C: int, cached: int = 0) -> List[Tuple[int, int]]:
     """
     n = L - cached
     return [(cached + s * C, cached + min((s + 1) * C, n)) for s in range(-(-n // C))]
+
+
+def random_tree(gen: torch.Generator, n: int, roots: int = 1) -> np.ndarray:
+    """Parent index of each of n draft-tree nodes in topological order (a
+    random recursive tree: node i hangs under a uniformly drawn earlier node;
+    the first `roots` nodes hang under the cached prefix, parent -1)."""
+    par = np.full(n, -1, np.int64)
+    for i in range(roots, n):
+        par[i] = int(torch.randint(0, i, (1,), generator=gen))
+    return par
+
+
+def tree_mask_rows(parents: np.ndarray, words: int) -> np.ndarray:
+    """Encode a draft tree as attention-mask rows: uint32 [n, words], bit j of
+    row i (word j // 32, bit j % 32) set when new token j is an ancestor of new
+    token i.  Bit i (the token itself) is set too.  Input layout only: the
+    encoding of which earlier draft tokens each token may see."""
+    n = len(parents)
+    assert n <= 32 * words
+    rows = np.zeros((n, words), np.uint32)
+    for i in range(n):
+        j = i
+        while j >= 0:
+            rows[i, j // 32] |= np.uint32(1 << (j % 32))
+            j = int(parents[j])
+            assert j < i
+    return rows
 
 
 def _alloc_pages(gen: torch.Generator, num_pages: int, lengths: Sequence[int], P: int) -> List[np.ndarray]:
@@ -302,9 +345,31 @@ def make_shared_prefix_workload(name, Hq, Hkv, d, P, seed, prefix_len, prompts, 
     return Workload(name, Hq, Hkv, d, P, num_pages, seed, seqs, [Step(reqs)], description=description)
 
 
+def make_tree_workload(name, Hq, Hkv, d, P, seed, trees, decodes=(), prompts=(), num_pages=None,
+                       description=""):
+    """One step of draft-tree verification ("Accelerating Sonar through
+    speculation", section EAGLE).  trees: (n_nodes, cached tokens, roots) per
+    verify request -- its n_nodes draft tokens are appended after the cached
+    ones and attended through the tree mask; decodes: kv_len of decode
+    requests; prompts: (qo_len, kv_len) of plain causal chunks."""
+    gen = torch.Generator().manual_seed(seed + 104729)
+    lengths = [c + n for n, c, _ in trees] + [kv for _, kv in prompts] + list(decodes)
+    used = sum(-(-x // P) for x in lengths)
+    if num_pages is None:
+        num_pages = _pool_pages(used)
+    pages = _alloc_pages(torch.Generator().manual_seed(seed + 7919), num_pages, lengths, P)
+    seqs = [Seq(L, pg) for L, pg in zip(lengths, pages)]
+    reqs = [Request(i, n, c + n, random_tree(gen, n, roots)) for i, (n, c, roots) in enumerate(trees)]
+    at = len(trees)
+    reqs += [Request(at + i, qo, kv) for i, (qo, kv) in enumerate(prompts)]
+    at += len(prompts)
+    reqs += [Request(at + i, 1, kv) for i, kv in enumerate(decodes)]
+    return Workload(name, Hq, Hkv, d, P, num_pages, seed, seqs, [Step(reqs)], description=description)
+
+
 CONFIG_NAMES = ["tiny_mixed", "mha_decode", "chunked_prefill_mixed", "gqa_decode_shard", "long_prefill"]
 # further workloads beyond the five configurations
-EXTRA_NAMES = ["prefix_shared"]
+EXTRA_NAMES = ["prefix_shared", "tree_verify"]
 
 
 def make_workload(name: str) -> Workload:
@@ -366,6 +431,18 @@ def make_workload(name: str) -> Workload:
                                                "(64 pages read in place): prompts at suffix chunks "
                                                "[1024,1536) and [1536,2048) + 64 decodes kv = 1024 + "
                                                "U[512,3072]; Hq 32 / Hkv 8, d 128, P 16")
+    if name == "tree_verify":
+        # "Accelerating Sonar through speculation", section EAGLE: the target
+        # model verifies a tree of draft tokens under a custom attention mask.
+        # 32 requests, each a 64-node draft tree (random recursive tree, one
+        # root) over kv ~ U[1024, 4096] cached tokens; 7B-class GQA 32 / 8.
+        seed = 1007
+        g = torch.Generator().manual_seed(seed)
+        cached = torch.randint(1024, 4096 + 1, (32,), generator=g).tolist()
+        return make_tree_workload(name, 32, 8, 128, 16, seed, [(64, c, 1) for c in cached],
+                                  description="32 verify requests, each a 64-node draft tree "
+                                              "(random recursive tree) over kv ~ U[1024,4096] cached "
+                                              "tokens under its tree mask; Hq 32 / Hkv 8, d 128, P 16")
     raise KeyError(name)
 
 

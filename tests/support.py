@@ -21,14 +21,17 @@ def oracle_pool(wl):
     return pool
 
 
-def oracle_step(wl, pool, k, sel_rows=None):
-    """Append step k's new K/V into `pool` (in place) and attend: (out, lse, pairs)."""
+def oracle_step(wl, pool, k, sel_rows=None, tree_mask=None):
+    """Append step k's new K/V into `pool` (in place) and attend: (out, lse, pairs).
+    A step with draft trees attends under its tree mask (or `tree_mask`)."""
     t = wl.step_table(k)
     q, kn, vn = wl.step_inputs(k)
     oracle.kv_append(pool, kn, vn, t["qo_indptr"], t["page_indices"], t["kv_indptr"], t["last_page_len"])
+    if tree_mask is None and wl.has_tree(k):
+        tree_mask = wl.tree_mask(k)
     return oracle.attention(q, pool, t["qo_indptr"], t["kv_indptr"], t["page_indices"],
                             t["last_page_len"], wl.causal, wl.sm_scale, wl.num_qo_heads,
-                            sel_rows=sel_rows)
+                            sel_rows=sel_rows, tree_mask=tree_mask)
 
 
 def bf16_round(x: np.ndarray) -> np.ndarray:

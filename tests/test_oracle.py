@@ -19,7 +19,8 @@ import torch
 import oracle
 from oracle import dense
 from synth import (SENTINEL_BF16, Request, Step, chunk_schedule, make_prompt_workload,
-                   make_random_workload, make_shared_prefix_workload, make_workload)
+                   make_random_workload, make_shared_prefix_workload, make_tree_workload,
+                   make_workload, tree_mask_rows)
 from support import oracle_pool, oracle_step
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -487,3 +488,111 @@ def test_prefix_hit_equals_recompute():
         np.testing.assert_allclose(la, lb, rtol=0, atol=1e-12)
         assert na == nb
     assert np.array_equal(pa[wa.seqs[1].pages], pb[wb.seqs[0].pages])
+
+
+# --------------------------------------------------------------- tree masks
+TREE_CASES = [
+    # (seed, Hq, Hkv, d, P, trees (nodes, cached, roots), decodes, prompts)
+    (201, 4, 2, 16, 4, [(9, 14, 1), (1, 5, 1), (33, 40, 3)], [11], [(6, 20)]),
+    (202, 6, 2, 8, 16, [(40, 3, 1), (17, 0, 17), (64, 70, 2)], [], []),
+    (203, 2, 2, 8, 4, [(5, 0, 1), (70, 9, 1)], [3, 30], [(3, 3)]),
+]
+
+
+def _tree_run(case):
+    seed, Hq, Hkv, d, P, trees, decodes, prompts = case
+    wl = make_tree_workload(f"tree_{seed}", Hq, Hkv, d, P, seed, trees, decodes, prompts)
+    pool = oracle_pool(wl)
+    out, lse, pairs = oracle_step(wl, pool, 0)
+    return wl, pool, out, lse, pairs
+
+
+@pytest.mark.parametrize("case", TREE_CASES, ids=lambda c: f"seed{c[0]}")
+def test_tree_mask_matches_dense_bruteforce(case):
+    """The C oracle's tree visibility against the NumPy brute force's masked
+    score matrix (unpacked mask bits, strict lower triangle, diagonal)."""
+    wl, pool, out, lse, _ = _tree_run(case)
+    t = wl.step_table(0)
+    q, _, _ = wl.step_inputs(0)
+    dout, dlse, _ = dense.attention(_bits(q), pool, t["qo_indptr"], t["kv_indptr"], t["page_indices"],
+                                    t["last_page_len"], True, wl.sm_scale, wl.num_qo_heads,
+                                    tree_mask=wl.tree_mask(0))
+    np.testing.assert_allclose(out, dout, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, dlse, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("case", TREE_CASES, ids=lambda c: f"seed{c[0]}")
+def test_tree_node_equals_its_branch_as_a_sequence(case):
+    """EAGLE: a draft token is verified against the accepted prefix and its own
+    branch.  Each tree node's output equals library attention (torch SDPA,
+    fp64) of its query over the cached keys followed by the keys of its
+    root-to-node path, walked from the parent array (not from the mask)."""
+    wl, pool, out, lse, pairs = _tree_run(case)
+    q, _, _ = wl.step_inputs(0)
+    g = wl.group_size
+    row, n_pairs = 0, 0
+    for r in wl.steps[0].requests:
+        cached = r.kv_len - r.qo_len
+        K, V = wl.k_rows(r.seq, 0, r.kv_len), wl.v_rows(r.seq, 0, r.kv_len)
+        par = r.parents if r.parents is not None else np.arange(r.qo_len) - 1
+        for i in range(r.qo_len):
+            path, j = [], i
+            while j >= 0:
+                path.append(j)
+                j = int(par[j])
+            keys = list(range(cached)) + [cached + j for j in reversed(path)]
+            n_pairs += len(keys)
+            Kp = torch.from_numpy(np.repeat(_f64(K[keys]), g, axis=1).transpose(1, 0, 2).copy())
+            Vp = torch.from_numpy(np.repeat(_f64(V[keys]), g, axis=1).transpose(1, 0, 2).copy())
+            Qi = torch.from_numpy(_f64(q[row + i:row + i + 1]).transpose(1, 0, 2).copy())
+            ref = torch.nn.functional.scaled_dot_product_attention(Qi, Kp, Vp, scale=wl.sm_scale)
+            np.testing.assert_allclose(out[row + i], ref.numpy()[:, 0], rtol=0, atol=1e-12)
+            ref_lse = torch.logsumexp(torch.einsum("hqc,hkc->hqk", Qi, Kp) * wl.sm_scale, -1)
+            np.testing.assert_allclose(lse[row + i], ref_lse.numpy()[:, 0], rtol=0, atol=1e-12)
+        row += r.qo_len
+    assert pairs == n_pairs
+
+
+def test_chain_mask_equals_causal():
+    """A mask row holding every earlier new token is the plain causal rule:
+    outputs bit-identical to attention without a mask."""
+    wl = make_random_workload(211, 4, 2, 16, 4, [(40, 47), (1, 9), (33, 33)], extra_pages=2)
+    mask = np.concatenate([tree_mask_rows(np.arange(n) - 1, 2) for n in (40, 1, 33)], 0)
+    pa, pb = oracle_pool(wl), oracle_pool(wl)
+    oa, la, na = oracle_step(wl, pa, 0)
+    ob, lb, nb = oracle_step(wl, pb, 0, tree_mask=mask)
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb) and na == nb
+
+
+def test_tree_mask_arguments_checked():
+    wl = make_random_workload(212, 2, 1, 8, 4, [(40, 41)], extra_pages=1)
+    pool = oracle_pool(wl)
+    t = wl.step_table(0)
+    q, _, _ = wl.step_inputs(0)
+    args = (q, pool, t["qo_indptr"], t["kv_indptr"], t["page_indices"], t["last_page_len"])
+    with pytest.raises(oracle.OracleError):          # 40 new tokens need 2 words
+        oracle.attention(*args, True, 0.3, 2, tree_mask=np.zeros((40, 1), np.uint32))
+    with pytest.raises(oracle.OracleError):          # a tree mask needs the causal rule
+        oracle.attention(*args, False, 0.3, 2, tree_mask=np.zeros((40, 2), np.uint32))
+
+
+@pytest.mark.parametrize("case", TREE_CASES[:2], ids=lambda c: f"seed{c[0]}")
+def test_tree_mask_bits_on_and_above_diagonal_are_ignored(case):
+    """Only bits of earlier new tokens count: a token always sees itself and
+    never a later token, whatever its row holds there.  Scrambling every bit
+    on or above the diagonal (the self bit cleared or set, later bits random)
+    leaves the outputs bit-identical."""
+    wl, _, out, lse, pairs = _tree_run(case)
+    mask = wl.tree_mask(0).copy()
+    rng = np.random.default_rng(7)
+    row = 0
+    for r in wl.steps[0].requests:
+        for i in range(r.qo_len):
+            for j in range(i, 32 * mask.shape[1]):
+                w, b = divmod(j, 32)
+                if j == i or rng.random() < 0.5:
+                    mask[row + i, w] ^= np.uint32(1 << b)
+        row += r.qo_len
+    pool = oracle_pool(wl)
+    o2, l2, p2 = oracle_step(wl, pool, 0, tree_mask=mask)
+    assert np.array_equal(out, o2) and np.array_equal(lse, l2) and pairs == p2
