@@ -48,6 +48,9 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 # the tensor-core kernel (as key-split work items); the others in the CUDA-core
 # split-KV kernel.  Mirrors the library planner's routing rule.
 TC_DECODE_MIN_GROUP = 4
+# Requests with 2 <= qo_len <= min(this, 128 / g) run as key-split items of the
+# tensor-core decode kernel (the planner's verify routing).
+VERIFY_MAX_TOKENS = 16
 
 
 def step_accounting(wl, k=0):
@@ -58,6 +61,8 @@ def step_accounting(wl, k=0):
     dec_bytes = pre_flops = pre_bytes = 0
     nnz_new = 0
     seen_prefix = set()
+    verify_max = min(VERIFY_MAX_TOKENS, 128 // wl.group_size)
+    ver_flops = ver_bytes = 0
     for r in wl.steps[k].requests:
         nnz_new += r.qo_len
         sq = wl.seqs[r.seq]
@@ -71,15 +76,30 @@ def step_accounting(wl, k=0):
             dec_bytes += kv_read * Hkv * d * 2 * 2 + 2 * Hq * d * 2 + npages * 4
         elif r.qo_len > 1:
             cached = r.kv_len - r.qo_len
-            pairs = r.qo_len * cached + r.qo_len * (r.qo_len + 1) // 2 if wl.causal else r.qo_len * r.kv_len
-            pre_flops += 4 * d * Hq * pairs
-            pre_bytes += kv_read * Hkv * d * 2 * 2 + 2 * r.qo_len * Hq * d * 2 + npages * 4
+            if r.parents is not None:
+                # draft tree: each node sees the cached keys and its branch
+                depth = np.zeros(r.qo_len, np.int64)
+                for i, p in enumerate(r.parents):
+                    depth[i] = 1 + (depth[p] if p >= 0 else 0)
+                pairs = r.qo_len * cached + int(depth.sum())
+            elif wl.causal:
+                pairs = r.qo_len * cached + r.qo_len * (r.qo_len + 1) // 2
+            else:
+                pairs = r.qo_len * r.kv_len
+            fl = 4 * d * Hq * pairs
+            by = kv_read * Hkv * d * 2 * 2 + 2 * r.qo_len * Hq * d * 2 + npages * 4
+            pre_flops += fl
+            pre_bytes += by
+            if r.qo_len <= verify_max:  # key-split items of the tensor-core decode kernel
+                ver_flops += fl
+                ver_bytes += by
     app_bytes = nnz_new * Hkv * d * 2 * 2 * 2
     tc_decode = wl.group_size >= TC_DECODE_MIN_GROUP
     return dict(decode_bytes=dec_bytes, append_bytes=app_bytes, prefill_flops=pre_flops,
                 prefill_bytes=pre_bytes, nnz_new=nnz_new,
                 # work per kernel
-                tc_flops=pre_flops, tc_bytes=pre_bytes, tc_decode_bytes=dec_bytes if tc_decode else 0,
+                tc_flops=pre_flops - ver_flops, tc_bytes=pre_bytes - ver_bytes,
+                tc_decode_bytes=(dec_bytes if tc_decode else 0) + ver_bytes,
                 cuda_decode_bytes=0 if tc_decode else dec_bytes)
 
 
@@ -208,6 +228,12 @@ class GpuStep:
         self.q, self.k_new, self.v_new = (x.to(device) for x in (q, kn, vn))
         self.runner = daa.BatchAttention(self.table, wl.num_qo_heads, self.pool, causal=wl.causal,
                                          sm_scale=wl.sm_scale)
+        # draft-tree verification: the step's mask rows (int32 view of the bits)
+        self.tree = wl.has_tree(k)
+        self.h_mask = self.mask = None
+        if self.tree:
+            self.h_mask = torch.from_numpy(wl.tree_mask(k).view(np.int32)).pin_memory()
+            self.mask = self.h_mask.to(device)
         self.out = torch.empty_like(self.q)
         self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
         # pinned host copies of the int32 page table (re-sent every e2e step)
@@ -217,23 +243,38 @@ class GpuStep:
         torch.cuda.synchronize()
 
     def step(self):
-        if self.fused:
+        if self.tree:
+            self.runner.append(self.k_new, self.v_new)
+            self.runner.run(self.q, out=self.out, tree_mask=self.mask)
+        elif self.fused:
             self.runner.step(self.k_new, self.v_new, self.q, out=self.out)
         else:
             self.runner.append(self.k_new, self.v_new)
             self.runner.run(self.q, out=self.out)
 
+    def step_plain(self):
+        """The same step without its tree mask (plain causal attention)."""
+        self.runner.append(self.k_new, self.v_new)
+        self.runner.run(self.q, out=self.out)
+
     def step_e2e(self, stream):
         """Public API call with host buffers: H2D inputs, append + attention, D2H out."""
         for d, h in zip(self.d_ints, self.h_ints):
             d.copy_(h, non_blocking=True)
+        if self.tree:
+            self.mask.copy_(self.h_mask, non_blocking=True)
         self.q.copy_(self.h_q, non_blocking=True)
         self.k_new.copy_(self.h_k, non_blocking=True)
         self.v_new.copy_(self.h_v, non_blocking=True)
         qo, kv, pi, ll = self.d_ints
         hosts = (self.host_table["qo_indptr"], self.host_table["kv_indptr"],
                  self.host_table["last_page_len"])
-        if self.fused:
+        if self.tree:
+            self.daa.kv_append(self.k_new, self.v_new, self.pool, qo, pi, kv, ll)
+            self.daa.batch_attention_tree(self.q, self.pool, qo, kv, pi, ll, self.mask,
+                                          self.wl.sm_scale, out=self.out,
+                                          workspace=self.runner.workspace, host_indptr=hosts)
+        elif self.fused:
             self.daa.append_attention(self.k_new, self.v_new, self.q, self.pool, qo, kv, pi, ll,
                                       self.wl.causal, self.wl.sm_scale, out=self.out,
                                       workspace=self.runner.workspace, host_indptr=hosts)
@@ -247,6 +288,8 @@ class GpuStep:
     def e2e_bytes(self):
         h2d = sum(x.numel() * x.element_size() for x in self.h_ints)
         h2d += sum(x.numel() * x.element_size() for x in (self.h_q, self.h_k, self.h_v))
+        if self.tree:
+            h2d += self.h_mask.numel() * self.h_mask.element_size()
         d2h = self.h_out.numel() * self.h_out.element_size()
         return h2d, d2h
 
@@ -331,7 +374,7 @@ class OracleSample:
                 shared, head = src.prefix_len, seqs[owners[src.prefix]].pages
             n = -(-r.kv_len // P) - shared // P
             pages = np.concatenate([head, np.arange(nxt, nxt + n, dtype=np.int32)])
-            sreqs.append(Request(len(seqs), r.qo_len, r.kv_len))
+            sreqs.append(Request(len(seqs), r.qo_len, r.kv_len, r.parents))
             seqs.append(type(src)(src.length, pages, owners.get(src.prefix, -1), shared))
             orig.append(r.seq)
             nxt += n
@@ -346,6 +389,7 @@ class OracleSample:
                          it["last_page_len"])
         self.table = sw.step_table(0)
         self.q, self.kn, self.vn = sw.step_inputs(0)
+        self.mask = sw.tree_mask(0) if sw.has_tree(0) else None
         acc = step_accounting(sw)
         self.nbytes = acc["decode_bytes"] + acc["append_bytes"] + acc["prefill_bytes"]
         self.sample = (f"{len(picked)} of {len(reqs)} requests of step 0 (whole requests, decodes "
@@ -358,7 +402,8 @@ class OracleSample:
         o.kv_append(self.pool, self.kn, self.vn, st["qo_indptr"], st["page_indices"], st["kv_indptr"],
                     st["last_page_len"])
         o.attention(self.q, self.pool, st["qo_indptr"], st["kv_indptr"], st["page_indices"],
-                    st["last_page_len"], self.sw.causal, self.sw.sm_scale, self.sw.num_qo_heads)
+                    st["last_page_len"], self.sw.causal, self.sw.sm_scale, self.sw.num_qo_heads,
+                    tree_mask=self.mask)
         return time.perf_counter() - t0
 
 
@@ -512,6 +557,14 @@ def main():
         ms_e2e = timed(lambda: g.step_e2e(torch.cuda.current_stream()), args.steps, flush)
         barrier()
     h2d, d2h = g.e2e_bytes()
+    # draft-tree batches: the same steps without the mask, for the mask's cost
+    ms_plain = None
+    if g.tree and not args.quick:
+        for _ in range(3):
+            g.step_plain()
+        barrier()
+        ms_plain = timed(g.step_plain, args.steps, flush)
+        barrier()
     err = daa.device_error(reset=True)
 
     t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
@@ -576,6 +629,11 @@ def main():
             "algorithmic": {"bytes_per_step": algo_bytes, "decode_bytes": acc["decode_bytes"],
                             "append_bytes": acc["append_bytes"], "prefill_flops": acc["prefill_flops"]},
             "clocks": clk, "device_error": err}
+    if ms_plain is not None:
+        line["tree_mask"] = {"ms_per_step_masked": ms / args.steps,
+                             "ms_per_step_unmasked": ms_plain / args.steps,
+                             "overhead": ms / ms_plain - 1.0,
+                             "note": "same batch and kernels, plain causal attention without the mask"}
     if acc["prefill_flops"] and "prefill_tc" in per_kernel:
         # conservative: the kernel time also covers any decode splits it ran
         pm = float(np.mean(per_kernel["prefill_tc"]))

@@ -13,6 +13,9 @@ Entry points (same names as the C ABI, without the ``daa_`` prefix):
   last_page_len, causal, sm_scale, ...)`` -- attention for a batch mixing
   chunked-prefill requests (qo_len > 1, causal with the cache offset) and decode
   requests (qo_len = 1).
+* ``batch_attention_tree(..., tree_mask, ...)`` -- the same attention with
+  draft-tree masks over each request's new tokens (speculative-decoding
+  verification of a tree of draft tokens).
 * ``BatchAttention`` -- plans once from host copies of the page table and owns
   the workspace, for repeated calls over the same batch shape.
 
@@ -80,6 +83,9 @@ def load_library():
         lib.daa_append_attention.restype = i32
         lib.daa_append_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32,
                                              vp, vp, vp, sz, _Dims, vp]
+        lib.daa_batch_attention_tree.restype = i32
+        lib.daa_batch_attention_tree.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, f32,
+                                                 vp, vp, vp, sz, _Dims, vp]
         lib.daa_batch_attention_noalloc.restype = i32
         lib.daa_batch_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32,
                                                     vp, vp, _Dims, vp]
@@ -210,6 +216,56 @@ def batch_attention(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_l
     return out
 
 
+def batch_attention_tree(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len, tree_mask,
+                         sm_scale=None, out=None, lse=None, workspace=None, host_indptr=None,
+                         stream=None):
+    """Causal mixed-batch attention in which new token i of a request sees,
+    among its request's new tokens, itself and the earlier ones selected by
+    its mask row (for a draft tree numbered parents-first: its ancestors).
+
+    ``tree_mask``: contiguous int32 or uint32 CUDA tensor [nnz_qo, words], one
+    row per query row; bit t (word t // 32, bit t % 32) selects new token t.
+    Every request needs qo_len <= 32 * words.  Other arguments as
+    ``batch_attention``."""
+    lib = load_library()
+    _dev_bf16(q, "q"), _dev_bf16(kv_pages, "kv_pages")
+    for n, t in (("qo_indptr", qo_indptr), ("kv_indptr", kv_indptr), ("page_indices", page_indices),
+                 ("last_page_len", last_page_len)):
+        _dev_i32(t, n)
+    if not (isinstance(tree_mask, torch.Tensor) and tree_mask.is_cuda and tree_mask.dim() == 2
+            and tree_mask.element_size() == 4 and tree_mask.is_contiguous()
+            and not tree_mask.is_floating_point() and tree_mask.shape[0] == q.shape[0]):
+        raise TypeError("tree_mask must be a contiguous [nnz_qo, words] int32/uint32 CUDA tensor")
+    Hq, d = q.shape[1], q.shape[2]
+    dims = _dims(kv_pages, Hq)
+    if sm_scale is None:
+        sm_scale = 1.0 / float(d) ** 0.5
+    if host_indptr is None:
+        host_indptr = (qo_indptr, kv_indptr, last_page_len)
+    hq, hk, hl = (_host_i32(x) for x in host_indptr)
+    batch = len(hq) - 1
+    if out is None:
+        out = torch.empty_like(q)
+    _dev_bf16(out, "out")
+    if lse is not None and not (lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous()):
+        raise TypeError("lse must be a contiguous fp32 CUDA tensor")
+    if workspace is None:
+        st = ctypes.c_int32(0)
+        need = lib.daa_batch_attention_workspace_size(_ptr(hq), _ptr(hk), _ptr(hl), batch, dims,
+                                                      ctypes.byref(st))
+        _check(st.value, "batch_attention_tree")
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.daa_batch_attention_tree(_ptr(q), _ptr(kv_pages), _ptr(qo_indptr), _ptr(kv_indptr),
+                                        _ptr(page_indices), _ptr(last_page_len), _ptr(hq), _ptr(hk),
+                                        _ptr(hl), batch, _ptr(tree_mask), int(tree_mask.shape[1]),
+                                        float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                        ws_bytes, dims, _stream(stream)),
+           "batch_attention_tree")
+    return out
+
+
 def append_attention(k_new, v_new, q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len,
                      causal=True, sm_scale=None, out=None, lse=None, workspace=None,
                      host_indptr=None, stream=None):
@@ -329,8 +385,19 @@ class BatchAttention:
                                 host_indptr=(t.h_qo_indptr, t.h_kv_indptr, t.h_last_page_len),
                                 stream=stream)
 
-    def run(self, q, out=None, lse=None, stream=None):
+    def run(self, q, out=None, lse=None, stream=None, tree_mask=None):
+        """Attention over the batch; with ``tree_mask``, under draft-tree masks
+        (``batch_attention_tree``; the batch must be causal)."""
         t = self.t
+        if tree_mask is not None:
+            if not self.causal:
+                raise ValueError("a tree mask refines the causal rule")
+            return batch_attention_tree(q, self.kv_pages, t.qo_indptr, t.kv_indptr, t.page_indices,
+                                        t.last_page_len, tree_mask, self.sm_scale, out=out, lse=lse,
+                                        workspace=self.workspace,
+                                        host_indptr=(t.h_qo_indptr, t.h_kv_indptr,
+                                                     t.h_last_page_len),
+                                        stream=stream)
         return batch_attention(q, self.kv_pages, t.qo_indptr, t.kv_indptr, t.page_indices,
                                t.last_page_len, self.causal, self.sm_scale, out=out, lse=lse,
                                workspace=self.workspace,

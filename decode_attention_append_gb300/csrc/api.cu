@@ -178,6 +178,8 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
     a.lse_out = ls.lse_out;
     a.part_o = part_o;
     a.part_lse = part_lse;
+    a.tree_mask = ls.tree_mask;
+    a.mask_words = ls.mask_words;
     a.err = ls.err;
     if (a.n_tiles > 0) {
       const bool quads = plan_prefill_quads(dims);
@@ -297,11 +299,20 @@ daa_status attention_call(const void* k_new, const void* v_new, const void* q,
                           const int32_t* h_kv_indptr, const int32_t* h_last_page_len,
                           int32_t batch, int32_t causal, float sm_scale, void* out,
                           float* lse_out, void* workspace, size_t workspace_bytes,
-                          const daa_dims& dims, void* stream, bool fused) {
+                          const daa_dims& dims, void* stream, bool fused,
+                          const uint32_t* tree_mask = nullptr, int32_t mask_words = 0) {
   if (!(std::isfinite(sm_scale)) || !(sm_scale > 0.f)) return DAA_ERR_INVALID_ARG;
   HostPlan& pl = host_plan();
   daa_status st = make_plan(h_qo_indptr, h_kv_indptr, h_last_page_len, batch, dims, num_sms(), pl);
   if (st != DAA_OK) return st;
+  if (tree_mask) {
+    // the mask refines the causal rule; each request's new tokens fit its rows
+    if (!causal || mask_words < 1) return DAA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(tree_mask) & 3) != 0) return DAA_ERR_ALIGNMENT;
+    for (int r = 0; r < batch; ++r)
+      if ((int64_t)h_qo_indptr[r + 1] - h_qo_indptr[r] > 32 * (int64_t)mask_words)
+        return DAA_ERR_SHAPE;
+  }
   const PlanLayout& lay = pl.lay;
   if (lay.n_units == 0 && lay.n_tiles == 0) return DAA_OK;
   if (!q || !kv_pages || !qo_indptr || !kv_indptr || !page_indices || !last_page_len || !out)
@@ -342,6 +353,8 @@ daa_status attention_call(const void* k_new, const void* v_new, const void* q,
   ls.nnz_qo = nnz_qo;
   ls.out = out;
   ls.lse_out = lse_out;
+  ls.tree_mask = tree_mask;
+  ls.mask_words = tree_mask ? mask_words : 0;
   ls.scratch = ws;
   ls.err = device_error_word();
   ls.sms = num_sms();
@@ -375,6 +388,21 @@ daa_status daa_append_attention(const void* k_new, const void* v_new, const void
   return attention_call(k_new, v_new, q, kv_pages, qo_indptr, kv_indptr, page_indices,
                         last_page_len, h_qo_indptr, h_kv_indptr, h_last_page_len, batch, causal,
                         sm_scale, out, lse_out, workspace, workspace_bytes, dims, stream, true);
+}
+
+daa_status daa_batch_attention_tree(const void* q, const void* kv_pages,
+                                    const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                    const int32_t* page_indices, const int32_t* last_page_len,
+                                    const int32_t* h_qo_indptr, const int32_t* h_kv_indptr,
+                                    const int32_t* h_last_page_len, int32_t batch,
+                                    const uint32_t* tree_mask, int32_t mask_words, float sm_scale,
+                                    void* out, float* lse_out, void* workspace,
+                                    size_t workspace_bytes, daa_dims dims, void* stream) {
+  if (!tree_mask) return DAA_ERR_INVALID_ARG;
+  return attention_call(nullptr, nullptr, q, kv_pages, qo_indptr, kv_indptr, page_indices,
+                        last_page_len, h_qo_indptr, h_kv_indptr, h_last_page_len, batch, 1,
+                        sm_scale, out, lse_out, workspace, workspace_bytes, dims, stream, false,
+                        tree_mask, mask_words);
 }
 
 daa_status daa_device_error(int32_t* code, int32_t reset) {

@@ -82,6 +82,8 @@ struct PrefillArgs {
   float* lse_out;
   float* part_o;                // split items: [n_parts][Hq][d]
   float* part_lse;              // split items: [n_parts][Hq] (log2 domain)
+  const uint32_t* tree_mask;    // draft-tree mask rows [nnz_qo][mask_words], or null
+  int mask_words;
   int* err;
 };
 // Rows of packed (token, head) a prefill tile holds.
@@ -106,6 +108,8 @@ struct LaunchSet {
   int nnz_qo;
   void* out;
   float* lse_out;
+  const uint32_t* tree_mask;    // draft-tree mask rows, or null
+  int mask_words;
   void* scratch;
   int* err;
   int sms;

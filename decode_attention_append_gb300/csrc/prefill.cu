@@ -124,7 +124,7 @@ __device__ __forceinline__ bool ring_is_v(int i, int nq, int n) {
 __device__ __forceinline__ int ring_k_index(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int ring_v_index(int j, int n) { return j <= n - 2 ? 2 * j + 2 : 2 * n - 1; }
 
-template <class C>
+template <class C, bool TREE>
 __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
   using L = C;
   constexpr int D = C::D, KT = C::KT, PPT = C::PPT, RS = C::RS;
@@ -378,8 +378,13 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
     ro.hq = kvh * g + (row - tl * g);
     ro.write = row < q_ntok * g;
     ro.part = tile.part >= 0 ? tile.part + tl * tile.part_stride : -1;
-    tc_softmax_rows<D, KT>(a, tmem + lane_off, tmem + C::O_COL + q * D + lane_off, s_full, &o_done[q],
-                           q, nq == 1, n_kt, kt0, row_end, ro, [&](int b) {
+    TreeRow tr;
+    tr.bits = TREE && ro.write ? a.tree_mask + (int64_t)ro.q_row * a.mask_words : nullptr;
+    tr.words = a.mask_words;
+    tr.draft0 = tile.kv_len - tile.qo_len;
+    tr.tok = q_tok0 + tl;
+    tc_softmax_rows<D, KT, TREE>(a, tmem + lane_off, tmem + C::O_COL + q * D + lane_off, s_full, &o_done[q],
+                           q, nq == 1, n_kt, kt0, row_end, ro, tr, [&](int b) {
                              if (lane == 0) mbar_arrive(&p_full[b]);
                            });
   }
@@ -393,15 +398,15 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
 }
 
 // One entry per role, so profilers and traces tell the two apart.
-template <class C>
+template <class C, bool TREE>
 __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
-  tc_attention<C>(prm);
+  tc_attention<C, TREE>(prm);
 }
-template <class C>
+template <class C, bool TREE>
 __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 decode_tc_kernel(const __grid_constant__ PrefillParams prm) {
-  tc_attention<C>(prm);
+  tc_attention<C, TREE>(prm);
 }
 
 // --------------------------------------------------------------- host side
@@ -455,11 +460,17 @@ cudaError_t launch_tc(const PrefillArgs& a, const PrefillTile* tiles, int n_tile
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  auto kern = kDecode ? decode_tc_kernel<C> : prefill_tc_kernel<C>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC);
-  if (e != cudaSuccess) return e;
-  return launch_kernel(kern, dim3(n_tiles, a.Hkv), dim3(C::THREADS), C::ALLOC, stream, programmatic,
-                       prm);
+  auto go = [&](void (*kern)(PrefillParams)) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kern, dim3(n_tiles, a.Hkv), dim3(C::THREADS), C::ALLOC, stream,
+                         programmatic, prm);
+  };
+  // the draft-tree variant only when the call carries a mask
+  if constexpr (kDecode)
+    return a.tree_mask ? go(decode_tc_kernel<C, true>) : go(decode_tc_kernel<C, false>);
+  else
+    return a.tree_mask ? go(prefill_tc_kernel<C, true>) : go(prefill_tc_kernel<C, false>);
 }
 
 }  // namespace

@@ -146,6 +146,7 @@ __device__ __forceinline__ uint64_t desc_mnmajor_p(uint32_t addr) {
   return smem_desc_sw128(addr, PairCfg::KT * 128, 1024);
 }
 
+template <bool TREE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg::THREADS, 1)
 prefill_pair_kernel(const __grid_constant__ PairParams prm) {
   using C = PairCfg;
@@ -400,8 +401,13 @@ prefill_pair_kernel(const __grid_constant__ PairParams prm) {
     ro.hq = kvh * g + (row - tl * g);
     ro.write = row < q_ntok * g;
     ro.part = -1;
-    tc_softmax_rows<D, KT>(a, tmem + lane_off, tmem + C::O_COL + q * D + lane_off, s_full, &o_done[q],
-                           q, false, n_kt, kt0, row_end, ro, [&](int b) {
+    TreeRow tr;
+    tr.bits = TREE && ro.write ? a.tree_mask + (int64_t)ro.q_row * a.mask_words : nullptr;
+    tr.words = a.mask_words;
+    tr.draft0 = tile.kv_len - tile.qo_len;
+    tr.tok = q_tok0 + tl;
+    tc_softmax_rows<D, KT, TREE>(a, tmem + lane_off, tmem + C::O_COL + q * D + lane_off, s_full, &o_done[q],
+                           q, false, n_kt, kt0, row_end, ro, tr, [&](int b) {
                              if (lane == 0) {
                                if (rank == 0)
                                  mbar_arrive(&p_full[b]);
@@ -470,10 +476,12 @@ cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream, bool 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // the draft-tree variant only when the call carries a mask
+  auto kern = a.tree_mask ? prefill_pair_kernel<true> : prefill_pair_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        PairCfg::ALLOC);
   if (e != cudaSuccess) return e;
-  return launch_kernel(prefill_pair_kernel, dim3(2 * a.n_tiles, a.Hkv), dim3(PairCfg::THREADS),
+  return launch_kernel(kern, dim3(2 * a.n_tiles, a.Hkv), dim3(PairCfg::THREADS),
                        PairCfg::ALLOC, stream, programmatic, prm);
 }
 

@@ -26,16 +26,53 @@ struct SoftmaxRowOut {
   int part;      // partial slot (key split) or -1
 };
 
+// Draft-tree mask of one row ("Accelerating Sonar through speculation", EAGLE:
+// a tree of draft tokens is verified under a custom attention mask).  The
+// request's new tokens sit at keys draft0 + t; this row's token `tok` sees all
+// cached keys, itself, and each earlier new token t < tok whose bit t is set in
+// `bits` (word t / 32, bit t % 32).  bits == nullptr: no mask.
+struct TreeRow {
+  const uint32_t* bits;
+  int words;
+  int draft0;
+  int tok;
+};
+
+// Keys key0 .. key0 + 31 that the row's mask hides (bit b = key key0 + b):
+// earlier new tokens whose mask bit is clear.  Cached keys, the row's own key
+// and later keys are never hidden here (later keys fall past row_end).
+__device__ __forceinline__ uint32_t tree_hidden_word(const TreeRow& tr, int key0) {
+  const int rel0 = key0 - tr.draft0;  // new-token index of bit 0
+  const int lo_b = max(0, -rel0);                 // first bit inside [0, tok)
+  const int hi_b = min(32, tr.tok - rel0);        // one past the last
+  if (tr.bits == nullptr || hi_b <= lo_b) return 0u;
+  uint32_t m;
+  if (rel0 >= 0) {
+    const int q = rel0 >> 5;
+    const uint32_t w0 = q < tr.words ? __ldg(tr.bits + q) : 0u;
+    const uint32_t w1 = q + 1 < tr.words ? __ldg(tr.bits + q + 1) : 0u;
+    m = __funnelshift_r(w0, w1, rel0 & 31);
+  } else {
+    m = __ldg(tr.bits) << lo_b;  // lo_b = -rel0 in 1 .. 31
+  }
+  const uint32_t hi_mask = hi_b >= 32 ? 0xffffffffu : ((1u << hi_b) - 1u);
+  const uint32_t inwin = hi_mask & ~((1u << lo_b) - 1u);
+  return inwin & ~m;
+}
+
+// TREE: the kernel variant for draft-tree masks (tr describes the row's mask);
+// the plain variant carries no mask code at all.
 // tmem_s0: TMEM address (lane field = this warp's 32 lanes) of S buffer 0; S
 // buffer b sits at tmem_s0 + b * KT.  tmem_o: this warp's lanes of O.
 // dbuf: S alternates between buffers 0 and 1 per key tile (single Q tile);
 // otherwise buffer `sbuf` is used for every tile.
-template <int D, int KT, class ReleaseP>
+template <int D, int KT, bool TREE, class ReleaseP>
 __device__ __forceinline__ void tc_softmax_rows(const PrefillArgs& a, uint32_t tmem_s0,
                                                 uint32_t tmem_o, uint64_t* s_full,
                                                 uint64_t* o_done_q, int sbuf, bool dbuf,
                                                 int n_kt, int kt0, int row_end,
-                                                const SoftmaxRowOut& ro, ReleaseP&& release_p) {
+                                                const SoftmaxRowOut& ro, const TreeRow& tr,
+                                                ReleaseP&& release_p) {
   const float sc = a.sm_scale_log2;
   float m_run = -INFINITY, l_run = 0.f;
 
@@ -49,7 +86,17 @@ __device__ __forceinline__ void tc_softmax_rows(const PrefillArgs& a, uint32_t t
 #pragma unroll
     for (int c = 0; c < KT; c += 32) tmem_ld32f(tmem_s + c, s + c);
     tmem_wait_ld();
-    const int lim = row_end - (kt0 + j) * KT;  // keys [(kt0+j)*KT, .. + lim) are valid
+    const int kb = (kt0 + j) * KT;
+    const int lim = row_end - kb;  // keys [kb, kb + lim) are valid
+    // tree mask: only tiles that hold an earlier new token of some row
+    if (TREE && __any_sync(0xffffffffu, kb + KT > tr.draft0 && kb < tr.draft0 + tr.tok)) {
+#pragma unroll
+      for (int k = 0; k < KT / 32; ++k) {
+        const uint32_t hid = tree_hidden_word(tr, kb + 32 * k);
+#pragma unroll
+        for (int b = 0; b < 32; ++b) s[32 * k + b] = ((hid >> b) & 1u) ? -INFINITY : s[32 * k + b];
+      }
+    }
     if (!__all_sync(0xffffffffu, lim >= KT)) {
 #pragma unroll
       for (int c = 0; c < KT; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;

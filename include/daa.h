@@ -29,8 +29,10 @@
  *    kv_len_r = (npages_r - 1) * page_size + last_page_len[r]
  *    (kv_len_r = 0 when it owns no page).  1 <= last_page_len[r] <= page_size
  *    whenever npages_r > 0.  The caller allocates pages; the table already
- *    covers the post-append length.  Pages of different requests must not
- *    overlap.
+ *    covers the post-append length.  A page that receives appended tokens
+ *    belongs to one request alone; pages that hold only cached tokens may be
+ *    listed by several requests (a prefix-cache hit: "Chunked prefill",
+ *    #prefix-cache-interaction), which read them in place.
  *  - Query / new-token rows (CSR): request r owns rows qo_indptr[r] ..
  *    qo_indptr[r+1]) of q, k_new, v_new and out; qo_len_r <= kv_len_r.  The new
  *    token i of request r sits at absolute position kv_len_r - qo_len_r + i.
@@ -200,6 +202,46 @@ daa_status daa_append_attention(const void* k_new, const void* v_new, const void
                                 int32_t batch, int32_t causal, float sm_scale, void* out,
                                 float* lse_out, void* workspace, size_t workspace_bytes,
                                 daa_dims dims, void* stream);
+
+/*
+ * Mixed-batch paged attention under draft-tree masks, for verifying the draft
+ * tokens of speculative decoding ("Accelerating Sonar through speculation"
+ * (Perplexity), section EAGLE: a tree of draft tokens is checked by the target
+ * model in one pass under a custom attention mask; each draft token is scored
+ * against the accepted prefix and its own branch of the tree).
+ *
+ * Computes daa_batch_attention with causal = 1, except that new token i of a
+ * request sees, among the request's new tokens, only itself and the earlier
+ * ones its mask row selects.  With pos0 = kv_len - qo_len (the key of new token
+ * 0), token i's key set is
+ *   J = {j < pos0}  U  {pos0 + i}  U  {pos0 + t : t < i, bit t of its row set}.
+ * Mask rows: tree_mask is uint32 [nnz_qo][mask_words] on the device, one row
+ * per query row (the row layout of q); bit t of a row is word t / 32, bit
+ * t % 32 (t counts the request's new tokens from 0).  Bits t >= i are ignored:
+ * a token always sees itself and never a later new token, so a row of all
+ * earlier bits set is plain causal attention and every request of a mixed
+ * batch can be given that way.  For a draft tree whose nodes are numbered so
+ * that parents precede children, row i holds the bits of i's ancestors.
+ * Requests with qo_len = 1 are unaffected (their key set is the same).
+ *
+ *  tree_mask      device, uint32 [nnz_qo][mask_words], 4-byte aligned
+ *  mask_words     words per row; every request needs qo_len <= 32 * mask_words
+ *  other arguments as daa_batch_attention (no `causal`: the rule is causal),
+ *  with the same workspace size (daa_batch_attention_workspace_size).
+ * Errors: those of daa_batch_attention; DAA_ERR_INVALID_ARG for a NULL mask or
+ * mask_words < 1, DAA_ERR_SHAPE when a request has more than 32 * mask_words
+ * new tokens, DAA_ERR_ALIGNMENT for a misaligned mask.  Only tiles of keys
+ * that hold earlier new tokens of a row evaluate the mask; the cached prefix
+ * streams exactly as in daa_batch_attention.
+ */
+daa_status daa_batch_attention_tree(const void* q, const void* kv_pages,
+                                    const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                    const int32_t* page_indices, const int32_t* last_page_len,
+                                    const int32_t* h_qo_indptr, const int32_t* h_kv_indptr,
+                                    const int32_t* h_last_page_len, int32_t batch,
+                                    const uint32_t* tree_mask, int32_t mask_words, float sm_scale,
+                                    void* out, float* lse_out, void* workspace,
+                                    size_t workspace_bytes, daa_dims dims, void* stream);
 
 /* Size of the device scratch array behind daa_batch_attention_noalloc (48 MiB). */
 #define DAA_NOALLOC_SCRATCH_BYTES (48u * 1024u * 1024u)

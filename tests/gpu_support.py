@@ -28,7 +28,8 @@ def gpu_fill(wl, pool, device):
 
 def gpu_step(wl, pool, k, device, with_lse=True, fused=False):
     """Append step k's new K/V and run attention: (out bf16 cpu, lse fp32 cpu).
-    fused: one append_attention call instead of kv_append + batch_attention."""
+    fused: one append_attention call instead of kv_append + batch_attention.
+    A step with draft trees appends, then attends under its tree mask."""
     st = wl.step_table(k)
     q, kn, vn = wl.step_inputs(k)
     tab = daa.PageTable.from_host(st["qo_indptr"], st["kv_indptr"], st["page_indices"],
@@ -37,7 +38,12 @@ def gpu_step(wl, pool, k, device, with_lse=True, fused=False):
     qd = q.to(device)
     lse = torch.full((q.shape[0], wl.num_qo_heads), float("nan"), device=device) if with_lse else None
     out = torch.full_like(qd, float("nan"))
-    if fused:
+    if wl.has_tree(k):
+        mask = torch.from_numpy(wl.tree_mask(k).view(np.int32)).to(device)
+        if kn.shape[0]:
+            runner.append(kn.to(device), vn.to(device))
+        runner.run(qd, out=out, lse=lse, tree_mask=mask)
+    elif fused:
         runner.step(kn.to(device), vn.to(device), qd, out=out, lse=lse)
     else:
         if kn.shape[0]:

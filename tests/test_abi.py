@@ -165,3 +165,23 @@ def test_oracle_and_library_share_no_code():
         if f.endswith((".py", ".c")):
             text = open(os.path.join(ROOT, "oracle", f)).read()
             assert "decode_attention_append_gb300" not in text and "daa.h" not in text, f
+
+
+def test_tree_attention_rejects_before_any_launch(lib):
+    """daa_batch_attention_tree: a mask is required, must be 4-byte aligned,
+    needs at least one word per row and enough words for every request's new
+    tokens (checked against the host mirror of qo_indptr)."""
+    d = _dims()
+    qo = np.asarray([0, 40], np.int32)     # one request of 40 new tokens
+    kv = np.asarray([0, 3], np.int32)
+    last = np.asarray([16], np.int32)
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+    dev = lambda x: ctypes.c_void_p(x)  # noqa: E731  (never dereferenced: rejected first)
+    call = lambda mask, words: lib.daa_batch_attention_tree(  # noqa: E731
+        dev(0x10000), dev(0x20000), dev(0x30000), dev(0x40000), dev(0x50000), dev(0x60000),
+        p(qo), p(kv), p(last), 1, mask, words, 0.125, dev(0x70000), None, dev(0x100000), 1 << 20,
+        d, None)
+    assert call(None, 2) == -1
+    assert call(dev(0x8000), 0) == -1
+    assert call(dev(0x8002), 2) == -7
+    assert call(dev(0x8000), 1) == -2      # 40 tokens need 2 words

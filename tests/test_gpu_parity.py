@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from synth import (SENTINEL_BF16, make_prompt_workload, make_random_workload,
-                   make_shared_prefix_workload, make_workload)
+                   make_shared_prefix_workload, make_tree_workload, make_workload, tree_mask_rows)
 from support import err_stats, oracle_pool, oracle_step
 
 pytestmark = pytest.mark.gpu
@@ -237,6 +237,60 @@ def test_shared_prefix_pages(dev, case, fused):
     seed, Hq, Hkv, d, sp, prompts, decodes = case
     wl = make_shared_prefix_workload(f"shared_{seed}", Hq, Hkv, d, 16, seed, sp, prompts, decodes)
     _run_both(wl, dev, fused=fused)
+
+
+TREES = [
+    # (seed, Hq, Hkv, d, trees (nodes, cached, roots), decode kv_lens, prompts (qo, kv))
+    # g = 1: every tree is a key-split verify item; CUDA-core decodes beside them
+    (301, 8, 8, 128, [(16, 300, 1), (9, 1000, 2), (5, 40, 1)], [100, 700], []),
+    # g = 4: a 16-node tree as a verify item, larger trees on the pair prefill
+    # kernel, a plain chunk in the same masked batch (10 mask words per row)
+    (302, 32, 8, 128, [(64, 1500, 1), (40, 200, 3), (16, 5000, 1), (100, 30, 1)], [900], [(300, 1200)]),
+    # g = 8, head_dim 64: verify item and the single-CTA prefill kernel
+    (303, 16, 2, 64, [(48, 700, 1), (12, 90, 1)], [64], []),
+    # g = 12: 10 tokens per Q tile; a 10-node verify item, a 33-node tree
+    (304, 12, 1, 128, [(10, 3000, 1), (33, 4000, 2)], [2000], []),
+]
+
+
+@pytest.mark.parametrize("case", TREES, ids=lambda c: f"seed{c[0]}")
+def test_tree_verify(dev, case):
+    """Draft-tree verification ("Accelerating Sonar through speculation",
+    EAGLE): every new token attends to the cached prefix and its own branch of
+    the tree, through daa_batch_attention_tree, against the oracle."""
+    seed, Hq, Hkv, d, trees, decodes, prompts = case
+    wl = make_tree_workload(f"tree_{seed}", Hq, Hkv, d, 16, seed, trees, decodes, prompts)
+    _run_both(wl, dev)
+
+
+def test_tree_verify_workload(dev):
+    _run_both(make_workload("tree_verify"), dev)
+
+
+def test_chain_mask_matches_unmasked_bitwise(dev):
+    """A mask row selecting every earlier new token is the causal rule: the
+    tree variant of the kernels returns the plain call's bits exactly."""
+    import decode_attention_append_gb300 as daa
+    from gpu_support import gpu_fill, new_pool
+    wl = make_random_workload(305, 32, 8, 128, 16, [(200, 900), (12, 400), (1, 77), (64, 64), (7, 20)],
+                              extra_pages=5)
+    pool = new_pool(wl, dev)
+    gpu_fill(wl, pool, dev)
+    st = wl.step_table(0)
+    q, kn, vn = wl.step_inputs(0)
+    tab = daa.PageTable.from_host(st["qo_indptr"], st["kv_indptr"], st["page_indices"],
+                                  st["last_page_len"], dev)
+    runner = daa.BatchAttention(tab, wl.num_qo_heads, pool, sm_scale=wl.sm_scale)
+    runner.append(kn.to(dev), vn.to(dev))
+    qd = q.to(dev)
+    mask = np.concatenate([tree_mask_rows(np.arange(r.qo_len) - 1, 7) for r in wl.steps[0].requests])
+    la = torch.empty(q.shape[0], wl.num_qo_heads, device=dev)
+    lb = torch.empty_like(la)
+    oa = runner.run(qd, lse=la)
+    ob = runner.run(qd, lse=lb, tree_mask=torch.from_numpy(mask.view(np.int32)).to(dev))
+    torch.cuda.synchronize()
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(la, lb)
 
 
 def test_no_device_error_recorded(dev):
