@@ -62,7 +62,10 @@ def step_accounting(wl, k=0):
     nnz_new = 0
     seen_prefix = set()
     verify_max = min(VERIFY_MAX_TOKENS, 128 // wl.group_size)
-    ver_flops = ver_bytes = 0
+    # requests that fit two 128-row Q tiles run in their own kernel where
+    # prefill runs on CTA pairs (head_dim 128)
+    short_max = 2 * (128 // wl.group_size) if wl.head_dim == 128 else verify_max
+    ver_flops = ver_bytes = sh_flops = sh_bytes = 0
     for r in wl.steps[k].requests:
         nnz_new += r.qo_len
         sq = wl.seqs[r.seq]
@@ -93,21 +96,35 @@ def step_accounting(wl, k=0):
             if r.qo_len <= verify_max:  # key-split items of the tensor-core decode kernel
                 ver_flops += fl
                 ver_bytes += by
+            elif r.qo_len <= short_max:
+                sh_flops += fl
+                sh_bytes += by
     app_bytes = nnz_new * Hkv * d * 2 * 2 * 2
     tc_decode = wl.group_size >= TC_DECODE_MIN_GROUP
     return dict(decode_bytes=dec_bytes, append_bytes=app_bytes, prefill_flops=pre_flops,
                 prefill_bytes=pre_bytes, nnz_new=nnz_new,
                 # work per kernel
-                tc_flops=pre_flops - ver_flops, tc_bytes=pre_bytes - ver_bytes,
+                tc_flops=pre_flops - ver_flops - sh_flops, tc_bytes=pre_bytes - ver_bytes - sh_bytes,
+                short_flops=sh_flops, short_bytes=sh_bytes,
                 tc_decode_bytes=(dec_bytes if tc_decode else 0) + ver_bytes,
                 cuda_decode_bytes=0 if tc_decode else dec_bytes)
 
 
 def kernel_source_hash(name):
-    """Hash of a kernel's source file and the device headers it shares."""
+    """Hash of a kernel's source file and of the device headers (.cuh) it
+    includes, directly or through another of them, in that order."""
+    import re
     csrc = os.path.join(ROOT, "decode_attention_append_gb300", "csrc")
+    files, todo = [], [name]
+    while todo:
+        f = todo.pop(0)
+        if f in files:
+            continue
+        files.append(f)
+        with open(os.path.join(csrc, f)) as fh:
+            todo += re.findall(r'#include "([\w.]+\.cuh)"', fh.read())
     h = hashlib.sha256()
-    for f in (name, "ptx.cuh", "softmax_tc.cuh"):
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -588,9 +605,10 @@ def main():
         mean_ms = float(np.mean(per_kernel[dom]))
         n_launch = len(per_kernel[dom]) / args.steps
         t = mean_ms * 1e-3
-        if dom == "prefill_tc":
-            # the tensor-core prefill kernel: bound by whichever ideal time is larger
-            fl, by = acc["tc_flops"] / n_launch, acc["tc_bytes"] / n_launch
+        if dom in ("prefill_tc", "short_tc"):
+            # the tensor-core prefill kernels: bound by whichever ideal time is larger
+            key = "tc" if dom == "prefill_tc" else "short"
+            fl, by = acc[key + "_flops"] / n_launch, acc[key + "_bytes"] / n_launch
             t_tensor, t_hbm = fl / (bf16 * 1e12), by / (hbm * 1e9)
             if t_tensor >= t_hbm:
                 # the kernel runs back to back for seconds (clock window + timed
@@ -602,7 +620,7 @@ def main():
                 roof = {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm, "unit": "GB/s",
                         "peak_source": f"{peak_src} HBM copy"}
             roof["ideal_fraction"] = (t_tensor + t_hbm) / t
-            kfile = "prefill_pair.cu" if wl.head_dim == 128 else "prefill.cu"
+            kfile = "prefill_pair.cu" if wl.head_dim == 128 and dom == "prefill_tc" else "prefill.cu"
         else:
             kb = {"decode_splitkv": acc["cuda_decode_bytes"], "decode_tc": acc["tc_decode_bytes"],
                   "kv_append": acc["append_bytes"]}.get(dom, 0)

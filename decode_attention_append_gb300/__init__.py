@@ -41,7 +41,8 @@ _lock = threading.Lock()
 DAA_OK = 0
 STATUS = {0: "ok", -1: "invalid argument", -2: "shape", -3: "page range", -4: "unsupported",
           -5: "CUDA error", -6: "workspace", -7: "alignment"}
-KERNEL_NAMES = {1: "kv_append", 2: "decode_splitkv", 3: "softmax_merge", 4: "prefill_tc", 5: "decode_tc"}
+KERNEL_NAMES = {1: "kv_append", 2: "decode_splitkv", 3: "softmax_merge", 4: "prefill_tc", 5: "decode_tc",
+                6: "short_tc"}
 
 
 class DaaError(RuntimeError):

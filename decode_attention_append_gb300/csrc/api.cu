@@ -163,8 +163,10 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
     a.pool = static_cast<const uint16_t*>(ls.kv_pages);
     a.page_indices = ls.page_indices;
     a.tiles = reinterpret_cast<const PrefillTile*>(ws + lay.off_tiles);
-    a.n_tiles = lay.n_tiles - lay.n_dec_tiles;
-    a.dec_tiles = a.tiles + a.n_tiles;
+    a.n_tiles = lay.n_tiles - lay.n_dec_tiles - lay.n_short_tiles;
+    a.short_tiles = a.tiles + a.n_tiles;
+    a.n_short_tiles = lay.n_short_tiles;
+    a.dec_tiles = a.short_tiles + a.n_short_tiles;
     a.n_dec_tiles = lay.n_dec_tiles;
     a.Hq = dims.num_qo_heads;
     a.Hkv = dims.num_kv_heads;
@@ -184,7 +186,15 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
     if (a.n_tiles > 0) {
       const bool quads = plan_prefill_quads(dims);
       if (run(kKernelPrefill, [&] {
-            return quads ? launch_prefill_pair(a, s, programmatic) : launch_prefill(a, s, programmatic);
+            return quads ? launch_prefill_pair(a, s, programmatic)
+                         : launch_prefill(a, a.tiles, a.n_tiles, s, programmatic);
+          }) != cudaSuccess)
+        return DAA_ERR_CUDA;
+      programmatic = !(trace && tracing());
+    }
+    if (a.n_short_tiles > 0) {
+      if (run(kKernelShort, [&] {
+            return launch_prefill(a, a.short_tiles, a.n_short_tiles, s, programmatic);
           }) != cudaSuccess)
         return DAA_ERR_CUDA;
       programmatic = !(trace && tracing());

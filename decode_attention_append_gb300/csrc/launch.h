@@ -71,7 +71,9 @@ struct PrefillArgs {
   const int32_t* page_indices;
   const PrefillTile* tiles;     // device: prefill items
   int n_tiles;
-  const PrefillTile* dec_tiles; // device: one-token (decode) items
+  const PrefillTile* short_tiles;  // device: short multi-token items (single-CTA kernel)
+  int n_short_tiles;
+  const PrefillTile* dec_tiles; // device: decode and verify items
   int n_dec_tiles;
   int Hq, Hkv, group, head_dim;
   int64_t num_pages;
@@ -88,9 +90,12 @@ struct PrefillArgs {
 };
 // Rows of packed (token, head) a prefill tile holds.
 constexpr int kPrefillTileRows = 128;
-// Tensor-core kernel over the prefill items (pairs of 128-row Q tiles) and
-// over the one-token decode items (a smaller instantiation, two CTAs per SM).
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, bool programmatic);
+// Single-CTA tensor-core kernel over `tiles` (pairs of 128-row Q tiles: the
+// prefill items for head_dim 64, the short items for head_dim 128), and the
+// decode instantiation over the decode / verify items (one Q tile, two CTAs
+// per SM).
+cudaError_t launch_prefill(const PrefillArgs& a, const PrefillTile* tiles, int n_tiles,
+                           cudaStream_t stream, bool programmatic);
 // head_dim 128: prefill items of four Q tiles on clusters of two CTAs
 // (tcgen05 cta_group::2); grid (2 * n_tiles, Hkv).
 cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream, bool programmatic);

@@ -48,7 +48,8 @@ struct PrefillTile {
   int32_t key_hi;     // one past the last key
   int32_t part;       // partial slot, or -1: write out / lse_out directly
   int32_t work;       // planner's sort key (keys read)
-  int32_t part_stride;  // key-split multi-token item: token t's partial slot is part + t * part_stride
+  int32_t part_stride;  // key-split multi-token item: token t (counted from tok0, across
+                        // both tiles) writes its partial to slot part + t * part_stride
 };
 
 static_assert(sizeof(DecodeUnit) == 32, "DecodeUnit layout");
@@ -62,6 +63,7 @@ enum KernelId : int32_t {
   kKernelMerge = 3,
   kKernelPrefill = 4,
   kKernelTcDecode = 5,
+  kKernelShort = 6,   // short multi-token items on the single-CTA kernel (head_dim 128)
 };
 
 }  // namespace daa

@@ -12,7 +12,11 @@
 //    at memory rate while the CUDA cores only run the softmax;
 //  * other decode requests go to the CUDA-core split-KV kernel as page-aligned
 //    key splits;
-//  * prefill requests (qo_len > 1) become items of 128-row tiles of packed
+//  * short multi-token requests whose rows fit two 128-row Q tiles (larger
+//    verify steps, e.g. draft trees) become items of the single-CTA
+//    tensor-core kernel, both tiles sharing every K/V tile; their keys are cut
+//    only when one request holds more keys than an SM's share of the batch;
+//  * longer prefill requests become items of 128-row tiles of packed
 //    (token, query head) rows for the tensor-core kernels -- four tiles on a
 //    pair of SMs for head_dim 128, two tiles on one SM otherwise -- longest
 //    key range first.
@@ -58,9 +62,12 @@ inline daa_status plan_check_dims(const daa_dims& d) {
   return DAA_OK;
 }
 
-// Offsets of the workspace sections (bytes).
+// Offsets of the workspace sections (bytes).  Tensor-core items are stored
+// as three consecutive groups, each launched as its own kernel: prefill items,
+// short items (single-CTA kernel, head_dim 128 only; for head_dim 64 they join
+// the prefill group, which runs the same kernel), decode / verify items.
 struct PlanLayout {
-  int n_units = 0, n_merges = 0, n_tiles = 0, n_dec_tiles = 0, n_parts = 0;
+  int n_units = 0, n_merges = 0, n_tiles = 0, n_dec_tiles = 0, n_short_tiles = 0, n_parts = 0;
   size_t off_units = 0, off_merges = 0, off_tiles = 0, plan_bytes = 0;
   size_t off_part_o = 0, off_part_lse = 0, total = 0;
 };
@@ -85,7 +92,10 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
   const bool tc_decode = g >= kTcDecodeMinGroup;
   const int verify_max = plan_verify_max(g);
 
-  int64_t dec_pages = 0;
+  const int tpt = kPrefillTileRows / g;  // tokens per 128-row Q tile
+  const int short_max = 2 * tpt;
+  const bool quads = plan_prefill_quads(d);
+  int64_t dec_pages = 0, short_pages = 0;
   for (int r = 0; r < batch; ++r) {
     const int64_t nq = (int64_t)qo[r + 1] - qo[r];
     const int64_t np = (int64_t)kv[r + 1] - kv[r];
@@ -94,6 +104,7 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
     const int64_t kv_len = np > 0 ? (np - 1) * P + last[r] : 0;
     if (nq > kv_len || kv_len > INT32_MAX / 2) return DAA_ERR_SHAPE;
     if (nq >= 1 && nq <= verify_max) dec_pages += np;
+    else if (nq > verify_max && nq <= short_max) short_pages += np;
   }
   const int64_t page_heads = dec_pages * d.num_kv_heads;
 
@@ -106,12 +117,19 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
   int64_t split_cc = (page_heads + (int64_t)sms * 40 - 1) / ((int64_t)sms * 40);
   split_cc = std::max<int64_t>(16, std::min<int64_t>(1024, split_cc));
 
-  // decode (qo_len 1) and verify (qo_len 2 .. verify_max) requests
+  // short items: one item's keys at most an SM's share of the short requests'
+  // K/V (so the longest item bounds the pass), whole 128-key tiles
+  int64_t split_short = (short_pages * d.num_kv_heads + sms - 1) / sms;
+  split_short = std::max<int64_t>(32, (split_short + 7) / 8 * 8);
+
+  // decode (qo_len 1), verify (qo_len 2 .. verify_max) and short
+  // (verify_max < qo_len <= short_max) requests: key-split items
   for (int r = 0; r < batch; ++r) {
     const int nq = qo[r + 1] - qo[r];
-    if (nq < 1 || nq > verify_max) continue;
+    if (nq < 1 || nq > short_max) continue;
+    const bool is_short = nq > verify_max;
     const bool on_tc = tc_decode || nq > 1;
-    const int64_t split = on_tc ? split_tc : split_cc;
+    const int64_t split = is_short ? split_short : on_tc ? split_tc : split_cc;
     const int np = kv[r + 1] - kv[r];
     const int kv_len = (np - 1) * P + last[r];
     // splits cut the keys token 0 can see, [0, kv_len - nq], so every split
@@ -138,13 +156,13 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
         t.kv_len = kv_len;
         t.page_base = kv[r];
         t.tok0 = 0;
-        t.ntok = nq;
-        t.ntok1 = 0;
+        t.ntok = std::min(nq, tpt);   // short items: two Q tiles
+        t.ntok1 = nq - t.ntok;
         t.key_lo = lo;
         t.key_hi = hi;
         t.part = part0 >= 0 ? part0 + s : -1;
         t.part_stride = nsplit;
-        t.work = hi - lo;
+        t.work = (hi - lo) * (t.ntok1 > 0 ? 2 : 1);
         if (!tiles.push_back(t)) return DAA_ERR_WORKSPACE;
       } else {
         DecodeUnit u{};
@@ -167,11 +185,9 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
   // prefill: 128-row Q tiles of packed (token, query head) rows (tpt tokens
   // each).  head_dim 128: items of four tiles for a CTA pair (ntok = the item's
   // tokens); otherwise pairs of tiles for one CTA (ntok, ntok1 per tile).
-  const int tpt = kPrefillTileRows / g;
-  const bool quads = plan_prefill_quads(d);
   for (int r = 0; r < batch; ++r) {
     const int nq = qo[r + 1] - qo[r];
-    if (nq <= verify_max) continue;
+    if (nq <= short_max) continue;
     const int np = kv[r + 1] - kv[r];
     const int kv_len = (np - 1) * P + last[r];
     for (int t0 = 0; t0 < nq; t0 += (quads ? 4 : 2) * tpt) {
@@ -200,16 +216,25 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
       if (!tiles.push_back(t)) return DAA_ERR_WORKSPACE;
     }
   }
-  // tensor-core items: prefill items, then decode / verify items (each group
-  // launches its own kernel), most work first
-  std::sort(tiles.data(), tiles.data() + tiles.size(), [verify_max](const PrefillTile& x, const PrefillTile& y) {
-    const bool dx = x.qo_len <= verify_max, dy = y.qo_len <= verify_max;
-    if (dx != dy) return dy;
+  // tensor-core items in launch groups -- prefill items, short items (their
+  // own group only where prefill runs on CTA pairs), decode / verify items --
+  // most work first within each group
+  auto group = [=](const PrefillTile& t) {
+    if (t.qo_len <= verify_max) return 2;
+    return quads && t.qo_len <= short_max ? 1 : 0;
+  };
+  std::sort(tiles.data(), tiles.data() + tiles.size(), [&](const PrefillTile& x, const PrefillTile& y) {
+    const int gx = group(x), gy = group(y);
+    if (gx != gy) return gx < gy;
     if (x.work != y.work) return x.work > y.work;
     if (x.q_row0 != y.q_row0) return x.q_row0 < y.q_row0;
     return x.tok0 != y.tok0 ? x.tok0 < y.tok0 : x.key_lo < y.key_lo;
   });
-  for (size_t i = 0; i < tiles.size(); ++i) lay.n_dec_tiles += tiles.data()[i].qo_len <= verify_max ? 1 : 0;
+  for (size_t i = 0; i < tiles.size(); ++i) {
+    const int gi = group(tiles.data()[i]);
+    lay.n_dec_tiles += gi == 2 ? 1 : 0;
+    lay.n_short_tiles += gi == 1 ? 1 : 0;
+  }
 
   lay.n_units = (int)units.size();
   lay.n_merges = (int)merges.size();

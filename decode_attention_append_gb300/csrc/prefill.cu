@@ -377,7 +377,7 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
     ro.q_row = tile.q_row0 + q_tok0 + tl;
     ro.hq = kvh * g + (row - tl * g);
     ro.write = row < q_ntok * g;
-    ro.part = tile.part >= 0 ? tile.part + tl * tile.part_stride : -1;
+    ro.part = tile.part >= 0 ? tile.part + (q_tok0 - tile.tok0 + tl) * tile.part_stride : -1;
     TreeRow tr;
     tr.bits = TREE && ro.write ? a.tree_mask + (int64_t)ro.q_row * a.mask_words : nullptr;
     tr.words = a.mask_words;
@@ -475,9 +475,10 @@ cudaError_t launch_tc(const PrefillArgs& a, const PrefillTile* tiles, int n_tile
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, bool pr) {
-  return a.head_dim == 128 ? launch_tc<CfgPrefill128, false>(a, a.tiles, a.n_tiles, stream, pr)
-                           : launch_tc<CfgPrefill64, false>(a, a.tiles, a.n_tiles, stream, pr);
+cudaError_t launch_prefill(const PrefillArgs& a, const PrefillTile* tiles, int n_tiles,
+                           cudaStream_t stream, bool pr) {
+  return a.head_dim == 128 ? launch_tc<CfgPrefill128, false>(a, tiles, n_tiles, stream, pr)
+                           : launch_tc<CfgPrefill64, false>(a, tiles, n_tiles, stream, pr);
 }
 
 cudaError_t launch_tc_decode(const PrefillArgs& a, cudaStream_t stream, bool pr) {

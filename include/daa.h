@@ -141,8 +141,10 @@ size_t daa_batch_attention_workspace_size(const int32_t* h_qo_indptr, const int3
  * split-KV decode kernel (CUDA cores when a kv head serves fewer than 4 query
  * heads, tensor cores otherwise); requests with 2 <= qo_len <= min(16, 128 / g)
  * (g = Hq / Hkv; e.g. speculative-decoding verify steps) run as key-split
- * items of the tensor-core decode kernel; longer requests run the tensor-core
- * prefill kernel.  Split requests are combined by the softmax_merge pass, one
+ * items of the tensor-core decode kernel; requests up to 256 / g tokens (two
+ * 128-row tiles of packed query rows) run as items of the single-CTA
+ * tensor-core kernel, key-split when long; longer requests run the
+ * tensor-core prefill kernel.  Split requests are combined by the softmax_merge pass, one
  * merge per token.  Rows of requests with qo_len = 0 do not exist; nothing is
  * written.
  *
@@ -302,7 +304,9 @@ daa_status daa_device_error(int32_t* code, int32_t reset);
  * events and copies out up to `max_records` (kernel id, milliseconds) pairs in
  * launch order, returning how many were written, then clears the record.
  * Kernel ids: 1 kv_append, 2 decode split-KV (CUDA cores), 3 softmax_merge,
- * 4 tensor-core prefill, 5 tensor-core decode split-KV.
+ * 4 tensor-core prefill, 5 tensor-core decode split-KV (decode and verify
+ * items), 6 tensor-core short multi-token items (head_dim 128: requests whose
+ * rows fit two 128-row Q tiles).
  */
 daa_status daa_trace_enable(int32_t capacity);
 daa_status daa_trace_disable(void);

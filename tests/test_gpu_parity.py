@@ -139,6 +139,28 @@ def test_verify_batches(dev, case):
     _run_both(wl, dev)
 
 
+SHORT = [
+    # (seed, Hq, Hkv, d, [(qo, kv), ...], causal): requests whose rows fit two
+    # 128-row Q tiles (verify cap < qo <= 256 / g) run on the single-CTA kernel,
+    # key-split when long; qo = 256 / g + 1 is the first pair-prefill request
+    (121, 8, 8, 128, [(17, 40000), (200, 3000), (256, 256), (257, 900), (1, 5000), (150, 50000)], True),
+    (122, 32, 8, 128, [(17, 12000), (33, 33), (64, 7000), (65, 7000), (40, 300)], True),
+    (123, 12, 1, 128, [(11, 30000), (20, 20), (21, 5000), (1, 3000)], True),
+    (124, 8, 1, 128, [(100, 5000), (17, 17), (32, 9000)], False),
+    (125, 16, 4, 64, [(40, 9000), (84, 84), (64, 64)], True),
+]
+
+
+@pytest.mark.parametrize("case", SHORT, ids=lambda c: f"seed{c[0]}")
+def test_short_requests(dev, case):
+    """Short multi-token requests: one or two Q tiles on the single-CTA kernel,
+    key splits merged per token, against the oracle."""
+    seed, Hq, Hkv, d, reqs, causal = case
+    wl = make_random_workload(seed, Hq, Hkv, d, 16, reqs, extra_pages=7)
+    wl.causal = causal
+    _run_both(wl, dev)
+
+
 def test_decode_kv_len_one_returns_v(dev):
     from gpu_support import gpu_fill, gpu_step, new_pool
     wl = make_random_workload(111, 8, 2, 128, 16, [(1, 1), (1, 1)])
