@@ -108,13 +108,16 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
   }
   const int64_t page_heads = dec_pages * d.num_kv_heads;
 
-  // split sizes (pages).  CUDA-core splits: enough CTAs that the longest split
-  // is a small fraction of the pass.  Tensor-core splits: whole 128-key tiles,
-  // about four items per SM.
+  // split sizes (pages).  CUDA-core splits: about twenty per SM (ten per CTA
+  // slot), so the longest split is a small fraction of the pass while the
+  // split-KV partials stay few.  Tensor-core splits: whole 128-key tiles, about
+  // four items per SM.  Both targets were measured on GB300 (MHA decode: 20
+  // per SM 7% faster than 40 or 80; tensor-core items: 4 per SM within a few
+  // percent of the best for decode-heavy, mixed and shared-prefix batches).
   int64_t split_tc = (page_heads + (int64_t)sms * 4 - 1) / ((int64_t)sms * 4);
   split_tc = (split_tc + 7) / 8 * 8;
   split_tc = std::max<int64_t>(32, std::min<int64_t>(2048, split_tc));
-  int64_t split_cc = (page_heads + (int64_t)sms * 40 - 1) / ((int64_t)sms * 40);
+  int64_t split_cc = (page_heads + (int64_t)sms * 20 - 1) / ((int64_t)sms * 20);
   split_cc = std::max<int64_t>(16, std::min<int64_t>(1024, split_cc));
 
   // short items: one item's keys at most an SM's share of the short requests'

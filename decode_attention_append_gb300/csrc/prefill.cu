@@ -212,15 +212,20 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
                       kvh * g, tile.q_row0 + tile.tok0 + q * tile.ntok, q_full);
     }
     int64_t pid = load_ids(0);
-    // items whose keys reach the rows appended in this step (the request's
-    // last qo_len keys: every prefill item, the split(s) holding them for a
-    // decode or verify request) wait for the kernel launched before this one
-    if (tile.key_hi > tile.kv_len - tile.qo_len) grid_dep_wait();
+    // the request's last qo_len keys are the rows appended in this step: the
+    // first ring item that reaches them waits for the kernel launched before
+    // this one (tiles of cached keys stream while that kernel still runs)
+    const int first_new = tile.kv_len - tile.qo_len;
+    bool dep_waited = false;
     for (int i = 0; i < 2 * n_kt; ++i) {
       const int64_t pid_next = load_ids(i + 1);
       const int st = i % RS;
       const bool is_v = ring_is_v(i, nq, n_kt);
       const int pg0 = (kt0 + ring_tile(i, nq, n_kt)) * PPT;
+      if (!dep_waited && (pg0 / PPT + 1) * KT > first_new) {
+        grid_dep_wait();
+        dep_waited = true;
+      }
       const int np = min(PPT, npages_req - pg0);
       uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
       if (lane == 0) {

@@ -240,11 +240,19 @@ prefill_pair_kernel(const __grid_constant__ PairParams prm) {
       }
     }
     int64_t id0 = load_ids(0), id1 = load_ids(1), id2 = load_ids(2), id3 = load_ids(3);
-    if (tile.key_hi > tile.kv_len - tile.qo_len) grid_dep_wait();  // reads rows appended in this step
+    // the request's last qo_len keys are the rows appended in this step: the
+    // first key tile that reaches them waits for the kernel launched before
+    // this one (tiles of cached keys stream while that kernel still runs)
+    const int first_new = tile.kv_len - tile.qo_len;
+    bool dep_waited = false;
     for (int i = 0; i < 2 * n_kt; ++i) {
       const int st = i % RS;
       const bool is_v = i & 1;
       const int pg0 = (kt0 + (i >> 1)) * PPT;
+      if (!dep_waited && (kt0 + (i >> 1) + 1) * KT > first_new) {
+        grid_dep_wait();
+        dep_waited = true;
+      }
       const int np = min(PPT, npages_req - pg0);
       const int kp = max(0, min(4, np - 4 * (int)rank));  // pages of this CTA's K half
       uint8_t* buf = smem + C::OFF_RING + st * C::H_BYTES;
