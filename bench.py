@@ -311,6 +311,21 @@ class GpuStep:
         return h2d, d2h
 
 
+def max_over_ranks(values, dist, device):
+    """Element-wise MAX of per-rank timings over all ranks (every rank gets it):
+    the job is as slow as its slowest replica."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_rate(units_per_step, steps, world, ms):
+    """Whole-job throughput (G units/s): every one of `world` replicas processed
+    `units_per_step` per step for `steps` steps within `ms` milliseconds."""
+    return units_per_step * steps * world / (ms * 1e-3) / 1e9
+
+
 def soak(fn, seconds):
     """Run fn back to back for about `seconds` of wall time (untimed)."""
     t0 = time.perf_counter()
@@ -584,10 +599,7 @@ def main():
         barrier()
     err = daa.device_error(reset=True)
 
-    t = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms, ms_e2e = float(t[0]), float(t[1])
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e], dist, dev)
     if rank != 0:
         dist.destroy_process_group()
         return 0
@@ -634,12 +646,12 @@ def main():
         roof["traffic"] = measured_traffic(args.workload, kfile)
         roof["share"] = {k: round(v / sum(tot.values()), 4) for k, v in tot.items()}
 
-    value = algo_bytes * args.steps * world / (ms * 1e-3) / 1e9
+    value = job_rate(algo_bytes, args.steps, world, ms)
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config,
-            "e2e": {"value": algo_bytes * args.steps * world / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
+            "e2e": {"value": job_rate(algo_bytes, args.steps, world, ms_e2e), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": ms_e2e / args.steps},
             "gpu_launches": int(round(launches * args.steps)),
