@@ -90,6 +90,8 @@ def load_library():
         lib.daa_batch_attention_noalloc.restype = i32
         lib.daa_batch_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32,
                                                     vp, vp, _Dims, vp]
+        lib.daa_selftest_bounded_wait.restype = i32
+        lib.daa_selftest_bounded_wait.argtypes = [ctypes.POINTER(i32)]
         lib.daa_device_error.restype = i32
         lib.daa_device_error.argtypes = [ctypes.POINTER(i32), i32]
         lib.daa_trace_enable.restype = i32
@@ -412,6 +414,15 @@ def device_error(reset: bool = True) -> int:
     code = ctypes.c_int32(0)
     _check(lib.daa_device_error(ctypes.byref(code), int(reset)), "device_error")
     return int(code.value)
+
+
+def selftest_bounded_wait() -> bool:
+    """Run the library's bounded wait on a barrier nothing completes; True when
+    it gave up by its time limit (the device error word then holds 2)."""
+    lib = load_library()
+    flag = ctypes.c_int32(-1)
+    _check(lib.daa_selftest_bounded_wait(ctypes.byref(flag)), "selftest_bounded_wait")
+    return flag.value == 1
 
 
 def trace_enable(capacity: int = 4096) -> None:

@@ -19,10 +19,23 @@
 #include "../../include/daa.h"
 #include "launch.h"
 #include "planner.h"
+#include "ptx.cuh"
 
 namespace daa {
 
 __device__ int g_daa_device_error = 0;
+__device__ int g_daa_selftest_flag = 0;
+
+// Self-test of the bounded wait every kernel uses: one thread waits on the
+// first phase of an mbarrier that nothing arrives on.  The wait must give up
+// after its time limit, record kDevErrBarrierTimeout and let the kernel exit.
+__global__ void selftest_wait_kernel(int* err, int* gave_up) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  *gave_up = mbar_wait(&bar, 0, err) ? 0 : 1;
+}
 
 int* device_error_word() {
   static int* addr[64] = {nullptr};
@@ -413,6 +426,19 @@ daa_status daa_batch_attention_tree(const void* q, const void* kv_pages,
                         last_page_len, h_qo_indptr, h_kv_indptr, h_last_page_len, batch, 1,
                         sm_scale, out, lse_out, workspace, workspace_bytes, dims, stream, false,
                         tree_mask, mask_words);
+}
+
+daa_status daa_selftest_bounded_wait(int32_t* gave_up) {
+  if (!gave_up) return DAA_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  void* flag = nullptr;
+  if (!err || cudaGetSymbolAddress(&flag, g_daa_selftest_flag) != cudaSuccess) return DAA_ERR_CUDA;
+  selftest_wait_kernel<<<1, 32>>>(err, static_cast<int*>(flag));
+  if (cudaGetLastError() != cudaSuccess) return DAA_ERR_CUDA;
+  int v = -1;
+  if (cudaMemcpyFromSymbol(&v, g_daa_selftest_flag, sizeof(int)) != cudaSuccess) return DAA_ERR_CUDA;
+  *gave_up = v;
+  return DAA_OK;
 }
 
 daa_status daa_device_error(int32_t* code, int32_t reset) {

@@ -294,8 +294,24 @@ daa_status daa_batch_attention_noalloc(const void* q, const void* kv_pages,
  * Reads the device error word of the current device into *code (0 = none, 1 =
  * page id out of range, 2 = a bounded wait timed out, 3 = inconsistent request
  * lengths) and clears it when `reset` is non-zero.  Synchronises the device.
+ * Kernels never trap on these: a page id outside the pool is replaced by page
+ * 0 (or, in the append, the row is skipped), so the outputs of that call are
+ * undefined but the context stays usable.  Every wait inside a kernel is
+ * bounded (1 s); one that runs out records code 2 and the kernel runs on to its
+ * exit.  While the word holds code 2, waits of later launches give up at once,
+ * so clear it (reset = 1) after a timeout has been reported.
  */
 daa_status daa_device_error(int32_t* code, int32_t reset);
+
+/*
+ * Health check of the bounded waits (no counterpart on the pages): launches a
+ * one-thread kernel on the legacy default stream that waits on an mbarrier
+ * phase nothing completes, with the same bounded wait the attention kernels
+ * use, and returns after that wait has given up (about 1 s).  *gave_up = 1 when
+ * the wait ended by its limit; the device error word then holds code 2 (read
+ * and clear it with daa_device_error).  Synchronises the device.
+ */
+daa_status daa_selftest_bounded_wait(int32_t* gave_up);
 
 /*
  * Per-kernel timing with CUDA events.  While enabled, every kernel the library
