@@ -222,7 +222,7 @@ class GpuStep:
     """Device-resident workload: pool with the cached prefixes, page table,
     the step's q / k_new / v_new, outputs and workspace."""
 
-    def __init__(self, wl, device, k=0, fused=True):
+    def __init__(self, wl, device, k=0, fused=True, prefix_groups=True):
         import decode_attention_append_gb300 as daa
         self.daa = daa
         self.fused = fused
@@ -243,8 +243,12 @@ class GpuStep:
         q, kn, vn = wl.step_inputs(k)
         self.h_q, self.h_k, self.h_v = (x.pin_memory() for x in (q, kn, vn))
         self.q, self.k_new, self.v_new = (x.to(device) for x in (q, kn, vn))
+        # requests that share a cached prefix: the shared-prefix calls attend it
+        # once per group (off with --no-prefix-groups)
+        groups = wl.prefix_groups(k)
+        self.groups = groups if prefix_groups and int(groups[1].max(initial=0)) > 0 else None
         self.runner = daa.BatchAttention(self.table, wl.num_qo_heads, self.pool, causal=wl.causal,
-                                         sm_scale=wl.sm_scale)
+                                         sm_scale=wl.sm_scale, prefix_groups=self.groups)
         # draft-tree verification: the step's mask rows (int32 view of the bits)
         self.tree = wl.has_tree(k)
         self.h_mask = self.mask = None
@@ -294,12 +298,14 @@ class GpuStep:
         elif self.fused:
             self.daa.append_attention(self.k_new, self.v_new, self.q, self.pool, qo, kv, pi, ll,
                                       self.wl.causal, self.wl.sm_scale, out=self.out,
-                                      workspace=self.runner.workspace, host_indptr=hosts)
+                                      workspace=self.runner.workspace, host_indptr=hosts,
+                                      prefix_groups=self.groups)
         else:
             self.daa.kv_append(self.k_new, self.v_new, self.pool, qo, pi, kv, ll)
             self.daa.batch_attention(self.q, self.pool, qo, kv, pi, ll, self.wl.causal,
                                      self.wl.sm_scale, out=self.out,
-                                     workspace=self.runner.workspace, host_indptr=hosts)
+                                     workspace=self.runner.workspace, host_indptr=hosts,
+                                     prefix_groups=self.groups)
         self.h_out.copy_(self.out, non_blocking=True)
 
     def e2e_bytes(self):
@@ -357,12 +363,12 @@ class GpuStep:
         elif self.fused:
             self.daa.append_attention(kn, vn, q, self.pool, qo, kv, pi, ll, self.wl.causal,
                                       self.wl.sm_scale, out=out, workspace=self.runner.workspace,
-                                      host_indptr=hosts, stream=stream)
+                                      host_indptr=hosts, stream=stream, prefix_groups=self.groups)
         else:
             self.daa.kv_append(kn, vn, self.pool, qo, pi, kv, ll, stream=stream)
             self.daa.batch_attention(q, self.pool, qo, kv, pi, ll, self.wl.causal, self.wl.sm_scale,
                                      out=out, workspace=self.runner.workspace, host_indptr=hosts,
-                                     stream=stream)
+                                     stream=stream, prefix_groups=self.groups)
 
     def run_pipeline(self, steps):
         """`steps` end-to-end steps, timed on the compute stream by CUDA events
@@ -557,6 +563,9 @@ def main():
     ap.add_argument("--api", default="fused", choices=["fused", "two-call"],
                     help="fused: one append_attention call per step; two-call: kv_append then "
                          "batch_attention")
+    ap.add_argument("--no-prefix-groups", action="store_true",
+                    help="requests that share a cached prefix: plain calls (each request reads "
+                         "the prefix) instead of the shared-prefix calls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="profiling runs: timed steps only (no clock window, no traced or e2e pass)")
@@ -621,7 +630,8 @@ def main():
             __graft_entry__.build()
     import decode_attention_append_gb300 as daa
 
-    g = GpuStep(wl, dev, fused=args.api == "fused")
+    g = GpuStep(wl, dev, fused=args.api == "fused", prefix_groups=not args.no_prefix_groups)
+    config["prefix_groups"] = g.groups is not None
     flush_buf = None
     need_flush = algo_bytes < 2 * L2_BYTES
     if need_flush:

@@ -90,6 +90,16 @@ def load_library():
         lib.daa_batch_attention_noalloc.restype = i32
         lib.daa_batch_attention_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32,
                                                     vp, vp, _Dims, vp]
+        lib.daa_batch_attention_shared_prefix_workspace_size.restype = sz
+        lib.daa_batch_attention_shared_prefix_workspace_size.argtypes = [
+            vp, vp, vp, i32, vp, vp, i32, _Dims, ctypes.POINTER(i32)]
+        lib.daa_batch_attention_shared_prefix.restype = i32
+        lib.daa_batch_attention_shared_prefix.argtypes = [
+            vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, f32, vp, vp, vp, sz, _Dims, vp]
+        lib.daa_append_attention_shared_prefix.restype = i32
+        lib.daa_append_attention_shared_prefix.argtypes = [
+            vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, f32, vp, vp, vp, sz,
+            _Dims, vp]
         lib.daa_selftest_bounded_wait.restype = i32
         lib.daa_selftest_bounded_wait.argtypes = [ctypes.POINTER(i32)]
         lib.daa_device_error.restype = i32
@@ -176,15 +186,59 @@ def batch_attention_workspace_size(h_qo_indptr, h_kv_indptr, h_last_page_len, nu
     return int(n)
 
 
+def _host_groups(prefix_groups):
+    """(indptr, prefix_len) -> host int32 arrays and the group count."""
+    ind, pl = (_host_i32(x) for x in prefix_groups)
+    if len(ind) != len(pl) + 1:
+        raise ValueError("prefix_groups: indptr must have one more entry than prefix_len")
+    return ind, pl, len(pl)
+
+
+def shared_prefix_workspace_size(h_qo_indptr, h_kv_indptr, h_last_page_len, prefix_groups,
+                                 num_qo_heads, num_kv_heads, head_dim, page_size,
+                                 num_pages) -> int:
+    """Workspace bytes of ``batch_attention(..., prefix_groups=...)`` (and of
+    ``append_attention`` with the same groups)."""
+    lib = load_library()
+    qo, kv, ll = _host_i32(h_qo_indptr), _host_i32(h_kv_indptr), _host_i32(h_last_page_len)
+    gi, gl, ng = _host_groups(prefix_groups)
+    st = ctypes.c_int32(0)
+    n = lib.daa_batch_attention_shared_prefix_workspace_size(
+        _ptr(qo), _ptr(kv), _ptr(ll), len(qo) - 1, _ptr(gi), _ptr(gl), ng,
+        _Dims(num_qo_heads, num_kv_heads, head_dim, page_size, num_pages), ctypes.byref(st))
+    _check(st.value, "shared_prefix_workspace_size")
+    return int(n)
+
+
+def _workspace_need(lib, hq, hk, hl, dims, groups, what):
+    st = ctypes.c_int32(0)
+    if groups is None:
+        need = lib.daa_batch_attention_workspace_size(_ptr(hq), _ptr(hk), _ptr(hl), len(hq) - 1,
+                                                      dims, ctypes.byref(st))
+    else:
+        gi, gl, ng = groups
+        need = lib.daa_batch_attention_shared_prefix_workspace_size(
+            _ptr(hq), _ptr(hk), _ptr(hl), len(hq) - 1, _ptr(gi), _ptr(gl), ng, dims,
+            ctypes.byref(st))
+    _check(st.value, what)
+    return int(need)
+
+
 def batch_attention(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len, causal=True,
                     sm_scale=None, out=None, lse=None, workspace=None, host_indptr=None,
-                    stream=None):
+                    stream=None, prefix_groups=None):
     """Mixed-batch paged attention.  Returns ``out`` (and fills ``lse`` if given).
 
     ``host_indptr`` = (h_qo_indptr, h_kv_indptr, h_last_page_len) host copies of
     the page table used for planning; when omitted they are copied from the
     device (a synchronisation).  ``workspace`` (uint8 CUDA tensor) is allocated
     by torch here when omitted; the library itself never allocates.
+
+    ``prefix_groups`` = (indptr, prefix_len), host int arrays: group i is
+    requests [indptr[i], indptr[i+1]) whose first prefix_len[i] keys sit in the
+    same pages (a shared cached prefix).  The shared keys are then attended
+    once for all the group's rows (``daa_batch_attention_shared_prefix``); the
+    result is the same.
     """
     lib = load_library()
     _dev_bf16(q, "q"), _dev_bf16(kv_pages, "kv_pages")
@@ -204,18 +258,24 @@ def batch_attention(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_l
     _dev_bf16(out, "out")
     if lse is not None and not (lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous()):
         raise TypeError("lse must be a contiguous fp32 CUDA tensor")
-    st = ctypes.c_int32(0)
-    need = lib.daa_batch_attention_workspace_size(_ptr(hq), _ptr(hk), _ptr(hl), batch, dims,
-                                                  ctypes.byref(st))
-    _check(st.value, "batch_attention")
+    groups = None if prefix_groups is None else _host_groups(prefix_groups)
+    need = _workspace_need(lib, hq, hk, hl, dims, groups, "batch_attention")
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib.daa_batch_attention(_ptr(q), _ptr(kv_pages), _ptr(qo_indptr), _ptr(kv_indptr),
-                                   _ptr(page_indices), _ptr(last_page_len), _ptr(hq), _ptr(hk),
-                                   _ptr(hl), batch, int(bool(causal)), float(sm_scale), _ptr(out),
-                                   _ptr(lse), _ptr(workspace), ws_bytes, dims, _stream(stream)),
-           "batch_attention")
+    if groups is None:
+        st = lib.daa_batch_attention(_ptr(q), _ptr(kv_pages), _ptr(qo_indptr), _ptr(kv_indptr),
+                                     _ptr(page_indices), _ptr(last_page_len), _ptr(hq), _ptr(hk),
+                                     _ptr(hl), batch, int(bool(causal)), float(sm_scale), _ptr(out),
+                                     _ptr(lse), _ptr(workspace), ws_bytes, dims, _stream(stream))
+    else:
+        gi, gl, ng = groups
+        st = lib.daa_batch_attention_shared_prefix(
+            _ptr(q), _ptr(kv_pages), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(page_indices),
+            _ptr(last_page_len), _ptr(hq), _ptr(hk), _ptr(hl), batch, _ptr(gi), _ptr(gl), ng,
+            int(bool(causal)), float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+            dims, _stream(stream))
+    _check(st, "batch_attention")
     return out
 
 
@@ -271,11 +331,12 @@ def batch_attention_tree(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_p
 
 def append_attention(k_new, v_new, q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len,
                      causal=True, sm_scale=None, out=None, lse=None, workspace=None,
-                     host_indptr=None, stream=None):
+                     host_indptr=None, stream=None, prefix_groups=None):
     """``kv_append`` of this step's new K/V (rows laid out like ``q``) followed
     by ``batch_attention``, in one call: same results, with the attention
     kernels launched behind the append so that the work that does not read the
-    appended rows overlaps it.  Arguments as ``batch_attention``."""
+    appended rows overlaps it.  Arguments as ``batch_attention`` (including
+    ``prefix_groups``)."""
     lib = load_library()
     _dev_bf16(k_new, "k_new"), _dev_bf16(v_new, "v_new")
     _dev_bf16(q, "q"), _dev_bf16(kv_pages, "kv_pages")
@@ -297,20 +358,26 @@ def append_attention(k_new, v_new, q, kv_pages, qo_indptr, kv_indptr, page_indic
     _dev_bf16(out, "out")
     if lse is not None and not (lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous()):
         raise TypeError("lse must be a contiguous fp32 CUDA tensor")
+    groups = None if prefix_groups is None else _host_groups(prefix_groups)
     if workspace is None:
-        st = ctypes.c_int32(0)
-        need = lib.daa_batch_attention_workspace_size(_ptr(hq), _ptr(hk), _ptr(hl), batch, dims,
-                                                      ctypes.byref(st))
-        _check(st.value, "append_attention")
+        need = _workspace_need(lib, hq, hk, hl, dims, groups, "append_attention")
         if need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib.daa_append_attention(_ptr(k_new), _ptr(v_new), _ptr(q), _ptr(kv_pages),
-                                    _ptr(qo_indptr), _ptr(kv_indptr), _ptr(page_indices),
-                                    _ptr(last_page_len), _ptr(hq), _ptr(hk), _ptr(hl), batch,
-                                    int(bool(causal)), float(sm_scale), _ptr(out), _ptr(lse),
-                                    _ptr(workspace), ws_bytes, dims, _stream(stream)),
-           "append_attention")
+    if groups is None:
+        st = lib.daa_append_attention(_ptr(k_new), _ptr(v_new), _ptr(q), _ptr(kv_pages),
+                                      _ptr(qo_indptr), _ptr(kv_indptr), _ptr(page_indices),
+                                      _ptr(last_page_len), _ptr(hq), _ptr(hk), _ptr(hl), batch,
+                                      int(bool(causal)), float(sm_scale), _ptr(out), _ptr(lse),
+                                      _ptr(workspace), ws_bytes, dims, _stream(stream))
+    else:
+        gi, gl, ng = groups
+        st = lib.daa_append_attention_shared_prefix(
+            _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(kv_pages), _ptr(qo_indptr), _ptr(kv_indptr),
+            _ptr(page_indices), _ptr(last_page_len), _ptr(hq), _ptr(hk), _ptr(hl), batch,
+            _ptr(gi), _ptr(gl), ng, int(bool(causal)), float(sm_scale), _ptr(out), _ptr(lse),
+            _ptr(workspace), ws_bytes, dims, _stream(stream))
+    _check(st, "append_attention")
     return out
 
 
@@ -363,15 +430,21 @@ class BatchAttention:
     """Plan-once / run-many wrapper for one batch shape (FlashInfer-style)."""
 
     def __init__(self, table: PageTable, num_qo_heads: int, kv_pages: torch.Tensor, causal=True,
-                 sm_scale=None):
+                 sm_scale=None, prefix_groups=None):
         self.t = table
         self.kv_pages = kv_pages
         self.causal = causal
         self.Hq = num_qo_heads
         self.sm_scale = sm_scale if sm_scale is not None else 1.0 / float(kv_pages.shape[4]) ** 0.5
+        self.prefix_groups = prefix_groups
         n, _, hkv, p, d = kv_pages.shape
-        need = batch_attention_workspace_size(table.h_qo_indptr, table.h_kv_indptr,
-                                              table.h_last_page_len, num_qo_heads, hkv, d, p, n)
+        if prefix_groups is None:
+            need = batch_attention_workspace_size(table.h_qo_indptr, table.h_kv_indptr,
+                                                  table.h_last_page_len, num_qo_heads, hkv, d, p, n)
+        else:
+            need = shared_prefix_workspace_size(table.h_qo_indptr, table.h_kv_indptr,
+                                                table.h_last_page_len, prefix_groups,
+                                                num_qo_heads, hkv, d, p, n)
         self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=kv_pages.device)
 
     def append(self, k_new, v_new, stream=None):
@@ -386,13 +459,15 @@ class BatchAttention:
                                 t.page_indices, t.last_page_len, self.causal, self.sm_scale,
                                 out=out, lse=lse, workspace=self.workspace,
                                 host_indptr=(t.h_qo_indptr, t.h_kv_indptr, t.h_last_page_len),
-                                stream=stream)
+                                stream=stream, prefix_groups=self.prefix_groups)
 
     def run(self, q, out=None, lse=None, stream=None, tree_mask=None):
         """Attention over the batch; with ``tree_mask``, under draft-tree masks
         (``batch_attention_tree``; the batch must be causal)."""
         t = self.t
         if tree_mask is not None:
+            if self.prefix_groups is not None:
+                raise ValueError("tree masks and prefix groups are not combined")
             if not self.causal:
                 raise ValueError("a tree mask refines the causal rule")
             return batch_attention_tree(q, self.kv_pages, t.qo_indptr, t.kv_indptr, t.page_indices,
@@ -405,7 +480,7 @@ class BatchAttention:
                                t.last_page_len, self.causal, self.sm_scale, out=out, lse=lse,
                                workspace=self.workspace,
                                host_indptr=(t.h_qo_indptr, t.h_kv_indptr, t.h_last_page_len),
-                               stream=stream)
+                               stream=stream, prefix_groups=self.prefix_groups)
 
 
 def device_error(reset: bool = True) -> int:

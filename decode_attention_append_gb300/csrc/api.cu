@@ -101,8 +101,21 @@ HostPlan& host_plan() {
 }
 
 daa_status make_plan(const int32_t* qo, const int32_t* kv, const int32_t* last, int32_t batch,
-                     const daa_dims& d, int sms, HostPlan& pl) {
-  return plan_batch(qo, kv, last, batch, d, sms, pl.units, pl.merges, pl.tiles, pl.lay);
+                     const daa_dims& d, int sms, HostPlan& pl,
+                     const PrefixGroups* groups = nullptr) {
+  return plan_batch(qo, kv, last, batch, d, sms, pl.units, pl.merges, pl.tiles, pl.lay, groups);
+}
+
+// Host prefix groups of a shared-prefix call, checked for null arrays and a
+// negative count (the planner checks them against the page table).
+daa_status make_groups(const int32_t* h_prefix_indptr, const int32_t* h_prefix_len,
+                       int32_t n_groups, PrefixGroups& g) {
+  if (n_groups < 0) return DAA_ERR_INVALID_ARG;
+  if (n_groups > 0 && (!h_prefix_indptr || !h_prefix_len)) return DAA_ERR_INVALID_ARG;
+  g.indptr = h_prefix_indptr;
+  g.prefix_len = h_prefix_len;
+  g.n = n_groups;
+  return DAA_OK;
 }
 
 // ------------------------------------------------------------------ tracing
@@ -309,6 +322,19 @@ size_t daa_batch_attention_workspace_size(const int32_t* h_qo_indptr, const int3
   return st == DAA_OK ? pl.lay.total : 0;
 }
 
+size_t daa_batch_attention_shared_prefix_workspace_size(
+    const int32_t* h_qo_indptr, const int32_t* h_kv_indptr, const int32_t* h_last_page_len,
+    int32_t batch, const int32_t* h_prefix_indptr, const int32_t* h_prefix_len, int32_t n_groups,
+    daa_dims dims, daa_status* status) {
+  PrefixGroups g{};
+  daa_status st = make_groups(h_prefix_indptr, h_prefix_len, n_groups, g);
+  HostPlan& pl = host_plan();
+  if (st == DAA_OK)
+    st = make_plan(h_qo_indptr, h_kv_indptr, h_last_page_len, batch, dims, num_sms(), pl, &g);
+  if (status) *status = st;
+  return st == DAA_OK ? pl.lay.total : 0;
+}
+
 }  // extern "C"
 
 namespace {
@@ -323,10 +349,12 @@ daa_status attention_call(const void* k_new, const void* v_new, const void* q,
                           int32_t batch, int32_t causal, float sm_scale, void* out,
                           float* lse_out, void* workspace, size_t workspace_bytes,
                           const daa_dims& dims, void* stream, bool fused,
-                          const uint32_t* tree_mask = nullptr, int32_t mask_words = 0) {
+                          const uint32_t* tree_mask = nullptr, int32_t mask_words = 0,
+                          const PrefixGroups* groups = nullptr) {
   if (!(std::isfinite(sm_scale)) || !(sm_scale > 0.f)) return DAA_ERR_INVALID_ARG;
   HostPlan& pl = host_plan();
-  daa_status st = make_plan(h_qo_indptr, h_kv_indptr, h_last_page_len, batch, dims, num_sms(), pl);
+  daa_status st =
+      make_plan(h_qo_indptr, h_kv_indptr, h_last_page_len, batch, dims, num_sms(), pl, groups);
   if (st != DAA_OK) return st;
   if (tree_mask) {
     // the mask refines the causal rule; each request's new tokens fit its rows
@@ -426,6 +454,38 @@ daa_status daa_batch_attention_tree(const void* q, const void* kv_pages,
                         last_page_len, h_qo_indptr, h_kv_indptr, h_last_page_len, batch, 1,
                         sm_scale, out, lse_out, workspace, workspace_bytes, dims, stream, false,
                         tree_mask, mask_words);
+}
+
+daa_status daa_batch_attention_shared_prefix(
+    const void* q, const void* kv_pages, const int32_t* qo_indptr, const int32_t* kv_indptr,
+    const int32_t* page_indices, const int32_t* last_page_len, const int32_t* h_qo_indptr,
+    const int32_t* h_kv_indptr, const int32_t* h_last_page_len, int32_t batch,
+    const int32_t* h_prefix_indptr, const int32_t* h_prefix_len, int32_t n_groups, int32_t causal,
+    float sm_scale, void* out, float* lse_out, void* workspace, size_t workspace_bytes,
+    daa_dims dims, void* stream) {
+  PrefixGroups g{};
+  daa_status st = make_groups(h_prefix_indptr, h_prefix_len, n_groups, g);
+  if (st != DAA_OK) return st;
+  return attention_call(nullptr, nullptr, q, kv_pages, qo_indptr, kv_indptr, page_indices,
+                        last_page_len, h_qo_indptr, h_kv_indptr, h_last_page_len, batch, causal,
+                        sm_scale, out, lse_out, workspace, workspace_bytes, dims, stream, false,
+                        nullptr, 0, &g);
+}
+
+daa_status daa_append_attention_shared_prefix(
+    const void* k_new, const void* v_new, const void* q, void* kv_pages, const int32_t* qo_indptr,
+    const int32_t* kv_indptr, const int32_t* page_indices, const int32_t* last_page_len,
+    const int32_t* h_qo_indptr, const int32_t* h_kv_indptr, const int32_t* h_last_page_len,
+    int32_t batch, const int32_t* h_prefix_indptr, const int32_t* h_prefix_len, int32_t n_groups,
+    int32_t causal, float sm_scale, void* out, float* lse_out, void* workspace,
+    size_t workspace_bytes, daa_dims dims, void* stream) {
+  PrefixGroups g{};
+  daa_status st = make_groups(h_prefix_indptr, h_prefix_len, n_groups, g);
+  if (st != DAA_OK) return st;
+  return attention_call(k_new, v_new, q, kv_pages, qo_indptr, kv_indptr, page_indices,
+                        last_page_len, h_qo_indptr, h_kv_indptr, h_last_page_len, batch, causal,
+                        sm_scale, out, lse_out, workspace, workspace_bytes, dims, stream, true,
+                        nullptr, 0, &g);
 }
 
 daa_status daa_selftest_bounded_wait(int32_t* gave_up) {

@@ -5,8 +5,10 @@
 // (o_p normalised over its own keys, lse_p in the log2 domain):
 //   M = max_p lse_p,  w_p = 2^(lse_p - M),  o = sum_p w_p o_p / sum_p w_p,
 //   lse = M + log2 sum_p w_p   (reported as natural log).
-// One warp per (request, query head); lanes stride the d dimension so every
-// partial row is read with coalesced 16-byte loads.
+// One warp per (query row, query head); lanes stride the d dimension so every
+// partial row is read with coalesced 16-byte loads.  A row's parts are its
+// n_parts consecutive key-split slots plus, when it follows a shared prefix
+// attended once for a group of requests, the slot holding that prefix part.
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -23,10 +25,11 @@ __global__ void __launch_bounds__(32 * kMergeWarps) softmax_merge_kernel(const M
   grid_dep_wait();  // the partials come from the decode kernel launched before
   if (hq >= a.Hq) return;
   const MergeItem it = a.items[blockIdx.x];
-  const float* lse = a.part_lse + (int64_t)it.part_begin * a.Hq + hq;
+  const int n = it.n_parts + (it.extra >= 0 ? 1 : 0);
+  auto slot = [&](int p) -> int64_t { return p < it.n_parts ? it.part_begin + p : it.extra; };
 
   float M = -INFINITY;
-  for (int p = lane; p < it.n_parts; p += 32) M = fmaxf(M, lse[(int64_t)p * a.Hq]);
+  for (int p = lane; p < n; p += 32) M = fmaxf(M, a.part_lse[slot(p) * a.Hq + hq]);
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
 
@@ -34,10 +37,11 @@ __global__ void __launch_bounds__(32 * kMergeWarps) softmax_merge_kernel(const M
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
   float wsum = 0.f;
-  for (int p = 0; p < it.n_parts; ++p) {
-    const float w = ex2_approx(lse[(int64_t)p * a.Hq] - M);
+  for (int p = 0; p < n; ++p) {
+    const int64_t sl = slot(p);
+    const float w = ex2_approx(a.part_lse[sl * a.Hq + hq] - M);
     wsum += w;
-    const float* po = a.part_o + ((int64_t)(it.part_begin + p) * a.Hq + hq) * D + lane * EPL;
+    const float* po = a.part_o + (sl * a.Hq + hq) * D + lane * EPL;
     if constexpr (EPL == 4) {
       const float4 v = *reinterpret_cast<const float4*>(po);
       acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);

@@ -18,12 +18,14 @@ struct DecodeUnit {
   int32_t pad0, pad1;
 };
 
-// softmax_merge of the partials of one decode request that was split.
+// softmax_merge of the partials of one query row: n_parts consecutive slots
+// from part_begin (the key splits of its request), plus slot `extra` when the
+// row's shared prefix was attended by a prefix-group item (else -1).
 struct MergeItem {
   int32_t q_row;
   int32_t part_begin;  // first partial slot
   int32_t n_parts;     // consecutive slots to merge
-  int32_t pad;
+  int32_t extra;       // one more slot (the row's shared-prefix partial), or -1
 };
 
 // A work item of the tensor-core kernel: one or two 128-row tiles of packed
@@ -48,13 +50,26 @@ struct PrefillTile {
   int32_t key_hi;     // one past the last key
   int32_t part;       // partial slot, or -1: write out / lse_out directly
   int32_t work;       // planner's sort key (keys read)
-  int32_t part_stride;  // key-split multi-token item: token t (counted from tok0, across
-                        // both tiles) writes its partial to slot part + t * part_stride
+  int32_t part_stride;  // key-split multi-token item: token t of the request writes its
+                        // partial to slot part + t * part_stride
+  int32_t kind;       // kTileRequest, or kTilePrefixGroup (see below)
+  int32_t pad0, pad1, pad2;
 };
+
+// Tile kinds.  A prefix-group item attends the query rows of several
+// consecutive requests that share a cached prefix to the keys of that prefix
+// (read once for all of them): q_row0 / qo_len span the group's rows,
+// kv_len = key_hi = the shared keys (a multiple of 128), page_base = the first
+// request's page list; every row sees every key (the prefix precedes all new
+// tokens), and each row writes its partial to the slot the row-to-slot table
+// of the plan gives.
 
 static_assert(sizeof(DecodeUnit) == 32, "DecodeUnit layout");
 static_assert(sizeof(MergeItem) == 16, "MergeItem layout");
-static_assert(sizeof(PrefillTile) == 48, "PrefillTile layout");
+constexpr int32_t kTileRequest = 0;
+constexpr int32_t kTilePrefixGroup = 1;
+
+static_assert(sizeof(PrefillTile) == 64, "PrefillTile layout");
 
 // Kernel ids reported by the tracer.
 enum KernelId : int32_t {

@@ -26,6 +26,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <vector>
 
 #include "../../include/daa.h"
 #include "launch.h"
@@ -62,6 +63,16 @@ inline daa_status plan_check_dims(const daa_dims& d) {
   return DAA_OK;
 }
 
+// Requests that share a cached prefix (a prefix-cache hit, "Chunked prefill",
+// #prefix-cache-interaction): group i is requests [indptr[i], indptr[i+1]),
+// consecutive, whose first prefix_len[i] tokens sit in the same pages.  Host
+// arrays.
+struct PrefixGroups {
+  const int32_t* indptr;      // [n + 1], non-decreasing, within [0, batch]
+  const int32_t* prefix_len;  // [n], multiples of the page size
+  int32_t n;
+};
+
 // Offsets of the workspace sections (bytes).  Tensor-core items are stored
 // as three consecutive groups, each launched as its own kernel: prefill items,
 // short items (single-CTA kernel, head_dim 128 only; for head_dim 64 they join
@@ -73,10 +84,19 @@ struct PlanLayout {
 };
 
 // Vec: push_back(const T&) -> bool (false when full), size(), data(), clear().
+// With `groups`: within each group, every maximal run of consecutive requests
+// with 1 <= qo_len <= two Q tiles (decode, verify and short requests) that has
+// two or more such members attends the group's shared keys -- whole 128-key
+// tiles of its prefix -- once for all its rows (prefix-group items), and each
+// member's own items start after them; softmax_merge then combines each row's
+// prefix partial with its own.  Prefill requests of a group keep the prefix in
+// their own items: their Q tiles are full already, so sharing would only add
+// partials to merge.  Without groups the plan allocates nothing beyond the
+// Vecs.
 template <class UnitVec, class MergeVec, class TileVec>
 daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last, int32_t batch,
                       const daa_dims& d, int sms, UnitVec& units, MergeVec& merges,
-                      TileVec& tiles, PlanLayout& lay) {
+                      TileVec& tiles, PlanLayout& lay, const PrefixGroups* groups = nullptr) {
   units.clear();
   merges.clear();
   tiles.clear();
@@ -106,6 +126,58 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
     if (nq >= 1 && nq <= verify_max) dec_pages += np;
     else if (nq > verify_max && nq <= short_max) short_pages += np;
   }
+  // prefix-group runs (see above): shared keys and the partial slot of row 0
+  // of each member, per request; slots [0, group_rows) hold the runs' rows
+  struct Run {
+    int r0, r1, sk, slot0;
+  };
+  std::vector<Run> runs;
+  std::vector<int32_t> shared_keys, shared_slot;
+  int group_rows = 0;
+  if (groups && groups->n > 0) {
+    if (!groups->indptr || !groups->prefix_len) return DAA_ERR_INVALID_ARG;
+    if (groups->indptr[0] < 0 || groups->indptr[groups->n] > batch) return DAA_ERR_SHAPE;
+    shared_keys.assign(batch, 0);
+    shared_slot.assign(batch, -1);
+    for (int i = 0; i < groups->n; ++i) {
+      const int b0 = groups->indptr[i], b1 = groups->indptr[i + 1];
+      const int pl = groups->prefix_len[i];
+      if (b1 < b0 || pl < 0 || pl % P != 0) return DAA_ERR_SHAPE;
+      for (int r = b0; r < b1; ++r) {
+        const int np = kv[r + 1] - kv[r];
+        const int64_t kv_len = np > 0 ? (int64_t)(np - 1) * P + last[r] : 0;
+        if (pl > kv_len - (qo[r + 1] - qo[r])) return DAA_ERR_SHAPE;  // the prefix is cached
+      }
+      const int sk = pl / kPrefillTileRows * kPrefillTileRows;
+      if (sk == 0) continue;
+      for (int r = b0; r < b1;) {
+        const int nq = qo[r + 1] - qo[r];
+        if (nq > short_max || nq == 0) {  // a prefill request ends a run; runs start with rows
+          ++r;
+          continue;
+        }
+        int r1 = r, members = 0;
+        for (; r1 < b1 && qo[r1 + 1] - qo[r1] <= short_max; ++r1)
+          if (qo[r1 + 1] > qo[r1]) ++members;
+        if (members >= 2) {
+          runs.push_back(Run{r, r1, sk, group_rows});
+          for (int m = r; m < r1; ++m) {
+            shared_keys[m] = sk;
+            shared_slot[m] = group_rows + (qo[m] - qo[r]);
+          }
+          group_rows += qo[r1] - qo[r];
+        }
+        r = r1;
+      }
+    }
+    // the shared keys are not read again by the members' own splits
+    for (int r = 0; r < batch; ++r) {
+      const int64_t nq = (int64_t)qo[r + 1] - qo[r];
+      if (nq >= 1 && nq <= verify_max) dec_pages -= shared_keys[r] / P;
+      else if (nq > verify_max && nq <= short_max) short_pages -= shared_keys[r] / P;
+    }
+  }
+  auto shared_of = [&](int r) -> int { return shared_keys.empty() ? 0 : shared_keys[r]; };
   const int64_t page_heads = dec_pages * d.num_kv_heads;
 
   // split sizes (pages).  CUDA-core splits: about twenty per SM (ten per CTA
@@ -125,6 +197,38 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
   int64_t split_short = (short_pages * d.num_kv_heads + sms - 1) / sms;
   split_short = std::max<int64_t>(32, (split_short + 7) / 8 * 8);
 
+  // prefix-group items first: each run's rows hold consecutive partial slots
+  // (one per token, in row order) from slot 0, named by their merge items
+  lay.n_parts = group_rows;
+  for (const Run& run : runs) {
+    const int rows = qo[run.r1] - qo[run.r0];
+    for (int t0 = 0; t0 < rows; t0 += (quads ? 4 : 2) * tpt) {
+      PrefillTile t{};
+      t.q_row0 = qo[run.r0];
+      t.qo_len = rows;
+      t.kv_len = run.sk;
+      t.page_base = kv[run.r0];
+      t.tok0 = t0;
+      int ntiles;
+      if (quads) {
+        t.ntok = std::min(4 * tpt, rows - t0);
+        t.ntok1 = 0;
+        ntiles = (t.ntok + tpt - 1) / tpt;
+      } else {
+        t.ntok = std::min(tpt, rows - t0);
+        t.ntok1 = t.ntok == tpt ? std::max(0, std::min(tpt, rows - t0 - tpt)) : 0;
+        ntiles = t.ntok1 > 0 ? 2 : 1;
+      }
+      t.key_lo = 0;
+      t.key_hi = run.sk;
+      t.part = run.slot0;
+      t.part_stride = 1;
+      t.kind = kTilePrefixGroup;
+      t.work = run.sk * ntiles;
+      if (!tiles.push_back(t)) return DAA_ERR_WORKSPACE;
+    }
+  }
+
   // decode (qo_len 1), verify (qo_len 2 .. verify_max) and short
   // (verify_max < qo_len <= short_max) requests: key-split items
   for (int r = 0; r < batch; ++r) {
@@ -135,23 +239,28 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
     const int64_t split = is_short ? split_short : on_tc ? split_tc : split_cc;
     const int np = kv[r + 1] - kv[r];
     const int kv_len = (np - 1) * P + last[r];
-    // splits cut the keys token 0 can see, [0, kv_len - nq], so every split
-    // starts at a key each token sees; the last split also takes the tail
+    const int sk = shared_of(r);  // keys a prefix-group item covers
+    // splits cut the keys token 0 can see past the shared ones, [sk, kv_len -
+    // nq], so every split starts at a key each token sees; the last split also
+    // takes the tail
     const int64_t vis = (int64_t)kv_len - nq + 1;
-    const int nsplit = (int)((vis + split * P - 1) / (split * P));
+    const int nsplit = (int)((vis - sk + split * P - 1) / (split * P));
     // partial slots: token t of split s at part0 + t * nsplit + s, so each
-    // token's splits are consecutive for its softmax_merge item
+    // token's splits are consecutive for its softmax_merge item (which also
+    // takes the row's prefix partial when sk > 0)
     int part0 = -1;
-    if (nsplit > 1) {
+    if (nsplit > 1 || sk > 0) {
+      const int32_t pbase = sk > 0 ? shared_slot[r] : -1;
       for (int t = 0; t < nq; ++t)
-        if (!merges.push_back(MergeItem{qo[r] + t, lay.n_parts + t * nsplit, nsplit, 0}))
+        if (!merges.push_back(MergeItem{qo[r] + t, lay.n_parts + t * nsplit, nsplit,
+                                        sk > 0 ? pbase + t : -1}))
           return DAA_ERR_WORKSPACE;
       part0 = lay.n_parts;
       lay.n_parts += nsplit * nq;
     }
     for (int s = 0; s < nsplit; ++s) {
-      const int lo = (int)(s * split * P);
-      const int hi = s == nsplit - 1 ? kv_len : (int)((s + 1) * split * P);
+      const int lo = (int)(sk + s * split * P);
+      const int hi = s == nsplit - 1 ? kv_len : (int)(sk + (s + 1) * split * P);
       if (on_tc) {
         PrefillTile t{};
         t.q_row0 = qo[r];
@@ -223,6 +332,7 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
   // own group only where prefill runs on CTA pairs), decode / verify items --
   // most work first within each group
   auto group = [=](const PrefillTile& t) {
+    if (t.kind == kTilePrefixGroup) return 0;  // with the prefill items
     if (t.qo_len <= verify_max) return 2;
     return quads && t.qo_len <= short_max ? 1 : 0;
   };

@@ -150,10 +150,13 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
   const bool one_token = tile.ntok == 1 && nq == 1;
 
   // key tiles kt0 .. kt0 + n_kt - 1 cover keys [key_lo, kend); causal rows mask
-  // beyond their own position
+  // beyond their own position.  A prefix-group item's keys (a cached prefix
+  // shared by several requests) precede every one of its rows: no mask.
+  const bool prefix_group = tile.kind == kTilePrefixGroup;
+  const bool causal = a.causal && !prefix_group;
   const int pos_first = tile.kv_len - tile.qo_len + tile.tok0;
   const int ntok_all = tile.ntok + tile.ntok1;
-  const int kv_end = a.causal ? min(tile.kv_len, pos_first + ntok_all) : tile.kv_len;
+  const int kv_end = causal ? min(tile.kv_len, pos_first + ntok_all) : tile.kv_len;
   const int kend = min(kv_end, tile.key_hi);
   const int kt0 = tile.key_lo / KT;
   const int n_kt = (kend + KT - 1) / KT - kt0;
@@ -214,8 +217,9 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
     int64_t pid = load_ids(0);
     // the request's last qo_len keys are the rows appended in this step: the
     // first ring item that reaches them waits for the kernel launched before
-    // this one (tiles of cached keys stream while that kernel still runs)
-    const int first_new = tile.kv_len - tile.qo_len;
+    // this one (tiles of cached keys stream while that kernel still runs).  A
+    // prefix-group item reads only cached keys.
+    const int first_new = prefix_group ? tile.kv_len : tile.kv_len - tile.qo_len;
     bool dep_waited = false;
     for (int i = 0; i < 2 * n_kt; ++i) {
       const int64_t pid_next = load_ids(i + 1);
@@ -247,6 +251,11 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
       }
       pid = pid_next;
     }
+    // a prefix-group item reads no appended row but still waits before it
+    // exits: a launch may hold nothing else, and the kernels after it rely on
+    // its completion implying that of the kernel before it.  (Key splits of
+    // cached rows need not: their request's last split waits.)
+    if (prefix_group && !dep_waited) grid_dep_wait();
     __syncwarp();
     if (last_partial) {
       // last V tile: rows past the request's last key must hold finite values
@@ -377,17 +386,20 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
     const int q_tok0 = tile.tok0 + q * tile.ntok;  // first token of this Q tile
     const int tl = row / g;
     const int qpos = tile.kv_len - tile.qo_len + q_tok0 + tl;
-    const int row_end = min(a.causal ? min(qpos + 1, tile.kv_len) : tile.kv_len, kend);  // keys < row_end
+    const int row_end = min(causal ? min(qpos + 1, tile.kv_len) : tile.kv_len, kend);  // keys < row_end
     SoftmaxRowOut ro;
     ro.q_row = tile.q_row0 + q_tok0 + tl;
     ro.hq = kvh * g + (row - tl * g);
     ro.write = row < q_ntok * g;
-    ro.part = tile.part >= 0 ? tile.part + (q_tok0 - tile.tok0 + tl) * tile.part_stride : -1;
+    // partial slot of token t (counted from the first token of the request,
+    // or of the group): part + t * part_stride
+    ro.part = tile.part >= 0 ? tile.part + (q_tok0 + tl) * tile.part_stride : -1;
     TreeRow tr;
-    tr.bits = TREE && ro.write ? a.tree_mask + (int64_t)ro.q_row * a.mask_words : nullptr;
+    tr.bits = TREE && ro.write && !prefix_group ? a.tree_mask + (int64_t)ro.q_row * a.mask_words
+                                                : nullptr;
     tr.words = a.mask_words;
-    tr.draft0 = tile.kv_len - tile.qo_len;
-    tr.tok = q_tok0 + tl;
+    tr.draft0 = prefix_group ? tile.kv_len : tile.kv_len - tile.qo_len;  // no draft keys
+    tr.tok = prefix_group ? 0 : q_tok0 + tl;
     tc_softmax_rows<D, KT, TREE>(a, tmem + lane_off, tmem + C::O_COL + q * D + lane_off, s_full, &o_done[q],
                            q, nq == 1, n_kt, kt0, row_end, ro, tr, [&](int b) {
                              if (lane == 0) mbar_arrive(&p_full[b]);

@@ -245,6 +245,69 @@ daa_status daa_batch_attention_tree(const void* q, const void* kv_pages,
                                     void* out, float* lse_out, void* workspace,
                                     size_t workspace_bytes, daa_dims dims, void* stream);
 
+/*
+ * Mixed-batch paged attention for requests that share a cached prefix, with
+ * that prefix's keys read once for the whole group ("Chunked prefill"
+ * (k4i.top), #prefix-cache-interaction: the cached blocks of a prefix hit are
+ * skipped, only the suffix is computed; #correctness: attention over a key set
+ * is the softmax_merge of attentions over a partition of it).
+ *
+ * The result -- out, lse_out -- is that of daa_batch_attention on the same
+ * arguments (equal up to fp32 rounding order).  What differs is the schedule.
+ * For every group of two or more requests, the query rows of all its requests
+ * (one per new token and query head) are attended to the group's shared keys
+ * in one pass, with the rows of several requests packed into the same
+ * 128-row tensor-core tiles.  Only whole 128-key tiles of the prefix are
+ * shared; the rest of it is read per request.  Each request's own items then
+ * cover only the keys after the shared part.  softmax_merge combines the two
+ * parts per row.  K/V bytes of the shared prefix are read once per group
+ * instead of once per request.
+ *
+ * Groups (host arrays): group i is requests [h_prefix_indptr[i],
+ * h_prefix_indptr[i+1]) -- consecutive requests, groups in request order --
+ * whose first h_prefix_len[i] keys are the same tokens in the same pages: for
+ * every request r of the group, page_indices[kv_indptr[r] + p] is the same
+ * page for every p < h_prefix_len[i] / page_size.  The library cannot check
+ * this (page ids live only on the device); a group that breaks it gives wrong
+ * outputs, never an access outside the pool.  h_prefix_len[i] must be a
+ * multiple of page_size and cached: at most kv_len_r - qo_len_r for every
+ * request of the group.  Requests in no group, and groups of one request,
+ * are planned as in daa_batch_attention.
+ *
+ *  h_prefix_indptr  host int32 [n_groups + 1], non-decreasing, in [0, batch]
+ *  h_prefix_len     host int32 [n_groups]
+ *  n_groups         >= 0 (0: exactly daa_batch_attention's plan)
+ *  workspace        at least daa_batch_attention_shared_prefix_workspace_size(...)
+ *                   bytes with the same groups
+ *  other arguments as daa_batch_attention / daa_append_attention.
+ * Errors: those of daa_batch_attention; DAA_ERR_INVALID_ARG for n_groups < 0
+ * or NULL group arrays with n_groups > 0; DAA_ERR_SHAPE for a group outside
+ * [0, batch], a decreasing indptr, a prefix length that is negative, not a
+ * multiple of page_size, or longer than some member's cached keys.
+ */
+size_t daa_batch_attention_shared_prefix_workspace_size(
+    const int32_t* h_qo_indptr, const int32_t* h_kv_indptr, const int32_t* h_last_page_len,
+    int32_t batch, const int32_t* h_prefix_indptr, const int32_t* h_prefix_len, int32_t n_groups,
+    daa_dims dims, daa_status* status);
+
+daa_status daa_batch_attention_shared_prefix(
+    const void* q, const void* kv_pages, const int32_t* qo_indptr, const int32_t* kv_indptr,
+    const int32_t* page_indices, const int32_t* last_page_len, const int32_t* h_qo_indptr,
+    const int32_t* h_kv_indptr, const int32_t* h_last_page_len, int32_t batch,
+    const int32_t* h_prefix_indptr, const int32_t* h_prefix_len, int32_t n_groups, int32_t causal,
+    float sm_scale, void* out, float* lse_out, void* workspace, size_t workspace_bytes,
+    daa_dims dims, void* stream);
+
+/* daa_append_attention (append, then attention, in one call) with the prefix
+ * groups of daa_batch_attention_shared_prefix. */
+daa_status daa_append_attention_shared_prefix(
+    const void* k_new, const void* v_new, const void* q, void* kv_pages, const int32_t* qo_indptr,
+    const int32_t* kv_indptr, const int32_t* page_indices, const int32_t* last_page_len,
+    const int32_t* h_qo_indptr, const int32_t* h_kv_indptr, const int32_t* h_last_page_len,
+    int32_t batch, const int32_t* h_prefix_indptr, const int32_t* h_prefix_len, int32_t n_groups,
+    int32_t causal, float sm_scale, void* out, float* lse_out, void* workspace,
+    size_t workspace_bytes, daa_dims dims, void* stream);
+
 /* Size of the device scratch array behind daa_batch_attention_noalloc (48 MiB). */
 #define DAA_NOALLOC_SCRATCH_BYTES (48u * 1024u * 1024u)
 

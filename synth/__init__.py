@@ -16,6 +16,7 @@ from .workloads import (  # noqa: F401
     make_workload,
     make_prompt_workload,
     make_random_workload,
+    make_prefix_groups_workload,
     make_shared_prefix_workload,
     make_tree_workload,
     random_tree,

@@ -221,6 +221,27 @@ class Workload:
         return self._gather(_KIND_Q, spans), self._gather(_KIND_K, spans), self._gather(_KIND_V, spans)
 
     # ------------------------------------------------------------ tree masks
+    def prefix_groups(self, k: int = 0):
+        """Prefix groups of step k, as the shared-prefix calls take them:
+        (indptr, prefix_len) int32 arrays, group i being requests
+        [indptr[i], indptr[i+1]).  A maximal run of consecutive requests whose
+        sequences share one prefix (same owner and length) is a group; the
+        requests between such runs form groups of prefix length 0."""
+        reqs = self.steps[k].requests
+        key = lambda r: (self.seqs[r.seq].prefix, self.seqs[r.seq].prefix_len)  # noqa: E731
+        indptr, plen = [0], []
+        i = 0
+        while i < len(reqs):
+            j = i + 1
+            shared = key(reqs[i])[0] >= 0
+            while j < len(reqs) and (key(reqs[j]) == key(reqs[i]) if shared
+                                     else key(reqs[j])[0] < 0):
+                j += 1
+            indptr.append(j)
+            plen.append(key(reqs[i])[1] if shared else 0)
+            i = j
+        return np.asarray(indptr, np.int32), np.asarray(plen, np.int32)
+
     def has_tree(self, k: int = 0) -> bool:
         return any(r.parents is not None for r in self.steps[k].requests)
 
@@ -343,6 +364,50 @@ def make_shared_prefix_workload(name, Hq, Hkv, d, P, seed, prefix_len, prompts, 
     reqs = [Request(1 + i, qo, kv) for i, (qo, kv) in enumerate(prompts)]
     reqs += [Request(1 + len(prompts) + j, 1, kv) for j, kv in enumerate(decodes)]
     return Workload(name, Hq, Hkv, d, P, num_pages, seed, seqs, [Step(reqs)], description=description)
+
+
+def make_prefix_groups_workload(name, Hq, Hkv, d, P, seed, layout, causal=True, description=""):
+    """One step over a batch whose requests hit several cached prefixes.
+
+    layout, in batch order: ("group", prefix_len, [(qo_len, kv_len), ...]) --
+    requests whose first prefix_len tokens (whole pages) are one shared prefix,
+    owned by a sequence that is not itself a request -- and ("solo", qo_len,
+    kv_len) requests with pages of their own."""
+    lengths, plan = [], []  # plan: (owner index or -1, prefix_len, qo, kv) per request
+    for ent in layout:
+        if ent[0] == "group":
+            _, pl, reqs = ent
+            assert pl % P == 0
+            owner = len(lengths)
+            lengths.append(pl)
+            for qo, kv in reqs:
+                plan.append((owner, pl, qo, kv))
+                lengths.append(kv - pl)
+        else:
+            _, qo, kv = ent
+            plan.append((-1, 0, qo, kv))
+            lengths.append(kv)
+    used = sum(-(-L // P) for L in lengths)
+    num_pages = _pool_pages(used)
+    pages = _alloc_pages(torch.Generator().manual_seed(seed + 7919), num_pages, lengths, P)
+    seqs, reqs, at = [], [], 0
+    for ent in layout:
+        if ent[0] == "group":
+            owner = len(seqs)
+            seqs.append(Seq(ent[1], pages[at]))
+            at += 1
+            for qo, kv in ent[2]:
+                own = np.concatenate([pages[owner], pages[at]]).astype(np.int32)
+                reqs.append(Request(len(seqs), qo, kv))
+                seqs.append(Seq(kv, own, owner, ent[1]))
+                at += 1
+        else:
+            reqs.append(Request(len(seqs), ent[1], ent[2]))
+            seqs.append(Seq(ent[2], pages[at]))
+            at += 1
+    wl = Workload(name, Hq, Hkv, d, P, num_pages, seed, seqs, [Step(reqs)], description=description)
+    wl.causal = causal
+    return wl
 
 
 def make_tree_workload(name, Hq, Hkv, d, P, seed, trees, decodes=(), prompts=(), num_pages=None,

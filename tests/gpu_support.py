@@ -26,15 +26,17 @@ def gpu_fill(wl, pool, device):
                   t.last_page_len)
 
 
-def gpu_step(wl, pool, k, device, with_lse=True, fused=False):
+def gpu_step(wl, pool, k, device, with_lse=True, fused=False, groups=False):
     """Append step k's new K/V and run attention: (out bf16 cpu, lse fp32 cpu).
     fused: one append_attention call instead of kv_append + batch_attention.
+    groups: pass the step's prefix groups (the shared-prefix calls).
     A step with draft trees appends, then attends under its tree mask."""
     st = wl.step_table(k)
     q, kn, vn = wl.step_inputs(k)
     tab = daa.PageTable.from_host(st["qo_indptr"], st["kv_indptr"], st["page_indices"],
                                   st["last_page_len"], device)
-    runner = daa.BatchAttention(tab, wl.num_qo_heads, pool, causal=wl.causal, sm_scale=wl.sm_scale)
+    runner = daa.BatchAttention(tab, wl.num_qo_heads, pool, causal=wl.causal, sm_scale=wl.sm_scale,
+                                prefix_groups=wl.prefix_groups(k) if groups else None)
     qd = q.to(device)
     lse = torch.full((q.shape[0], wl.num_qo_heads), float("nan"), device=device) if with_lse else None
     out = torch.full_like(qd, float("nan"))

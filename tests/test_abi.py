@@ -185,3 +185,48 @@ def test_tree_attention_rejects_before_any_launch(lib):
     assert call(dev(0x8000), 0) == -1
     assert call(dev(0x8002), 2) == -7
     assert call(dev(0x8000), 1) == -2      # 40 tokens need 2 words
+
+
+def _ws_groups(lib, qo, kv, last, dims, ind, plen, n=None):
+    st = ctypes.c_int32(0)
+    qo, kv, last = (np.asarray(x, np.int32) for x in (qo, kv, last))
+    ind = None if ind is None else np.asarray(ind, np.int32)
+    plen = None if plen is None else np.asarray(plen, np.int32)
+    p = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+    ng = (len(plen) if plen is not None else 0) if n is None else n
+    size = lib.daa_batch_attention_shared_prefix_workspace_size(
+        p(qo), p(kv), p(last), len(qo) - 1, p(ind), p(plen), ng, dims, ctypes.byref(st))
+    return size, st.value
+
+
+# three decodes (kv 300, 400, 500) that share a 256-token prefix; head_dim 128, GQA 8:1
+_G_QO, _G_KV, _G_LAST = [0, 1, 2, 3], [0, 19, 44, 76], [12, 16, 4]
+
+
+@pytest.mark.parametrize("ind,plen,n,expect", [
+    ([0, 3], [256], -1, -1),          # negative group count
+    (None, None, 1, -1),              # group arrays missing
+    ([0, 4], [256], None, -2),        # group past the batch
+    ([-1, 3], [256], None, -2),       # group before the batch
+    ([2, 1], [256], None, -2),        # decreasing indptr
+    ([0, 3], [250], None, -2),        # prefix not whole pages
+    ([0, 3], [-16], None, -2),        # negative prefix
+    ([0, 3], [304], None, -2),        # prefix longer than the first request's cached keys (299)
+])
+def test_shared_prefix_validation_rejects(lib, ind, plen, n, expect):
+    size, st = _ws_groups(lib, _G_QO, _G_KV, _G_LAST, _dims(Hq=8, Hkv=1, d=128, n=256), ind, plen, n)
+    assert st == expect and size == 0
+
+
+def test_shared_prefix_workspace(lib):
+    """No groups: the plain plan.  A 256-token prefix shared by three decodes:
+    one partial row per decode for the shared part plus one for its own part."""
+    dims = _dims(Hq=8, Hkv=1, d=128, n=256)
+    plain, st = _ws(lib, _G_QO, _G_KV, _G_LAST, dims)
+    assert st == 0
+    none, st = _ws_groups(lib, _G_QO, _G_KV, _G_LAST, dims, None, None, 0)
+    assert st == 0 and none == plain
+    small, st = _ws_groups(lib, _G_QO, _G_KV, _G_LAST, dims, [0, 3], [112])  # under one tile
+    assert st == 0 and small == plain
+    shared, st = _ws_groups(lib, _G_QO, _G_KV, _G_LAST, dims, [0, 3], [256])
+    assert st == 0 and shared >= plain + 2 * 3 * 8 * 128 * 4

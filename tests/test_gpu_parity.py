@@ -14,8 +14,9 @@ import pytest
 import torch
 
 import oracle
-from synth import (SENTINEL_BF16, make_prompt_workload, make_random_workload,
-                   make_shared_prefix_workload, make_tree_workload, make_workload, tree_mask_rows)
+from synth import (SENTINEL_BF16, make_prefix_groups_workload, make_prompt_workload,
+                   make_random_workload, make_shared_prefix_workload, make_tree_workload,
+                   make_workload, tree_mask_rows)
 from support import err_stats, oracle_pool, oracle_step
 
 pytestmark = pytest.mark.gpu
@@ -43,7 +44,7 @@ def _check(out, lse, ref, ref_lse, what):
     return mx, mean, rel
 
 
-def _run_both(wl, dev, sel_rows=None, compare_pool=True, fused=False):
+def _run_both(wl, dev, sel_rows=None, compare_pool=True, fused=False, groups=False):
     from gpu_support import compact, gpu_fill, gpu_step, new_pool, pool_bits
     cw, mapping = compact(wl)
     opool = oracle_pool(cw)
@@ -51,7 +52,7 @@ def _run_both(wl, dev, sel_rows=None, compare_pool=True, fused=False):
     gpu_fill(wl, gpool, dev)
     stats = []
     for k in range(len(wl.steps)):
-        out, lse = gpu_step(wl, gpool, k, dev, fused=fused)
+        out, lse = gpu_step(wl, gpool, k, dev, fused=fused, groups=groups)
         ref, ref_lse, _ = oracle_step(cw, opool, k, sel_rows=sel_rows)
         if sel_rows is not None:
             out, lse = out[sel_rows], lse[sel_rows]
@@ -259,6 +260,85 @@ def test_shared_prefix_pages(dev, case, fused):
     seed, Hq, Hkv, d, sp, prompts, decodes = case
     wl = make_shared_prefix_workload(f"shared_{seed}", Hq, Hkv, d, 16, seed, sp, prompts, decodes)
     _run_both(wl, dev, fused=fused)
+
+
+@pytest.mark.parametrize("case", SHARED, ids=lambda c: f"seed{c[0]}")
+def test_shared_prefix_groups_small_cases(dev, case):
+    """The same batches through the shared-prefix call: prefixes under one
+    128-key tile are planned as without groups, the 256-token one is attended
+    once for the group's decodes and verify request."""
+    seed, Hq, Hkv, d, sp, prompts, decodes = case
+    wl = make_shared_prefix_workload(f"shared_{seed}", Hq, Hkv, d, 16, seed, sp, prompts, decodes)
+    _run_both(wl, dev, groups=True)
+
+
+def _dec(kv0, n, step):
+    return [(1, kv0 + step * i) for i in range(n)]
+
+
+CASCADE = [
+    # (seed, Hq, Hkv, d, layout, causal).  Runs of decode / verify / short
+    # requests inside a group attend its shared 128-key tiles once; a prefill
+    # request in a group ends a run and keeps the prefix in its own items.
+    # g = 4, head_dim 128: decodes, a verify and a short request share a
+    # 1024-token prefix (pair kernel group items, tensor-core decode splits
+    # after the prefix); a prompt chunk splits the group into two runs; a second
+    # group whose prefix (400 tokens) is not whole tiles; solo requests between
+    (401, 32, 8, 128, [("group", 1024, _dec(1025, 12, 131) + [(7, 1500), (40, 2000), (200, 1400)]
+                        + _dec(3000, 5, 17)),
+                       ("solo", 1, 777), ("solo", 100, 900),
+                       ("group", 400, _dec(401, 4, 300) + [(9, 1000)])], True),
+    # g = 1 (MHA): CUDA-core decode splits after the prefix; 40 rows of one Q
+    # tile in the group item
+    (402, 16, 16, 128, [("group", 512, _dec(513, 40, 61))], True),
+    # g = 8, head_dim 64: group items on the single-CTA prefill kernel; a
+    # member whose only own key is its new token (kv = prefix + 1)
+    (403, 16, 2, 64, [("group", 384, _dec(385, 9, 203) + [(20, 700), (3, 387)])], True),
+    # g = 12: 30 decodes and a 10-token verify request over 1024 shared keys
+    (404, 12, 1, 128, [("solo", 1, 5000), ("group", 1024, _dec(1100, 30, 97) + [(10, 2500)])], True),
+    # not causal: every row sees all its keys, the shared ones included
+    (405, 32, 8, 128, [("group", 640, _dec(700, 8, 211) + [(12, 900), (64, 1200)])], False),
+    # a group of one member and a group with a prefix under one tile: no group
+    # items (the plan of the plain call)
+    (406, 32, 8, 128, [("group", 1024, [(1, 2000)]), ("group", 96, _dec(100, 6, 50))], True),
+]
+
+
+@pytest.mark.parametrize("case", CASCADE, ids=lambda c: f"seed{c[0]}")
+@pytest.mark.parametrize("fused", [False, True])
+def test_shared_prefix_groups(dev, case, fused):
+    """daa_batch_attention_shared_prefix / daa_append_attention_shared_prefix
+    ("Chunked prefill", #prefix-cache-interaction with the softmax_merge of
+    #correctness): outputs and LSE against the oracle, pool bit-exact."""
+    seed, Hq, Hkv, d, layout, causal = case
+    wl = make_prefix_groups_workload(f"groups_{seed}", Hq, Hkv, d, 16, seed, layout, causal=causal)
+    _run_both(wl, dev, fused=fused, groups=True)
+
+
+def test_shared_prefix_groups_match_plain_call(dev):
+    """The shared-prefix call and the plain call agree row by row (only the
+    fp32 summation order differs); groups that yield no group item give the
+    plain call's bits exactly."""
+    from gpu_support import gpu_fill, gpu_step, new_pool
+    for seed, exact in ((401, False), (406, True)):
+        case = next(c for c in CASCADE if c[0] == seed)
+        wl = make_prefix_groups_workload(f"groups_{seed}", *case[1:4], 16, seed, case[4])
+        outs = []
+        for groups in (False, True):
+            pool = new_pool(wl, dev)
+            gpu_fill(wl, pool, dev)
+            outs.append(gpu_step(wl, pool, 0, dev, groups=groups))
+        (oa, la), (ob, lb) = outs
+        if exact:
+            assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+            assert torch.equal(la, lb)
+        else:
+            assert (oa.float() - ob.float()).abs().max().item() <= 1e-2
+            assert (la - lb).abs().max().item() <= 1e-4
+
+
+def test_prefix_shared_workload_groups(dev):
+    _run_both(make_workload("prefix_shared"), dev, groups=True)
 
 
 TREES = [
