@@ -209,6 +209,8 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
     a.tree_mask = ls.tree_mask;
     a.mask_words = ls.mask_words;
     a.err = ls.err;
+    a.dec_counter = reinterpret_cast<int*>(ws + lay.off_sched);
+    a.sms = ls.sms;
     if (a.n_tiles > 0) {
       const bool quads = plan_prefill_quads(dims);
       if (run(kKernelPrefill, [&] {

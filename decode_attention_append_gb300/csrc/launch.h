@@ -87,6 +87,8 @@ struct PrefillArgs {
   const uint32_t* tree_mask;    // draft-tree mask rows [nnz_qo][mask_words], or null
   int mask_words;
   int* err;
+  int* dec_counter;             // zeroed work counter of the persistent decode kernel
+  int sms;                      // SMs of the device (persistent grid size)
 };
 // Rows of packed (token, head) a prefill tile holds.
 constexpr int kPrefillTileRows = 128;

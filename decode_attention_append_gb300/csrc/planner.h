@@ -77,9 +77,12 @@ struct PrefixGroups {
 // as three consecutive groups, each launched as its own kernel: prefill items,
 // short items (single-CTA kernel, head_dim 128 only; for head_dim 64 they join
 // the prefill group, which runs the same kernel), decode / verify items.
+// The plan ends with one zeroed 256-byte block (off_sched): the work counter
+// the persistent decode kernel takes its items from, reset by every call's
+// plan copy.
 struct PlanLayout {
   int n_units = 0, n_merges = 0, n_tiles = 0, n_dec_tiles = 0, n_short_tiles = 0, n_parts = 0;
-  size_t off_units = 0, off_merges = 0, off_tiles = 0, plan_bytes = 0;
+  size_t off_units = 0, off_merges = 0, off_tiles = 0, off_sched = 0, plan_bytes = 0;
   size_t off_part_o = 0, off_part_lse = 0, total = 0;
 };
 
@@ -359,6 +362,8 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
   off = plan_align_up(off + merges.size() * sizeof(MergeItem));
   lay.off_tiles = off;
   off = plan_align_up(off + tiles.size() * sizeof(PrefillTile));
+  lay.off_sched = off;
+  off += kPlanAlign;
   lay.plan_bytes = off;
   lay.off_part_o = off;
   off = plan_align_up(off + (size_t)lay.n_parts * d.num_qo_heads * d.head_dim * sizeof(float));

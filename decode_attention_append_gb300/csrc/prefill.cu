@@ -34,6 +34,8 @@
 // before the last PV so they cannot poison it.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "launch.h"
 #include "ptx.cuh"
 #include "softmax_tc.cuh"
@@ -414,6 +416,332 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Persistent decode / verify kernel: the items of the decode launch (key
+// splits of decode and small verify requests, one Q tile each) run on a grid
+// of two CTAs per SM, each CTA taking item after item from a work counter in
+// the plan's order (most keys first), so the last wave is never partly empty
+// and each CTA pays its set-up (barriers, TMEM, tensor-map prefetch) once.
+// Across items the pipeline does not drain: the producer streams the next
+// item's K/V tiles while the MMA issuer and the softmax warps finish the
+// current one.  Per CTA, ring stages, S buffers and the phases of s_full,
+// p_full and o_done follow running counts of ring items and key tiles over
+// all its items, exactly as within one item.  Hand-offs across items:
+//   item_full / item_empty [2]  item index from the producer to the MMA warp and
+//                               the four softmax warps (two slots)
+//   q_empty      the last S of an item is done: Q may be overwritten
+//   o_free       the epilogue of an item has read O: the next PV may overwrite
+// The MMA warp itself zeroes the stale rows of a request's last V tile once
+// it has landed, just before the PV that reads it.  (Taking the next item
+// from the counter a ring's depth before the current one ends was measured
+// slower: it unbalances the last items.)  Softmax
+// warps that hold no real row of an item skip it; warp 0 arrives on p_full
+// and o_free on their behalf.
+template <class C>
+struct PersistLayout {
+  static constexpr int RS = C::RS;
+  // barriers after C::OFF_BAR, then two item slots and the TMEM address
+  static constexpr int NBAR = 2 + 2 * RS + 2 + 2 + 1 + 1 + 2 + 2;
+  static constexpr int OFF_SLOT = C::OFF_BAR + NBAR * 8;
+  static constexpr int OFF_TMEM = OFF_SLOT + 8;
+  static constexpr int ALLOC = OFF_TMEM + 16 + 1024;
+  static_assert(C::NQX == 1, "one Q tile per item");
+  static_assert(ALLOC <= (C::MIN_BLOCKS == 1 ? 232448 : 115712), "shared memory budget");
+};
+
+template <class C, bool TREE>
+__device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
+  using PL = PersistLayout<C>;
+  constexpr int D = C::D, KT = C::KT, PPT = C::PPT, RS = C::RS;
+  const PrefillArgs& a = prm.a;
+  // work units: (item, kv head), item-major, so the heads of one item are
+  // consecutive and the plan's order (most keys first) is kept
+  const int n_units = a.n_dec_tiles * a.Hkv;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* ring_full = bars + 2;         // [RS]
+  uint64_t* ring_empty = ring_full + RS;  // [RS]
+  uint64_t* s_full = ring_empty + RS;     // [2]
+  uint64_t* p_full = s_full + 2;          // [2]
+  uint64_t* o_done = p_full + 2;
+  uint64_t* o_free = o_done + 1;
+  uint64_t* item_full = o_free + 1;       // [2]
+  uint64_t* item_empty = item_full + 2;   // [2]
+  volatile int* item_slot = reinterpret_cast<volatile int*>(smem + PL::OFF_SLOT);  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + PL::OFF_TMEM);
+
+  const int g = a.group;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    prefetch_tmap(&prm.tmap_q1);
+    prefetch_tmap(&prm.tmap_q);
+    prefetch_tmap(&prm.tmap_kv);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int i = 0; i < RS; ++i) {
+      mbar_init(&ring_full[i], 1);
+      mbar_init(&ring_empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], 4);
+      mbar_init(&item_full[b], 1);
+      mbar_init(&item_empty[b], 5);  // the MMA warp and the four softmax warps
+    }
+    mbar_init(o_done, 1);
+    mbar_init(o_free, 4);
+    fence_mbar_init();
+  }
+  if (warp == C::MMA) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (tid == 0) grid_dep_launch();
+
+  // Item geometry shared by the roles (same formulas as the one-item kernel).
+  struct Geo {
+    int n_kt, kt0, kend, npages_req, act;
+    bool last_partial, one_token;
+  };
+  auto geometry = [&](const PrefillTile& t) {
+    Geo q;
+    const int pos_first = t.kv_len - t.qo_len + t.tok0;
+    const int kv_end = a.causal ? min(t.kv_len, pos_first + t.ntok) : t.kv_len;
+    q.kend = min(kv_end, t.key_hi);
+    q.kt0 = t.key_lo / KT;
+    q.n_kt = (q.kend + KT - 1) / KT - q.kt0;
+    q.npages_req = (t.kv_len + kP - 1) / kP;
+    q.last_partial = t.kv_len - (q.kt0 + q.n_kt - 1) * KT < KT;
+    q.one_token = t.ntok == 1;
+    q.act = (t.ntok * g + 31) / 32;
+    return q;
+  };
+
+  if (warp == C::PRODUCER) {
+    // ------------------------------------------------------------ producer
+    int64_t r0 = 0;       // ring items issued before the current item
+    bool dep_waited = false;
+    for (int k = 0;; ++k) {
+      const int slot = k & 1;
+      int unit = n_units;
+      if (lane == 0) {
+        const bool ok = k < 2 || mbar_wait(&item_empty[slot], ((k >> 1) - 1) & 1, a.err);
+        unit = ok ? atomicAdd(a.dec_counter, 1) : n_units;
+        item_slot[slot] = unit;
+        mbar_arrive(&item_full[slot]);
+      }
+      unit = __shfl_sync(0xffffffffu, unit, 0);
+      if (unit >= n_units) break;
+      const PrefillTile tile = prm.tiles[unit / a.Hkv];
+      const int kvh = unit % a.Hkv;
+      const Geo ge = geometry(tile);
+      const int n_kt = ge.n_kt;
+      auto load_ids = [&](int i) -> int64_t {
+        if (i >= 2 * n_kt) return -1;
+        const int pg0 = (ge.kt0 + ring_tile(i, 1, n_kt)) * PPT;
+        const int np = min(PPT, ge.npages_req - pg0);
+        return lane < np ? (int64_t)__ldg(a.page_indices + tile.page_base + pg0 + lane) : -1;
+      };
+      int64_t pid = load_ids(0);
+      if (lane == 0) {
+        // Q, once the previous item's last S has read it
+        if (k > 0) mbar_wait(q_empty, (k - 1) & 1, a.err);
+        const int tpt = ge.one_token ? 1 : kRows / g;
+        const void* tmap_q = ge.one_token ? (const void*)&prm.tmap_q1 : (const void*)&prm.tmap_q;
+        mbar_arrive_expect_tx(q_full, (uint32_t)(tpt * g * D * 2));
+        for (int b = 0; b < C::KB; ++b)
+          tma_load_3d(smem + C::OFF_Q + b * (kRows * 128), tmap_q, b * 64, kvh * g,
+                      tile.q_row0 + tile.tok0, q_full);
+      }
+      const int first_new = tile.kv_len - tile.qo_len;
+      for (int i = 0; i < 2 * n_kt; ++i) {
+        const int64_t pid_next = load_ids(i + 1);
+        const int64_t rg = r0 + i;
+        const int st = (int)(rg % RS);
+        const uint32_t ph = (uint32_t)((rg / RS) & 1);
+        const bool is_v = ring_is_v(i, 1, n_kt);
+        const int pg0 = (ge.kt0 + ring_tile(i, 1, n_kt)) * PPT;
+        if (!dep_waited && (pg0 / PPT + 1) * KT > first_new) {
+          grid_dep_wait();
+          dep_waited = true;
+        }
+        const int np = min(PPT, ge.npages_req - pg0);
+        uint8_t* buf = smem + C::OFF_RING + st * C::T_BYTES;
+        if (lane == 0) {
+          if (rg >= RS) mbar_wait(&ring_empty[st], ph ^ 1u, a.err);
+          mbar_arrive_expect_tx(&ring_full[st], (uint32_t)(np * kP * D * 2));
+        }
+        __syncwarp();
+        if (lane < np) {
+          int64_t page = pid;
+          if (page < 0 || page >= a.num_pages) {
+            set_device_error(a.err, kDevErrPageRange);
+            page = 0;  // fetch a valid page instead; the output is undefined anyway
+          }
+          const int32_t slice = (int32_t)((page * 2 + (is_v ? 1 : 0)) * a.Hkv + kvh);
+#pragma unroll
+          for (int b = 0; b < C::KB; ++b)
+            tma_load_3d(buf + b * (KT * 128) + lane * (kP * 128), &prm.tmap_kv, b * 64, 0, slice,
+                        &ring_full[st]);
+        }
+        pid = pid_next;
+      }
+      r0 += 2 * n_kt;
+    }
+  } else if (warp == C::MMA) {
+    // ----------------------------------------------------------------- MMA
+    constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, KT, 0, 0);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 0, 1);
+    const uint32_t sQ = smem_u32(smem + C::OFF_Q);
+    const uint32_t sR = smem_u32(smem + C::OFF_RING);
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      const bool ok = mbar_wait(bar, parity, a.err);
+      __syncwarp();
+      return ok;
+    };
+    auto commit = [&](uint64_t* bar) {
+      if (elect_one()) tc_commit(bar);
+      __syncwarp();
+    };
+    auto issue_s = [&](uint32_t col, int st) {
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * (kRows * 128) + (k & 3) * 32;
+        const uint32_t koff = (k >> 2) * (KT * 128) + (k & 3) * 32;
+        const uint64_t da = desc_kmajor(sQ + off);
+        const uint64_t db = desc_kmajor(sR + st * C::T_BYTES + koff);
+        if (elect_one()) tc_mma_ss(tmem + col, da, db, idesc_s, k > 0 ? 1u : 0u);
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](uint32_t pcol, int st, bool accumulate) {
+#pragma unroll
+      for (int k = 0; k < KT / 16; ++k) {
+        const uint64_t db = desc_mnmajor(sR + st * C::T_BYTES + k * (16 * 128), KT * 128);
+        if (elect_one())
+          tc_mma_ts(tmem + C::O_COL, tmem + pcol + k * 8, db, idesc_o, (accumulate || k > 0) ? 1u : 0u);
+      }
+      __syncwarp();
+    };
+    int64_t r0 = 0;  // ring items consumed before the current item
+    int j0 = 0;      // key tiles before the current item
+    for (int k = 0;; ++k) {
+      const int slot = k & 1;
+      const bool ok = wait(&item_full[slot], (k >> 1) & 1);
+      const int unit = ok ? item_slot[slot] : n_units;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[slot]);
+      if (unit >= n_units) break;
+      const PrefillTile tile = prm.tiles[unit / a.Hkv];
+      const Geo ge = geometry(tile);
+      const int n_kt = ge.n_kt;
+      auto stage = [&](int i) { return (int)((r0 + i) % RS); };
+      auto phase = [&](int i) { return (uint32_t)(((r0 + i) / RS) & 1); };
+      auto sbuf = [&](int j) { return (uint32_t)((j0 + j) & 1); };
+      // S(j) into buffer (j0 + j) & 1: S of the first two tiles, then per tile
+      // PV(j) and S(j + 2) into the buffer PV(j) just read
+      auto s_tile = [&](int j) {
+        const int ik = ring_k_index(j);
+        wait(&ring_full[stage(ik)], phase(ik));
+        tc_fence_after();
+        issue_s(sbuf(j) * KT, stage(ik));
+        commit(&s_full[sbuf(j)]);
+        commit(&ring_empty[stage(ik)]);
+        if (j == n_kt - 1) commit(q_empty);  // Q may be replaced
+      };
+      wait(q_full, k & 1);
+      s_tile(0);
+      if (n_kt > 1) s_tile(1);
+      if (k > 0) wait(o_free, (k - 1) & 1);  // the previous epilogue has read O
+      for (int j = 0; j < n_kt; ++j) {
+        const int iv = ring_v_index(j, n_kt);
+        wait(&ring_full[stage(iv)], phase(iv));
+        if (j == n_kt - 1 && ge.last_partial) {
+          // V rows past the request's last key (stale slots, pages not loaded)
+          // must be finite for PV: zero them in shared memory
+          const int keys = tile.kv_len - (ge.kt0 + n_kt - 1) * KT;
+          uint8_t* buf = smem + C::OFF_RING + stage(iv) * C::T_BYTES;
+          const int nz = (KT - keys) * 8;  // 16-byte chunks per 64-column block
+          for (int x = lane; x < nz * C::KB; x += 32) {
+            const int b = x / nz, rem = x - b * nz;
+            const int r = keys + (rem >> 3), ch = rem & 7;
+            *reinterpret_cast<uint4*>(buf + b * (KT * 128) + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        wait(&p_full[sbuf(j)], ((j0 + j) >> 1) & 1);
+        tc_fence_after();
+        issue_pv(sbuf(j) * KT, stage(iv), j > 0);
+        commit(o_done);
+        commit(&ring_empty[stage(iv)]);
+        if (j + 2 < n_kt) s_tile(j + 2);
+      }
+      r0 += 2 * n_kt;
+      j0 += n_kt;
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int row = tid & 127;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    int j0 = 0;
+    for (int k = 0;; ++k) {
+      const int slot = k & 1;
+      const bool ok = mbar_wait(&item_full[slot], (k >> 1) & 1, a.err);
+      const int unit = ok ? item_slot[slot] : n_units;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[slot]);
+      if (unit >= n_units) break;
+      const PrefillTile tile = prm.tiles[unit / a.Hkv];
+      const int kvh = unit % a.Hkv;
+      const Geo ge = geometry(tile);
+      // warp 0 always holds a real row; it arrives for the warps that do not
+      const uint32_t cnt = warp == 0 ? (uint32_t)(5 - ge.act) : 1u;
+      if (warp < ge.act) {
+        const int tl = row / g;
+        const int qpos = tile.kv_len - tile.qo_len + tile.tok0 + tl;
+        const int row_end = min(a.causal ? min(qpos + 1, tile.kv_len) : tile.kv_len, ge.kend);
+        SoftmaxRowOut ro;
+        ro.q_row = tile.q_row0 + tile.tok0 + tl;
+        ro.hq = kvh * g + (row - tl * g);
+        ro.write = row < tile.ntok * g;
+        ro.part = tile.part >= 0 ? tile.part + (tile.tok0 + tl) * tile.part_stride : -1;
+        TreeRow tr;
+        tr.bits = TREE && ro.write ? a.tree_mask + (int64_t)ro.q_row * a.mask_words : nullptr;
+        tr.words = a.mask_words;
+        tr.draft0 = tile.kv_len - tile.qo_len;
+        tr.tok = tile.tok0 + tl;
+        tc_softmax_rows<D, KT, TREE>(a, tmem + lane_off, tmem + C::O_COL + lane_off, s_full, o_done,
+                                     0, true, ge.n_kt, ge.kt0, row_end, ro, tr,
+                                     [&](int b) {
+                                       if (lane == 0) mbar_arrive_cnt(&p_full[b], cnt);
+                                     },
+                                     j0);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cnt(o_free, cnt);  // O of this item has been read
+      }
+      j0 += ge.n_kt;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 // One entry per role, so profilers and traces tell the two apart.
 template <class C, bool TREE>
 __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
@@ -423,7 +751,7 @@ prefill_tc_kernel(const __grid_constant__ PrefillParams prm) {
 template <class C, bool TREE>
 __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 decode_tc_kernel(const __grid_constant__ PrefillParams prm) {
-  tc_attention<C, TREE>(prm);
+  tc_decode_persistent<C, TREE>(prm);
 }
 
 // --------------------------------------------------------------- host side
@@ -477,11 +805,20 @@ cudaError_t launch_tc(const PrefillArgs& a, const PrefillTile* tiles, int n_tile
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  // decode: a persistent grid of MIN_BLOCKS CTAs per SM (over all kv heads),
+  // each taking items from the work counter; otherwise one CTA per item
+  int alloc = C::ALLOC;
+  dim3 grid(n_tiles, a.Hkv);
+  if constexpr (kDecode) {
+    alloc = PersistLayout<C>::ALLOC;
+    const int64_t units = (int64_t)n_tiles * a.Hkv;
+    const int slots = C::MIN_BLOCKS * (a.sms > 0 ? a.sms : 1);
+    grid = dim3((unsigned)std::min<int64_t>(units, slots), 1);
+  }
   auto go = [&](void (*kern)(PrefillParams)) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, alloc);
     if (e != cudaSuccess) return e;
-    return launch_kernel(kern, dim3(n_tiles, a.Hkv), dim3(C::THREADS), C::ALLOC, stream,
-                         programmatic, prm);
+    return launch_kernel(kern, grid, dim3(C::THREADS), alloc, stream, programmatic, prm);
   };
   // the draft-tree variant only when the call carries a mask
   if constexpr (kDecode)

@@ -66,19 +66,22 @@ __device__ __forceinline__ uint32_t tree_hidden_word(const TreeRow& tr, int key0
 // buffer b sits at tmem_s0 + b * KT.  tmem_o: this warp's lanes of O.
 // dbuf: S alternates between buffers 0 and 1 per key tile (single Q tile);
 // otherwise buffer `sbuf` is used for every tile.
+// j0: key tiles this CTA's MMA issuer processed before this item (a persistent
+// CTA runs item after item; the S buffers and the phases of s_full and o_done
+// continue across items).  0 for a CTA that runs one item.
 template <int D, int KT, bool TREE, class ReleaseP>
 __device__ __forceinline__ void tc_softmax_rows(const PrefillArgs& a, uint32_t tmem_s0,
                                                 uint32_t tmem_o, uint64_t* s_full,
                                                 uint64_t* o_done_q, int sbuf, bool dbuf,
                                                 int n_kt, int kt0, int row_end,
                                                 const SoftmaxRowOut& ro, const TreeRow& tr,
-                                                ReleaseP&& release_p) {
+                                                ReleaseP&& release_p, int j0 = 0) {
   const float sc = a.sm_scale_log2;
   float m_run = -INFINITY, l_run = 0.f;
 
   for (int j = 0; j < n_kt; ++j) {
-    const int b = dbuf ? (j & 1) : sbuf;
-    const uint32_t ph = dbuf ? ((j >> 1) & 1) : (j & 1);
+    const int b = dbuf ? ((j0 + j) & 1) : sbuf;
+    const uint32_t ph = dbuf ? (((j0 + j) >> 1) & 1) : (j & 1);
     const uint32_t tmem_s = tmem_s0 + b * KT;
     mbar_wait(&s_full[b], ph, a.err);
     tc_fence_after();
@@ -148,7 +151,7 @@ __device__ __forceinline__ void tc_softmax_rows(const PrefillArgs& a, uint32_t t
 
     // O (TMEM) is rescaled once PV of the previous tile is done with it
     if (warp_rescale) {
-      mbar_wait(o_done_q, (j - 1) & 1, a.err);
+      mbar_wait(o_done_q, (j0 + j - 1) & 1, a.err);
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < D; c += 64) {  // two 32-column loads in flight per wait
@@ -168,7 +171,7 @@ __device__ __forceinline__ void tc_softmax_rows(const PrefillArgs& a, uint32_t t
     // o_done must never run two phases ahead of this thread's parity waits:
     // with S double-buffered, S(j) done only implies PV(j-2) done, so consume
     // the phase of PV(j-1) before PV(j) can be issued (normally no wait).
-    if (j > 0 && !warp_rescale) mbar_wait(o_done_q, (j - 1) & 1, a.err);
+    if (j > 0 && !warp_rescale) mbar_wait(o_done_q, (j0 + j - 1) & 1, a.err);
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -176,7 +179,7 @@ __device__ __forceinline__ void tc_softmax_rows(const PrefillArgs& a, uint32_t t
   }
 
   // ---- epilogue: O / l -> bf16 rows of out; lse
-  mbar_wait(o_done_q, (n_kt - 1) & 1, a.err);
+  mbar_wait(o_done_q, (j0 + n_kt - 1) & 1, a.err);
   tc_fence_after();
   const float inv = l_run > 0.f ? 1.f / l_run : 0.f;  // no visible key: o = 0, lse = -inf
   const bool partial = ro.part >= 0;  // key split: fp32 partial for softmax_merge
