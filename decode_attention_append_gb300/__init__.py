@@ -57,6 +57,11 @@ class _Dims(ctypes.Structure):
                 ("num_pages", ctypes.c_int64)]
 
 
+class PlanInfo(ctypes.Structure):
+    """daa_plan_info: the record of a plan uploaded by ``batch_attention_plan``."""
+    _fields_ = [("words", ctypes.c_int64 * 24)]
+
+
 def library_path() -> str:
     return _LIB_PATH
 
@@ -100,6 +105,15 @@ def load_library():
         lib.daa_append_attention_shared_prefix.argtypes = [
             vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, f32, vp, vp, vp, sz,
             _Dims, vp]
+        pinfo = ctypes.POINTER(PlanInfo)
+        lib.daa_batch_attention_plan.restype = i32
+        lib.daa_batch_attention_plan.argtypes = [vp, vp, vp, i32, vp, vp, i32, _Dims, vp, sz, pinfo, vp]
+        lib.daa_batch_attention_run.restype = i32
+        lib.daa_batch_attention_run.argtypes = [vp, vp, vp, vp, vp, vp, pinfo, i32, f32, vp, vp, vp, sz,
+                                                _Dims, vp]
+        lib.daa_append_attention_run.restype = i32
+        lib.daa_append_attention_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, pinfo, i32, f32, vp, vp,
+                                                 vp, sz, _Dims, vp]
         lib.daa_selftest_bounded_wait.restype = i32
         lib.daa_selftest_bounded_wait.argtypes = [ctypes.POINTER(i32)]
         lib.daa_device_error.restype = i32
@@ -408,6 +422,73 @@ def batch_attention_noalloc(q, kv_pages, qo_indptr, kv_indptr, page_indices, las
     return out
 
 
+def batch_attention_plan(h_qo_indptr, h_kv_indptr, h_last_page_len, num_qo_heads, kv_pages,
+                         workspace, prefix_groups=None, stream=None) -> PlanInfo:
+    """Plan a batch once (host) and copy the plan into ``workspace``; the
+    returned record is what ``batch_attention_run`` / ``append_attention_run``
+    take.  ``workspace`` must hold at least the size query's bytes (with the
+    same ``prefix_groups``)."""
+    lib = load_library()
+    _dev_bf16(kv_pages, "kv_pages")
+    hq, hk, hl = (_host_i32(x) for x in (h_qo_indptr, h_kv_indptr, h_last_page_len))
+    gi, gl, ng = _host_groups(prefix_groups) if prefix_groups is not None else (None, None, 0)
+    dims = _dims(kv_pages, num_qo_heads)
+    info = PlanInfo()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.daa_batch_attention_plan(_ptr(hq), _ptr(hk), _ptr(hl), len(hq) - 1, _ptr(gi), _ptr(gl),
+                                        ng, dims, _ptr(workspace), ws_bytes, ctypes.byref(info),
+                                        _stream(stream)), "batch_attention_plan")
+    return info
+
+
+def _run_args(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len, out, lse):
+    _dev_bf16(q, "q"), _dev_bf16(kv_pages, "kv_pages")
+    for n, t in (("qo_indptr", qo_indptr), ("kv_indptr", kv_indptr), ("page_indices", page_indices),
+                 ("last_page_len", last_page_len)):
+        _dev_i32(t, n)
+    if out is None:
+        out = torch.empty_like(q)
+    _dev_bf16(out, "out")
+    if lse is not None and not (lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous()):
+        raise TypeError("lse must be a contiguous fp32 CUDA tensor")
+    return out
+
+
+def batch_attention_run(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len, info,
+                        workspace, causal=True, sm_scale=None, out=None, lse=None, stream=None):
+    """Attention on a plan made by ``batch_attention_plan`` (kernels only)."""
+    lib = load_library()
+    out = _run_args(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len, out, lse)
+    if sm_scale is None:
+        sm_scale = 1.0 / float(q.shape[2]) ** 0.5
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.daa_batch_attention_run(_ptr(q), _ptr(kv_pages), _ptr(qo_indptr), _ptr(kv_indptr),
+                                       _ptr(page_indices), _ptr(last_page_len), ctypes.byref(info),
+                                       int(bool(causal)), float(sm_scale), _ptr(out), _ptr(lse),
+                                       _ptr(workspace), ws_bytes, _dims(kv_pages, q.shape[1]),
+                                       _stream(stream)), "batch_attention_run")
+    return out
+
+
+def append_attention_run(k_new, v_new, q, kv_pages, qo_indptr, kv_indptr, page_indices,
+                         last_page_len, info, workspace, causal=True, sm_scale=None, out=None,
+                         lse=None, stream=None):
+    """``append_attention`` on a plan made by ``batch_attention_plan``."""
+    lib = load_library()
+    _dev_bf16(k_new, "k_new"), _dev_bf16(v_new, "v_new")
+    out = _run_args(q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len, out, lse)
+    if sm_scale is None:
+        sm_scale = 1.0 / float(q.shape[2]) ** 0.5
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.daa_append_attention_run(_ptr(k_new), _ptr(v_new), _ptr(q), _ptr(kv_pages),
+                                        _ptr(qo_indptr), _ptr(kv_indptr), _ptr(page_indices),
+                                        _ptr(last_page_len), ctypes.byref(info), int(bool(causal)),
+                                        float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                        ws_bytes, _dims(kv_pages, q.shape[1]), _stream(stream)),
+           "append_attention_run")
+    return out
+
+
 @dataclass
 class PageTable:
     """Device int32 CSR page table plus its host mirror (numpy)."""
@@ -446,6 +527,16 @@ class BatchAttention:
                                                 table.h_last_page_len, prefix_groups,
                                                 num_qo_heads, hkv, d, p, n)
         self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=kv_pages.device)
+        self.info = None  # set by plan(): run() and step() then launch the kernels only
+
+    def plan(self, stream=None):
+        """Upload the batch's plan once; later run() / step() calls (e.g. one per
+        layer) reuse it until the next plan() or a tree-mask run."""
+        t = self.t
+        self.info = batch_attention_plan(t.h_qo_indptr, t.h_kv_indptr, t.h_last_page_len, self.Hq,
+                                         self.kv_pages, self.workspace,
+                                         prefix_groups=self.prefix_groups, stream=stream)
+        return self.info
 
     def append(self, k_new, v_new, stream=None):
         t = self.t
@@ -453,8 +544,13 @@ class BatchAttention:
                   t.last_page_len, stream=stream)
 
     def step(self, k_new, v_new, q, out=None, lse=None, stream=None):
-        """append + run in one call (``append_attention``)."""
+        """append + run in one call (``append_attention``, or ``append_attention_run``
+        on the stored plan)."""
         t = self.t
+        if self.info is not None:
+            return append_attention_run(k_new, v_new, q, self.kv_pages, t.qo_indptr, t.kv_indptr,
+                                        t.page_indices, t.last_page_len, self.info, self.workspace,
+                                        self.causal, self.sm_scale, out=out, lse=lse, stream=stream)
         return append_attention(k_new, v_new, q, self.kv_pages, t.qo_indptr, t.kv_indptr,
                                 t.page_indices, t.last_page_len, self.causal, self.sm_scale,
                                 out=out, lse=lse, workspace=self.workspace,
@@ -465,7 +561,12 @@ class BatchAttention:
         """Attention over the batch; with ``tree_mask``, under draft-tree masks
         (``batch_attention_tree``; the batch must be causal)."""
         t = self.t
+        if tree_mask is None and self.info is not None:
+            return batch_attention_run(q, self.kv_pages, t.qo_indptr, t.kv_indptr, t.page_indices,
+                                       t.last_page_len, self.info, self.workspace, self.causal,
+                                       self.sm_scale, out=out, lse=lse, stream=stream)
         if tree_mask is not None:
+            self.info = None  # the tree call plans into the workspace itself
             if self.prefix_groups is not None:
                 raise ValueError("tree masks and prefix groups are not combined")
             if not self.causal:

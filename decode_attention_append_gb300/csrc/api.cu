@@ -108,6 +108,17 @@ daa_status make_plan(const int32_t* qo, const int32_t* kv, const int32_t* last, 
 
 // Host prefix groups of a shared-prefix call, checked for null arrays and a
 // negative count (the planner checks them against the page table).
+// What daa_batch_attention_plan leaves in the caller's daa_plan_info: the
+// plan's layout in the workspace and the shapes it was made for.
+struct PlanRecord {
+  int64_t magic;
+  int64_t num_qo_heads, num_kv_heads, head_dim, page_size, num_pages;
+  int64_t batch, nnz_qo;
+  PlanLayout lay;
+};
+constexpr int64_t kPlanMagic = 0x4441415f504c414eLL;  // "DAA_PLAN"
+static_assert(sizeof(PlanRecord) <= sizeof(daa_plan_info), "daa_plan_info too small");
+
 daa_status make_groups(const int32_t* h_prefix_indptr, const int32_t* h_prefix_len,
                        int32_t n_groups, PrefixGroups& g) {
   if (n_groups < 0) return DAA_ERR_INVALID_ARG;
@@ -488,6 +499,131 @@ daa_status daa_append_attention_shared_prefix(
                         last_page_len, h_qo_indptr, h_kv_indptr, h_last_page_len, batch, causal,
                         sm_scale, out, lse_out, workspace, workspace_bytes, dims, stream, true,
                         nullptr, 0, &g);
+}
+
+daa_status daa_batch_attention_plan(const int32_t* h_qo_indptr, const int32_t* h_kv_indptr,
+                                    const int32_t* h_last_page_len, int32_t batch,
+                                    const int32_t* h_prefix_indptr, const int32_t* h_prefix_len,
+                                    int32_t n_groups, daa_dims dims, void* workspace,
+                                    size_t workspace_bytes, daa_plan_info* info, void* stream) {
+  if (!info) return DAA_ERR_INVALID_ARG;
+  std::memset(info, 0, sizeof(*info));
+  PrefixGroups g{};
+  daa_status st = make_groups(h_prefix_indptr, h_prefix_len, n_groups, g);
+  if (st != DAA_OK) return st;
+  HostPlan& pl = host_plan();
+  st = make_plan(h_qo_indptr, h_kv_indptr, h_last_page_len, batch, dims, num_sms(), pl,
+                 n_groups > 0 ? &g : nullptr);
+  if (st != DAA_OK) return st;
+  const PlanLayout& lay = pl.lay;
+  if (lay.total > 0) {
+    if (!workspace || workspace_bytes < lay.total) return DAA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DAA_ERR_ALIGNMENT;
+    std::vector<uint8_t>& host = staging();
+    if (host.size() < lay.plan_bytes) host.resize(lay.plan_bytes);
+    plan_stage(lay, pl.units, pl.merges, pl.tiles, host.data());
+    if (cudaMemcpyAsync(workspace, host.data(), lay.plan_bytes, cudaMemcpyHostToDevice,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return DAA_ERR_CUDA;
+  }
+  PlanRecord rec{};
+  rec.magic = kPlanMagic;
+  rec.num_qo_heads = dims.num_qo_heads;
+  rec.num_kv_heads = dims.num_kv_heads;
+  rec.head_dim = dims.head_dim;
+  rec.page_size = dims.page_size;
+  rec.num_pages = dims.num_pages;
+  rec.batch = batch;
+  rec.nnz_qo = batch > 0 ? h_qo_indptr[batch] : 0;
+  rec.lay = lay;
+  std::memcpy(info, &rec, sizeof(rec));
+  return DAA_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Shared body of the two run calls: check the plan record against the call,
+// then (fused) the append and the attention kernels.
+daa_status run_call(const void* k_new, const void* v_new, const void* q, const void* kv_pages,
+                    const int32_t* qo_indptr, const int32_t* kv_indptr,
+                    const int32_t* page_indices, const int32_t* last_page_len,
+                    const daa_plan_info* info, int32_t causal, float sm_scale, void* out,
+                    float* lse_out, void* workspace, size_t workspace_bytes, daa_dims dims,
+                    void* stream, bool fused) {
+  if (!info) return DAA_ERR_INVALID_ARG;
+  PlanRecord rec;
+  std::memcpy(&rec, info, sizeof(rec));
+  if (rec.magic != kPlanMagic || rec.num_qo_heads != dims.num_qo_heads ||
+      rec.num_kv_heads != dims.num_kv_heads || rec.head_dim != dims.head_dim ||
+      rec.page_size != dims.page_size || rec.num_pages != dims.num_pages)
+    return DAA_ERR_INVALID_ARG;
+  if (!(std::isfinite(sm_scale)) || !(sm_scale > 0.f)) return DAA_ERR_INVALID_ARG;
+  const PlanLayout& lay = rec.lay;
+  if (lay.n_units == 0 && lay.n_tiles == 0) return DAA_OK;
+  if (!q || !kv_pages || !qo_indptr || !kv_indptr || !page_indices || !last_page_len || !out)
+    return DAA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_pages) || !aligned16(out)) return DAA_ERR_ALIGNMENT;
+  if ((reinterpret_cast<uintptr_t>(lse_out) & 3) != 0) return DAA_ERR_ALIGNMENT;
+  if (fused) {
+    if (!k_new || !v_new) return DAA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return DAA_ERR_ALIGNMENT;
+  }
+  if (!workspace || workspace_bytes < lay.total) return DAA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DAA_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int nnz_qo = (int)rec.nnz_qo;
+  if (fused && nnz_qo > 0) {
+    int* err = device_error_word();
+    cudaError_t e = traced(kKernelAppend, s, [&] {
+      return launch_kv_append(k_new, v_new, const_cast<void*>(kv_pages), qo_indptr, page_indices,
+                              kv_indptr, last_page_len, (int)rec.batch, nnz_qo, dims.num_kv_heads,
+                              dims.head_dim, dims.num_pages, num_sms(), err, s);
+    });
+    if (e != cudaSuccess) return DAA_ERR_CUDA;
+  }
+  LaunchSet ls{};
+  ls.q = q;
+  ls.kv_pages = kv_pages;
+  ls.page_indices = page_indices;
+  ls.dims = dims;
+  ls.causal = causal;
+  ls.sm_scale = sm_scale;
+  ls.nnz_qo = nnz_qo;
+  ls.out = out;
+  ls.lse_out = lse_out;
+  ls.scratch = workspace;
+  ls.err = device_error_word();
+  ls.sms = num_sms();
+  return launch_all(ls, lay, s, /*trace=*/true, /*after_append=*/fused && nnz_qo > 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+daa_status daa_batch_attention_run(const void* q, const void* kv_pages, const int32_t* qo_indptr,
+                                   const int32_t* kv_indptr, const int32_t* page_indices,
+                                   const int32_t* last_page_len, const daa_plan_info* info,
+                                   int32_t causal, float sm_scale, void* out, float* lse_out,
+                                   void* workspace, size_t workspace_bytes, daa_dims dims,
+                                   void* stream) {
+  return run_call(nullptr, nullptr, q, kv_pages, qo_indptr, kv_indptr, page_indices,
+                  last_page_len, info, causal, sm_scale, out, lse_out, workspace, workspace_bytes,
+                  dims, stream, false);
+}
+
+daa_status daa_append_attention_run(const void* k_new, const void* v_new, const void* q,
+                                    void* kv_pages, const int32_t* qo_indptr,
+                                    const int32_t* kv_indptr, const int32_t* page_indices,
+                                    const int32_t* last_page_len, const daa_plan_info* info,
+                                    int32_t causal, float sm_scale, void* out, float* lse_out,
+                                    void* workspace, size_t workspace_bytes, daa_dims dims,
+                                    void* stream) {
+  return run_call(k_new, v_new, q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len,
+                  info, causal, sm_scale, out, lse_out, workspace, workspace_bytes, dims, stream,
+                  true);
 }
 
 daa_status daa_selftest_bounded_wait(int32_t* gave_up) {

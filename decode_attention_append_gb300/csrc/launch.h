@@ -87,7 +87,8 @@ struct PrefillArgs {
   const uint32_t* tree_mask;    // draft-tree mask rows [nnz_qo][mask_words], or null
   int mask_words;
   int* err;
-  int* dec_counter;             // zeroed work counter of the persistent decode kernel
+  int* dec_counter;             // persistent decode kernel: [0] work counter, [1] CTAs
+                                // finished; zero before a launch, reset to zero by it
   int sms;                      // SMs of the device (persistent grid size)
 };
 // Rows of packed (token, head) a prefill tile holds.

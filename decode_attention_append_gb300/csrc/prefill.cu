@@ -597,6 +597,13 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
       }
       r0 += 2 * n_kt;
     }
+    // the last CTA to finish resets the work counter (dec_counter[0]) and the
+    // finish count (dec_counter[1]) for the next launch on this plan: every
+    // CTA has taken its last ticket before it counts itself finished
+    if (lane == 0 && atomicAdd(a.dec_counter + 1, 1) == (int)(gridDim.x * gridDim.y) - 1) {
+      atomicExch(a.dec_counter, 0);
+      atomicExch(a.dec_counter + 1, 0);
+    }
   } else if (warp == C::MMA) {
     // ----------------------------------------------------------------- MMA
     constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, KT, 0, 0);

@@ -308,6 +308,64 @@ daa_status daa_append_attention_shared_prefix(
     int32_t causal, float sm_scale, void* out, float* lse_out, void* workspace,
     size_t workspace_bytes, daa_dims dims, void* stream);
 
+/*
+ * Plan once, run many times.  The plan of a batch -- how its requests are cut
+ * into work items ("Disaggregated prefill and decode", "Prefill vs decode
+ * performance": attention splits over requests and over kv_len) -- depends
+ * only on the page table's lengths.  In a model, every attention layer of a
+ * step reads the same table, so one plan serves all of them.
+ * daa_batch_attention_plan builds it on the host and copies it into the head
+ * of the workspace (one cudaMemcpyAsync on `stream`).  daa_batch_attention_run
+ * and daa_append_attention_run then launch only the kernels.  The outputs are
+ * bit-identical to daa_batch_attention / daa_append_attention on the same
+ * arguments, with and without prefix groups.
+ *
+ * daa_plan_info is plain data: the workspace layout and the shapes the plan
+ * was made for.  The plan stays valid while the workspace is not written by
+ * anything else (another plan, or a call that plans for itself) and the page
+ * table's lengths (qo_indptr, kv_indptr, last_page_len) are unchanged.  The
+ * pages themselves and q, k_new, v_new may change between runs.  Runs of one
+ * plan must not overlap on the GPU: they share the workspace's partials.
+ *
+ *  plan: the host arrays of daa_batch_attention (plus the prefix groups of
+ *        daa_batch_attention_shared_prefix; n_groups = 0 for none), the
+ *        workspace (at least the matching workspace-size query's bytes; may be
+ *        NULL when that size is 0), `info` (written), `stream`.
+ *  run:  the device arrays of daa_batch_attention, `info`, then causal,
+ *        sm_scale, out, lse_out, the workspace, the dims the plan was made
+ *        for, `stream`.  The page table passed must be the one planned.
+ * Errors: plan -- those of the size query; DAA_ERR_INVALID_ARG for a NULL info;
+ * DAA_ERR_WORKSPACE / DAA_ERR_ALIGNMENT for the workspace; DAA_ERR_CUDA if the
+ * copy fails.  run -- DAA_ERR_INVALID_ARG for an info that no plan call wrote or
+ * whose dims differ from `dims`; otherwise those of daa_batch_attention.
+ */
+typedef struct {
+  int64_t words[24];
+} daa_plan_info;
+
+daa_status daa_batch_attention_plan(const int32_t* h_qo_indptr, const int32_t* h_kv_indptr,
+                                    const int32_t* h_last_page_len, int32_t batch,
+                                    const int32_t* h_prefix_indptr, const int32_t* h_prefix_len,
+                                    int32_t n_groups, daa_dims dims, void* workspace,
+                                    size_t workspace_bytes, daa_plan_info* info, void* stream);
+
+daa_status daa_batch_attention_run(const void* q, const void* kv_pages, const int32_t* qo_indptr,
+                                   const int32_t* kv_indptr, const int32_t* page_indices,
+                                   const int32_t* last_page_len, const daa_plan_info* info,
+                                   int32_t causal, float sm_scale, void* out, float* lse_out,
+                                   void* workspace, size_t workspace_bytes, daa_dims dims,
+                                   void* stream);
+
+/* daa_append_attention on a plan: the append of k_new, v_new, then the
+ * attention kernels launched behind it (as daa_append_attention). */
+daa_status daa_append_attention_run(const void* k_new, const void* v_new, const void* q,
+                                    void* kv_pages, const int32_t* qo_indptr,
+                                    const int32_t* kv_indptr, const int32_t* page_indices,
+                                    const int32_t* last_page_len, const daa_plan_info* info,
+                                    int32_t causal, float sm_scale, void* out, float* lse_out,
+                                    void* workspace, size_t workspace_bytes, daa_dims dims,
+                                    void* stream);
+
 /* Size of the device scratch array behind daa_batch_attention_noalloc (48 MiB). */
 #define DAA_NOALLOC_SCRATCH_BYTES (48u * 1024u * 1024u)
 

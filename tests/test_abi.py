@@ -230,3 +230,30 @@ def test_shared_prefix_workspace(lib):
     assert st == 0 and small == plain
     shared, st = _ws_groups(lib, _G_QO, _G_KV, _G_LAST, dims, [0, 3], [256])
     assert st == 0 and shared >= plain + 2 * 3 * 8 * 128 * 4
+
+
+def test_plan_and_run_reject_before_any_launch(lib):
+    """daa_batch_attention_plan / _run: a plan record is required and checked
+    (magic, dims) on the host; a workspace smaller than the plan is refused."""
+    import decode_attention_append_gb300 as daa
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+    dev = lambda x: ctypes.c_void_p(x)  # noqa: E731  (never dereferenced: rejected first)
+    d = _dims(Hq=8, Hkv=1, d=128, n=256)
+    qo, kv, last = (np.asarray(x, np.int32) for x in (_G_QO, _G_KV, _G_LAST))
+    info = daa.PlanInfo()
+    plan = lambda ws, nbytes, inf: lib.daa_batch_attention_plan(  # noqa: E731
+        p(qo), p(kv), p(last), 3, None, None, 0, d, ws, nbytes, inf, None)
+    assert plan(dev(0x100000), 1 << 20, None) == -1            # no record
+    assert plan(dev(0x100000), 64, ctypes.byref(info)) == -6   # workspace too small
+    assert plan(dev(0x100080), 1 << 20, ctypes.byref(info)) == -7  # misaligned workspace
+    run = lambda inf, dims: lib.daa_batch_attention_run(  # noqa: E731
+        dev(0x10000), dev(0x20000), dev(0x30000), dev(0x40000), dev(0x50000), dev(0x60000), inf, 1,
+        0.125, dev(0x70000), None, dev(0x100000), 1 << 20, dims, None)
+    assert run(None, d) == -1
+    assert run(ctypes.byref(daa.PlanInfo()), d) == -1           # never written by a plan
+    # an empty batch plans without touching the device; its record runs as a no-op
+    e0 = np.zeros(1, np.int32)
+    assert lib.daa_batch_attention_plan(p(e0), p(e0), None, 0, None, None, 0, d, None, 0,
+                                        ctypes.byref(info), None) == 0
+    assert run(ctypes.byref(info), d) == 0
+    assert run(ctypes.byref(info), _dims(Hq=8, Hkv=1, d=64, n=256)) == -1  # other dims
