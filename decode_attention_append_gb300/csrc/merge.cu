@@ -9,6 +9,8 @@
 // partial row is read with coalesced 16-byte loads.  A row's parts are its
 // n_parts consecutive key-split slots plus, when it follows a shared prefix
 // attended once for a group of requests, the slot holding that prefix part.
+#include <type_traits>
+
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -20,37 +22,60 @@ constexpr int kMergeWarps = 4;
 template <int D>
 __global__ void __launch_bounds__(32 * kMergeWarps) softmax_merge_kernel(const MergeArgs a) {
   constexpr int EPL = D / 32;  // elements per lane
+  using Vec = typename std::conditional<EPL == 4, float4, float2>::type;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = blockIdx.y * kMergeWarps + warp;
-  grid_dep_wait();  // the partials come from the decode kernel launched before
-  if (hq >= a.Hq) return;
+  // the item comes from the plan, copied before any kernel of the call ran
   const MergeItem it = a.items[blockIdx.x];
+  grid_dep_wait();  // the partials come from the kernels launched before
+  if (hq >= a.Hq) return;
   const int n = it.n_parts + (it.extra >= 0 ? 1 : 0);
   auto slot = [&](int p) -> int64_t { return p < it.n_parts ? it.part_begin + p : it.extra; };
 
-  float M = -INFINITY;
-  for (int p = lane; p < n; p += 32) M = fmaxf(M, a.part_lse[slot(p) * a.Hq + hq]);
+  // lane l holds part p0 + l's LSE: the running max over all parts first
+  float lse_l = lane < n ? a.part_lse[slot(lane) * a.Hq + hq] : -INFINITY;
+  float M = lse_l;
+  for (int p = lane + 32; p < n; p += 32) M = fmaxf(M, a.part_lse[slot(p) * a.Hq + hq]);
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
 
+  // then, 32 parts at a time, each lane's weight, and the partial rows four at
+  // a time (independent loads in flight instead of one round trip per part)
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
   float wsum = 0.f;
-  for (int p = 0; p < n; ++p) {
-    const int64_t sl = slot(p);
-    const float w = ex2_approx(a.part_lse[sl * a.Hq + hq] - M);
-    wsum += w;
-    const float* po = a.part_o + (sl * a.Hq + hq) * D + lane * EPL;
-    if constexpr (EPL == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(po);
-      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
-      acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(po);
-      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+  for (int p0 = 0; p0 < n; p0 += 32) {
+    if (p0 > 0) lse_l = p0 + lane < n ? a.part_lse[slot(p0 + lane) * a.Hq + hq] : -INFINITY;
+    const float w_l = p0 + lane < n ? ex2_approx(lse_l - M) : 0.f;
+    wsum += w_l;
+    const int m = min(32, n - p0);
+    for (int q = 0; q < m; q += 4) {
+      Vec v[4];
+      float w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        w[u] = __shfl_sync(0xffffffffu, w_l, (q + u) & 31);
+        if (q + u < m) {
+          v[u] = *reinterpret_cast<const Vec*>(a.part_o + (slot(p0 + q + u) * a.Hq + hq) * D + lane * EPL);
+        } else {
+          w[u] = 0.f;
+          v[u] = Vec{};
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if constexpr (EPL == 4) {
+          acc[0] = fmaf(w[u], v[u].x, acc[0]); acc[1] = fmaf(w[u], v[u].y, acc[1]);
+          acc[2] = fmaf(w[u], v[u].z, acc[2]); acc[3] = fmaf(w[u], v[u].w, acc[3]);
+        } else {
+          acc[0] = fmaf(w[u], v[u].x, acc[0]); acc[1] = fmaf(w[u], v[u].y, acc[1]);
+        }
+      }
     }
   }
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, m);
   const float inv = 1.f / wsum;
   uint16_t* dst = a.out + ((int64_t)it.q_row * a.Hq + hq) * D + lane * EPL;
   if constexpr (EPL == 4) {
