@@ -18,6 +18,7 @@ namespace daa {
 namespace {
 
 constexpr int kMergeWarps = 4;
+constexpr int kMergeBatch = 4;  // partial rows loaded per batch (8 measured slower)
 
 template <int D>
 __global__ void __launch_bounds__(32 * kMergeWarps) softmax_merge_kernel(const MergeArgs a) {
@@ -39,8 +40,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps) softmax_merge_kernel(const M
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
 
-  // then, 32 parts at a time, each lane's weight, and the partial rows four at
-  // a time (independent loads in flight instead of one round trip per part)
+  // then, 32 parts at a time, each lane's weight, and the partial rows four
+  // at a time (independent loads in flight instead of one round trip per part)
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
@@ -50,11 +51,11 @@ __global__ void __launch_bounds__(32 * kMergeWarps) softmax_merge_kernel(const M
     const float w_l = p0 + lane < n ? ex2_approx(lse_l - M) : 0.f;
     wsum += w_l;
     const int m = min(32, n - p0);
-    for (int q = 0; q < m; q += 4) {
-      Vec v[4];
-      float w[4];
+    for (int q = 0; q < m; q += kMergeBatch) {
+      Vec v[kMergeBatch];
+      float w[kMergeBatch];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kMergeBatch; ++u) {
         w[u] = __shfl_sync(0xffffffffu, w_l, (q + u) & 31);
         if (q + u < m) {
           v[u] = *reinterpret_cast<const Vec*>(a.part_o + (slot(p0 + q + u) * a.Hq + hq) * D + lane * EPL);
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) softmax_merge_kernel(const M
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kMergeBatch; ++u) {
         if constexpr (EPL == 4) {
           acc[0] = fmaf(w[u], v[u].x, acc[0]); acc[1] = fmaf(w[u], v[u].y, acc[1]);
           acc[2] = fmaf(w[u], v[u].z, acc[2]); acc[3] = fmaf(w[u], v[u].w, acc[3]);

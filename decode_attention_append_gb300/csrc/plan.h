@@ -49,11 +49,9 @@ struct PrefillTile {
   int32_t key_lo;     // first key (multiple of 128)
   int32_t key_hi;     // one past the last key
   int32_t part;       // partial slot, or -1: write out / lse_out directly
-  int32_t work;       // planner's sort key (keys read)
   int32_t part_stride;  // key-split multi-token item: token t of the request writes its
                         // partial to slot part + t * part_stride
   int32_t kind;       // kTileRequest, or kTilePrefixGroup (see below)
-  int32_t pad0, pad1, pad2;
 };
 
 // Tile kinds.  A prefix-group item attends the query rows of several
@@ -61,15 +59,16 @@ struct PrefillTile {
 // (read once for all of them): q_row0 / qo_len span the group's rows,
 // kv_len = key_hi = the shared keys (a multiple of 128), page_base = the first
 // request's page list; every row sees every key (the prefix precedes all new
-// tokens), and each row writes its partial to the slot the row-to-slot table
-// of the plan gives.
+// tokens), and row t of the group writes its partial to slot part + t.
+// The plan is copied to the device every call, so the item stays small: a
+// plan under 64 KB is copied inline with the launches.
 
 static_assert(sizeof(DecodeUnit) == 32, "DecodeUnit layout");
 static_assert(sizeof(MergeItem) == 16, "MergeItem layout");
 constexpr int32_t kTileRequest = 0;
 constexpr int32_t kTilePrefixGroup = 1;
 
-static_assert(sizeof(PrefillTile) == 64, "PrefillTile layout");
+static_assert(sizeof(PrefillTile) == 48, "PrefillTile layout");
 
 // Kernel ids reported by the tracer.
 enum KernelId : int32_t {

@@ -186,10 +186,16 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
   // split sizes (pages).  CUDA-core splits: about twenty per SM (ten per CTA
   // slot), so the longest split is a small fraction of the pass while the
   // split-KV partials stay few.  Tensor-core splits: whole 128-key tiles, about
-  // four items per SM.  Both targets were measured on GB300 (MHA decode: 20
-  // per SM 7% faster than 40 or 80; tensor-core items: 4 per SM within a few
-  // percent of the best for decode-heavy, mixed and shared-prefix batches).
-  int64_t split_tc = (page_heads + (int64_t)sms * 4 - 1) / ((int64_t)sms * 4);
+  // four items per SM, or six when prefill items run beside them: those hold
+  // their SMs for tens of microseconds, the decode CTAs that start after them
+  // take items late, and shorter items keep that tail short.  Targets measured
+  // on GB300 (MHA decode: 20 per SM 7% faster than 40 or 80; persistent
+  // tensor-core decode: 4 per SM best for the GQA decode shard, 6 per SM 9%
+  // faster than 4 for the chunked-prefill mixed batch).
+  bool prefill_beside = groups && groups->n > 0;  // prefix-group items join the prefill launch
+  for (int r = 0; r < batch && !prefill_beside; ++r) prefill_beside = qo[r + 1] - qo[r] > short_max;
+  const int64_t tc_per_sm = prefill_beside ? 6 : 4;
+  int64_t split_tc = (page_heads + (int64_t)sms * tc_per_sm - 1) / ((int64_t)sms * tc_per_sm);
   split_tc = (split_tc + 7) / 8 * 8;
   split_tc = std::max<int64_t>(32, std::min<int64_t>(2048, split_tc));
   int64_t split_cc = (page_heads + (int64_t)sms * 20 - 1) / ((int64_t)sms * 20);
@@ -212,22 +218,18 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
       t.kv_len = run.sk;
       t.page_base = kv[run.r0];
       t.tok0 = t0;
-      int ntiles;
       if (quads) {
         t.ntok = std::min(4 * tpt, rows - t0);
         t.ntok1 = 0;
-        ntiles = (t.ntok + tpt - 1) / tpt;
       } else {
         t.ntok = std::min(tpt, rows - t0);
         t.ntok1 = t.ntok == tpt ? std::max(0, std::min(tpt, rows - t0 - tpt)) : 0;
-        ntiles = t.ntok1 > 0 ? 2 : 1;
       }
       t.key_lo = 0;
       t.key_hi = run.sk;
       t.part = run.slot0;
       t.part_stride = 1;
       t.kind = kTilePrefixGroup;
-      t.work = run.sk * ntiles;
       if (!tiles.push_back(t)) return DAA_ERR_WORKSPACE;
     }
   }
@@ -277,7 +279,6 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
         t.key_hi = hi;
         t.part = part0 >= 0 ? part0 + s : -1;
         t.part_stride = nsplit;
-        t.work = (hi - lo) * (t.ntok1 > 0 ? 2 : 1);
         if (!tiles.push_back(t)) return DAA_ERR_WORKSPACE;
       } else {
         DecodeUnit u{};
@@ -312,22 +313,16 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
       t.kv_len = kv_len;
       t.page_base = kv[r];
       t.tok0 = t0;
-      int ntiles;
       if (quads) {
         t.ntok = std::min(4 * tpt, nq - t0);
         t.ntok1 = 0;
-        ntiles = (t.ntok + tpt - 1) / tpt;
       } else {
         t.ntok = std::min(tpt, nq - t0);
         t.ntok1 = t.ntok == tpt ? std::max(0, std::min(tpt, nq - t0 - tpt)) : 0;
-        ntiles = t.ntok1 > 0 ? 2 : 1;
       }
       t.key_lo = 0;
       t.key_hi = kv_len;
       t.part = -1;
-      // keys read by the item's last token, counted once per Q tile
-      const int toks = quads ? t.ntok : t.ntok + t.ntok1;
-      t.work = std::min(kv_len, kv_len - nq + t0 + toks) * ntiles;
       if (!tiles.push_back(t)) return DAA_ERR_WORKSPACE;
     }
   }
@@ -339,10 +334,21 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
     if (t.qo_len <= verify_max) return 2;
     return quads && t.qo_len <= short_max ? 1 : 0;
   };
+  // work of an item: keys read by its last row, counted once per Q tile
+  auto work = [=](const PrefillTile& t) -> int64_t {
+    const bool pair = quads && group(t) == 0;  // up to four tiles on a CTA pair
+    const int toks = t.ntok + t.ntok1;
+    const int ntiles = pair ? (toks + tpt - 1) / tpt : (t.ntok1 > 0 ? 2 : 1);
+    const int end = t.kind == kTilePrefixGroup
+                        ? t.key_hi
+                        : std::min(t.key_hi, t.kv_len - t.qo_len + t.tok0 + toks);
+    return (int64_t)(end - t.key_lo) * ntiles;
+  };
   std::sort(tiles.data(), tiles.data() + tiles.size(), [&](const PrefillTile& x, const PrefillTile& y) {
     const int gx = group(x), gy = group(y);
     if (gx != gy) return gx < gy;
-    if (x.work != y.work) return x.work > y.work;
+    const int64_t wx = work(x), wy = work(y);
+    if (wx != wy) return wx > wy;
     if (x.q_row0 != y.q_row0) return x.q_row0 < y.q_row0;
     return x.tok0 != y.tok0 ? x.tok0 < y.tok0 : x.key_lo < y.key_lo;
   });
