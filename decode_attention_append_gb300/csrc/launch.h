@@ -88,7 +88,10 @@ struct PrefillArgs {
   int mask_words;
   int* err;
   int* dec_counter;             // persistent decode kernel: [0] work counter, [1] CTAs
-                                // finished; zero before a launch, reset to zero by it
+                                // finished; from [4], arrival counters of the merges
+                                // it runs; zero before a launch, reset to zero by it
+  const MergeItem* merges;      // the plan's merge items
+  int n_kernel_merges;          // merge items run by the merge kernel (the first ones)
   int sms;                      // SMs of the device (persistent grid size)
 };
 // Rows of packed (token, head) a prefill tile holds.
