@@ -221,8 +221,6 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
     a.mask_words = ls.mask_words;
     a.err = ls.err;
     a.dec_counter = reinterpret_cast<int*>(ws + lay.off_sched);
-    a.merges = reinterpret_cast<const MergeItem*>(ws + lay.off_merges);
-    a.n_kernel_merges = lay.n_kernel_merges;
     a.sms = ls.sms;
     if (a.n_tiles > 0) {
       const bool quads = plan_prefill_quads(dims);
@@ -268,10 +266,10 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
       return DAA_ERR_CUDA;
     programmatic = !(trace && tracing());
   }
-  if (lay.n_kernel_merges > 0) {  // the others are merged inside the decode kernel
+  if (lay.n_merges > 0) {
     MergeArgs m{};
     m.items = reinterpret_cast<const MergeItem*>(ws + lay.off_merges);
-    m.n_items = lay.n_kernel_merges;
+    m.n_items = lay.n_merges;
     m.Hq = dims.num_qo_heads;
     m.head_dim = dims.head_dim;
     m.part_o = part_o;

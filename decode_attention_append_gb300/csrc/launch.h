@@ -88,10 +88,7 @@ struct PrefillArgs {
   int mask_words;
   int* err;
   int* dec_counter;             // persistent decode kernel: [0] work counter, [1] CTAs
-                                // finished; from [4], arrival counters of the merges
-                                // it runs; zero before a launch, reset to zero by it
-  const MergeItem* merges;      // the plan's merge items
-  int n_kernel_merges;          // merge items run by the merge kernel (the first ones)
+                                // finished; zero before a launch, reset to zero by it
   int sms;                      // SMs of the device (persistent grid size)
 };
 // Rows of packed (token, head) a prefill tile holds.

@@ -92,7 +92,7 @@ extern "C" daa_status daa_batch_attention_noalloc(
   PlanLayout lay;
   // the same plan as daa_batch_attention, built in the static containers
   st = plan_batch(h_qo_indptr, h_kv_indptr, h_last_page_len, batch, dims, sms, g_units, g_merges,
-                  g_tiles, lay, /*groups=*/nullptr, /*fuse_merges=*/false);
+                  g_tiles, lay);
   if (st != DAA_OK) return st;
   if (lay.n_units == 0 && lay.n_tiles == 0) return DAA_OK;
   if (lay.total > kScratchBytes) return DAA_ERR_WORKSPACE;

@@ -52,8 +52,6 @@ struct PrefillTile {
   int32_t part_stride;  // key-split multi-token item: token t of the request writes its
                         // partial to slot part + t * part_stride
   int32_t kind;       // kTileRequest, or kTilePrefixGroup (see below)
-  int32_t merge0 = -1;  // decode launch: merge item of the request's token 0 when the
-                        // persistent decode kernel merges its rows itself, else -1
 };
 
 // Tile kinds.  A prefix-group item attends the query rows of several
@@ -70,7 +68,7 @@ static_assert(sizeof(MergeItem) == 16, "MergeItem layout");
 constexpr int32_t kTileRequest = 0;
 constexpr int32_t kTilePrefixGroup = 1;
 
-static_assert(sizeof(PrefillTile) == 52, "PrefillTile layout");
+static_assert(sizeof(PrefillTile) == 48, "PrefillTile layout");
 
 // Kernel ids reported by the tracer.
 enum KernelId : int32_t {

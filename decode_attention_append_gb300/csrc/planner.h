@@ -80,19 +80,11 @@ struct PrefixGroups {
 // The plan ends with one zeroed 256-byte block (off_sched): the work counter
 // the persistent decode kernel takes its items from, reset by every call's
 // plan copy.
-// Merge items [0, n_kernel_merges) are run by the softmax_merge kernel; the
-// rest belong to requests of the persistent decode launch, whose last unit of
-// a (row, kv head) merges it in place: one arrival counter per such (merge
-// item, kv head) follows the two sched words, at off_sched + 16.
 struct PlanLayout {
   int n_units = 0, n_merges = 0, n_tiles = 0, n_dec_tiles = 0, n_short_tiles = 0, n_parts = 0;
-  int n_kernel_merges = 0;
   size_t off_units = 0, off_merges = 0, off_tiles = 0, off_sched = 0, plan_bytes = 0;
   size_t off_part_o = 0, off_part_lse = 0, total = 0;
 };
-// Arrival counters of in-kernel merges stay under this size (else the kernel
-// merges them all): the plan is copied every call.
-constexpr size_t kMaxMergeCounterBytes = 16384;
 
 // Vec: push_back(const T&) -> bool (false when full), size(), data(), clear().
 // With `groups`: within each group, every maximal run of consecutive requests
@@ -104,13 +96,10 @@ constexpr size_t kMaxMergeCounterBytes = 16384;
 // their own items: their Q tiles are full already, so sharing would only add
 // partials to merge.  Without groups the plan allocates nothing beyond the
 // Vecs.
-// fuse_merges: let the persistent decode kernel merge the rows of its
-// requests (the no-allocation entry point keeps every merge in the kernel).
 template <class UnitVec, class MergeVec, class TileVec>
 daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last, int32_t batch,
                       const daa_dims& d, int sms, UnitVec& units, MergeVec& merges,
-                      TileVec& tiles, PlanLayout& lay, const PrefixGroups* groups = nullptr,
-                      bool fuse_merges = true) {
+                      TileVec& tiles, PlanLayout& lay, const PrefixGroups* groups = nullptr) {
   units.clear();
   merges.clear();
   tiles.clear();
@@ -246,26 +235,12 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
   }
 
   // decode (qo_len 1), verify (qo_len 2 .. verify_max) and short
-  // (verify_max < qo_len <= short_max) requests: key-split items.  Pass 0:
-  // requests whose partials the merge kernel combines; pass 1: requests of
-  // the persistent decode launch, which merges them itself (their merge items
-  // come last)
-  int64_t fused_rows = 0;  // merge items pass 1 would add
-  for (int r = 0; r < batch && fuse_merges; ++r) {
-    const int nq = qo[r + 1] - qo[r];
-    if (nq >= 1 && nq <= verify_max && (tc_decode || nq > 1)) fused_rows += nq;
-  }
-  const bool fuse = fuse_merges &&
-                    fused_rows * d.num_kv_heads * (int64_t)sizeof(int32_t) <= (int64_t)kMaxMergeCounterBytes;
-  for (int pass = 0; pass < 2; ++pass) {
-  if (pass == 1) lay.n_kernel_merges = (int)merges.size();
+  // (verify_max < qo_len <= short_max) requests: key-split items
   for (int r = 0; r < batch; ++r) {
     const int nq = qo[r + 1] - qo[r];
     if (nq < 1 || nq > short_max) continue;
     const bool is_short = nq > verify_max;
     const bool on_tc = tc_decode || nq > 1;
-    const bool in_kernel = fuse && on_tc && !is_short;  // merged by the decode kernel
-    if ((pass == 1) != in_kernel) continue;
     const int64_t split = is_short ? split_short : on_tc ? split_tc : split_cc;
     const int np = kv[r + 1] - kv[r];
     const int kv_len = (np - 1) * P + last[r];
@@ -278,10 +253,9 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
     // partial slots: token t of split s at part0 + t * nsplit + s, so each
     // token's splits are consecutive for its softmax_merge item (which also
     // takes the row's prefix partial when sk > 0)
-    int part0 = -1, merge0 = -1;
+    int part0 = -1;
     if (nsplit > 1 || sk > 0) {
       const int32_t pbase = sk > 0 ? shared_slot[r] : -1;
-      merge0 = in_kernel ? (int)merges.size() : -1;
       for (int t = 0; t < nq; ++t)
         if (!merges.push_back(MergeItem{qo[r] + t, lay.n_parts + t * nsplit, nsplit,
                                         sk > 0 ? pbase + t : -1}))
@@ -305,7 +279,6 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
         t.key_hi = hi;
         t.part = part0 >= 0 ? part0 + s : -1;
         t.part_stride = nsplit;
-        t.merge0 = merge0;
         if (!tiles.push_back(t)) return DAA_ERR_WORKSPACE;
       } else {
         DecodeUnit u{};
@@ -318,7 +291,6 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
         if (!units.push_back(u)) return DAA_ERR_WORKSPACE;
       }
     }
-  }
   }
   // longest splits first (only the last split of a request is shorter)
   std::sort(units.data(), units.data() + units.size(), [](const DecodeUnit& x, const DecodeUnit& y) {
@@ -397,8 +369,7 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
   lay.off_tiles = off;
   off = plan_align_up(off + tiles.size() * sizeof(PrefillTile));
   lay.off_sched = off;
-  off = plan_align_up(off + 16 + (size_t)(merges.size() - lay.n_kernel_merges) * d.num_kv_heads *
-                                     sizeof(int32_t));
+  off += kPlanAlign;
   lay.plan_bytes = off;
   lay.off_part_o = off;
   off = plan_align_up(off + (size_t)lay.n_parts * d.num_qo_heads * d.head_dim * sizeof(float));

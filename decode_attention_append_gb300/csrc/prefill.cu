@@ -37,7 +37,6 @@
 #include <algorithm>
 
 #include "launch.h"
-#include "merge.cuh"
 #include "ptx.cuh"
 #include "softmax_tc.cuh"
 
@@ -442,9 +441,9 @@ template <class C>
 struct PersistLayout {
   static constexpr int RS = C::RS;
   // barriers after C::OFF_BAR, then two item slots and the TMEM address
-  static constexpr int NBAR = 2 + 2 * RS + 2 + 2 + 1 + 1 + 2 + 2 + 1;
-  static constexpr int OFF_SLOT = C::OFF_BAR + NBAR * 8;  // item slots [2], merge flags
-  static constexpr int OFF_TMEM = OFF_SLOT + 16;
+  static constexpr int NBAR = 2 + 2 * RS + 2 + 2 + 1 + 1 + 2 + 2;
+  static constexpr int OFF_SLOT = C::OFF_BAR + NBAR * 8;
+  static constexpr int OFF_TMEM = OFF_SLOT + 8;
   static constexpr int ALLOC = OFF_TMEM + 16 + 1024;
   static_assert(C::NQX == 1, "one Q tile per item");
   static_assert(ALLOC <= (C::MIN_BLOCKS == 1 ? 232448 : 115712), "shared memory budget");
@@ -472,9 +471,7 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
   uint64_t* o_free = o_done + 1;
   uint64_t* item_full = o_free + 1;       // [2]
   uint64_t* item_empty = item_full + 2;   // [2]
-  uint64_t* msync = item_empty + 2;       // the four softmax warps, around in-kernel merges
   volatile int* item_slot = reinterpret_cast<volatile int*>(smem + PL::OFF_SLOT);  // [2]
-  volatile uint32_t* merge_flags = reinterpret_cast<volatile uint32_t*>(smem + PL::OFF_SLOT + 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + PL::OFF_TMEM);
 
   const int g = a.group;
@@ -498,7 +495,6 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
     }
     mbar_init(o_done, 1);
     mbar_init(o_free, 4);
-    mbar_init(msync, 4);
     fence_mbar_init();
   }
   if (warp == C::MMA) {
@@ -705,7 +701,6 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
     const int row = tid & 127;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     int j0 = 0;
-    uint32_t mph = 0;  // msync phases passed
     for (int k = 0;; ++k) {
       const int slot = k & 1;
       const bool ok = mbar_wait(&item_full[slot], (k >> 1) & 1, a.err);
@@ -741,44 +736,6 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cnt(o_free, cnt);  // O of this item has been read
-      }
-      if (tile.merge0 >= 0) {
-        // the rows of this request are merged here ("Chunked prefill",
-        // #correctness: softmax_merge of the key splits' partials): each of
-        // its units counts itself in per (row, kv head); the last to arrive
-        // merges the row's g heads, one warp per head
-        if (warp < ge.act) __threadfence();  // this thread's partial row, for other CTAs
-        auto sync4 = [&]() {  // the four softmax warps (bounded, like every wait here)
-          __syncwarp();
-          if (lane == 0) mbar_arrive(msync);
-          mbar_wait(msync, mph & 1, a.err);
-          ++mph;
-          __syncwarp();
-        };
-        sync4();
-        if (tid == 0) {
-          uint32_t mine = 0;
-          for (int t = 0; t < tile.ntok; ++t) {
-            const int mi = tile.merge0 + t;
-            int* c = a.dec_counter + 4 + (int64_t)(mi - a.n_kernel_merges) * a.Hkv + kvh;
-            if (atomicAdd(c, 1) == a.merges[mi].n_parts - 1) {
-              mine |= 1u << t;
-              atomicExch(c, 0);  // ready for the next run of this plan
-            }
-          }
-          __threadfence();
-          *merge_flags = mine;
-        }
-        sync4();
-        const uint32_t mine = *merge_flags;
-        for (int t = 0; t < tile.ntok; ++t) {
-          if (!((mine >> t) & 1u)) continue;
-          const MergeItem it = a.merges[tile.merge0 + t];
-          if (it.extra >= 0) grid_dep_wait();  // the prefix partial: the prefill launch's
-          for (int h = warp; h < g; h += 4)
-            merge_row_head<D>(it, a.Hq, kvh * g + h, a.part_o, a.part_lse, a.out, a.lse_out, lane);
-        }
-        sync4();  // merge_flags is rewritten for the next unit
       }
       j0 += ge.n_kt;
     }

@@ -11,9 +11,9 @@
 // (n_groups = -1: the plain plan).  Output, per case: "S status", then
 //   "U q_row page_base tok_begin tok_end kv_len part" per decode unit,
 //   "M q_row part_begin n_parts extra" per merge item,
-//   "T q_row0 qo_len kv_len page_base tok0 ntok ntok1 key_lo key_hi part part_stride kind merge0"
+//   "T q_row0 qo_len kv_len page_base tok0 ntok ntok1 key_lo key_hi part part_stride kind"
 //   per tensor-core item (launch order),
-//   "L n_units n_merges n_tiles n_dec_tiles n_short_tiles n_parts n_kernel_merges", and "E".
+//   "L n_units n_merges n_tiles n_dec_tiles n_short_tiles n_parts", and "E".
 #include <cstdio>
 #include <vector>
 
@@ -73,11 +73,11 @@ int main() {
     for (const auto& m : merges.v)
       std::printf("M %d %d %d %d\n", m.q_row, m.part_begin, m.n_parts, m.extra);
     for (const auto& t : tiles.v)
-      std::printf("T %d %d %d %d %d %d %d %d %d %d %d %d %d\n", t.q_row0, t.qo_len, t.kv_len,
+      std::printf("T %d %d %d %d %d %d %d %d %d %d %d %d\n", t.q_row0, t.qo_len, t.kv_len,
                   t.page_base, t.tok0, t.ntok, t.ntok1, t.key_lo, t.key_hi, t.part, t.part_stride,
-                  t.kind, t.merge0);
-    std::printf("L %d %d %d %d %d %d %d\nE\n", lay.n_units, lay.n_merges, lay.n_tiles,
-                lay.n_dec_tiles, lay.n_short_tiles, lay.n_parts, lay.n_kernel_merges);
+                  t.kind);
+    std::printf("L %d %d %d %d %d %d\nE\n", lay.n_units, lay.n_merges, lay.n_tiles, lay.n_dec_tiles,
+                lay.n_short_tiles, lay.n_parts);
   }
   return 0;
 }

@@ -12,9 +12,6 @@ read the way the kernels read it:
     keys [0, key_hi), which every one of those rows must see;
 and a row writes either its output directly (one item covers all its keys) or
 a partial to slot part + t * part_stride that one softmax_merge item names.
-Merge items past the first n_kernel_merges are run inside the persistent
-decode kernel: each belongs to a request of the decode launch, whose every
-item names it through merge0 (its token 0's item).
 """
 import os
 import shutil
@@ -91,18 +88,8 @@ def _check(case, plan, causal=True):
         assert qo[r + 1] - qo[r] == 1 and kl == kv_len[r] and page_base == kv[r]
         contrib[q_row].append((lo, hi, part if part >= 0 else None))
     n_dec, n_short = plan["L"][3], plan["L"][4]
-    n_kernel_merges = plan["L"][6]
-    named = set()
-    for i, (q_row0, qo_len, kl, page_base, tok0, ntok, ntok1, key_lo, key_hi, part, stride, kind,
-            merge0) in enumerate(plan["T"]):
+    for q_row0, qo_len, kl, page_base, tok0, ntok, ntok1, key_lo, key_hi, part, stride, kind in plan["T"]:
         assert key_lo % 128 == 0 and key_lo < key_hi
-        if merge0 >= 0:  # merged in the decode kernel: a decode-launch item writing partials
-            assert i >= len(plan["T"]) - n_dec and part >= 0 and merge0 >= n_kernel_merges
-            for t in range(ntok):
-                assert plan["M"][merge0 + t][0] == q_row0 + t
-                named.add(merge0 + t)
-        elif i >= len(plan["T"]) - n_dec and part >= 0:
-            assert n_kernel_merges == len(plan["M"])  # in-kernel merging was off for this plan
         for tt in range(tok0, tok0 + ntok + ntok1):
             row = q_row0 + tt
             r = row_req[row]
@@ -140,7 +127,6 @@ def _check(case, plan, causal=True):
     assert all(0 <= s < plan["L"][5] for s in written)
     assert len(written) == sum(len(v) for v in merged.values())
     assert plan["L"][:3] == [len(plan["U"]), len(plan["M"]), len(plan["T"])]
-    assert named == set(range(n_kernel_merges, len(plan["M"])))  # no in-kernel merge left out
     assert n_dec + n_short <= len(plan["T"])
 
 
@@ -202,9 +188,9 @@ def test_plan_prefix_groups_share_keys(harness):
             ([0, n], [1024]))
     plan = _plan(harness, [case])[0]
     _check(case, plan)
-    groups = [t for t in plan["T"] if t[11] == 1]
+    groups = [t for t in plan["T"] if t[-1] == 1]
     assert len(groups) == 1 and groups[0][5] == n and groups[0][8] == 1024
-    own = [t for t in plan["T"] if t[11] == 0]
+    own = [t for t in plan["T"] if t[-1] == 0]
     assert own and all(t[7] >= 1024 for t in own)
     assert all(m[2] + (m[3] >= 0) >= 2 for m in plan["M"])
 
@@ -220,7 +206,7 @@ def test_plan_prefill_request_ends_a_run(harness):
     case = ((32, 8, 128, 152), qo, kv, last, ([0, 5], [1024]))
     plan = _plan(harness, [case])[0]
     _check(case, plan)
-    groups = [t for t in plan["T"] if t[11] == 1]
+    groups = [t for t in plan["T"] if t[-1] == 1]
     assert sorted((t[0], t[5]) for t in groups) == [(0, 2), (602, 2)]
-    prefill = [t for t in plan["T"] if t[11] == 0 and t[1] == 600]
+    prefill = [t for t in plan["T"] if t[-1] == 0 and t[1] == 600]
     assert prefill and all(t[7] == 0 and t[9] == -1 for t in prefill)
