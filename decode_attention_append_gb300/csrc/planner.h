@@ -26,6 +26,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <vector>
 
 #include "../../include/daa.h"
@@ -85,6 +86,46 @@ struct PlanLayout {
   size_t off_units = 0, off_merges = 0, off_tiles = 0, off_sched = 0, plan_bytes = 0;
   size_t off_part_o = 0, off_part_lse = 0, total = 0;
 };
+
+// Makespan, in keys, of greedy longest-first assignment of the tensor-core
+// decode units to `workers` persistent CTAs (each takes the next unit when it
+// is free), for key splits of `split_keys`; every unit also costs `overhead`
+// keys.  unit_keys(r, f) calls f(keys) for each split of request r, and every
+// split is repeated for each of `heads` kv heads.  Returns -1 when the batch
+// is too large to model (then a fixed target is used).  Allocation-free: a
+// fixed heap on the stack and a per-thread buffer for the last splits.
+template <class UnitKeys>
+int64_t plan_lpt_makespan(int batch, int heads, int workers, int64_t split_keys, int64_t overhead,
+                          UnitKeys&& unit_keys) {
+  constexpr int kMaxWorkers = 1024, kMaxTail = 8192;
+  thread_local int32_t tail[kMaxTail];
+  if (workers <= 0 || workers > kMaxWorkers) return -1;
+  int64_t n_full = 0;  // splits of exactly split_keys keys (all but each request's last)
+  int n_tail = 0;
+  for (int r = 0; r < batch; ++r) {
+    bool ok = true;
+    unit_keys(r, [&](int64_t keys) {
+      if (keys == split_keys) ++n_full;
+      else if (n_tail < kMaxTail) tail[n_tail++] = (int32_t)keys;
+      else ok = false;
+    });
+    if (!ok) return -1;
+  }
+  n_full *= heads;
+  // full splits first (the longest): workers end up one full unit apart
+  int64_t heap[kMaxWorkers];
+  const int64_t per = n_full / workers, extra = n_full % workers;
+  for (int w = 0; w < workers; ++w) heap[w] = (per + (w < extra ? 1 : 0)) * (split_keys + overhead);
+  std::make_heap(heap, heap + workers, std::greater<int64_t>());
+  std::sort(tail, tail + n_tail, std::greater<int32_t>());
+  for (int i = 0; i < n_tail; ++i)
+    for (int h = 0; h < heads; ++h) {
+      std::pop_heap(heap, heap + workers, std::greater<int64_t>());
+      heap[workers - 1] += tail[i] + overhead;
+      std::push_heap(heap, heap + workers, std::greater<int64_t>());
+    }
+  return *std::max_element(heap, heap + workers);
+}
 
 // Vec: push_back(const T&) -> bool (false when full), size(), data(), clear().
 // With `groups`: within each group, every maximal run of consecutive requests
@@ -185,19 +226,52 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
 
   // split sizes (pages).  CUDA-core splits: about twenty per SM (ten per CTA
   // slot), so the longest split is a small fraction of the pass while the
-  // split-KV partials stay few.  Tensor-core splits: whole 128-key tiles, about
-  // four items per SM, or six when prefill items run beside them: those hold
-  // their SMs for tens of microseconds, the decode CTAs that start after them
-  // take items late, and shorter items keep that tail short.  Targets measured
-  // on GB300 (MHA decode: 20 per SM 7% faster than 40 or 80; persistent
-  // tensor-core decode: 4 per SM best for the GQA decode shard, 6 per SM 9%
-  // faster than 4 for the chunked-prefill mixed batch).
+  // split-KV partials stay few.  Tensor-core splits: whole 128-key tiles.  With
+  // prefill items beside them, about six items per SM: the prefill holds its
+  // SMs for tens of microseconds, the decode CTAs that start after it take
+  // items late, and shorter items keep that tail short.  Alone, the count of
+  // items per SM (2 .. 8) whose greedy assignment to the persistent CTAs ends
+  // first.  Measured on GB300: MHA decode 20 CUDA-core splits per SM 7% faster
+  // than 40 or 80; chunked-prefill mixed batch 6 tensor-core items per SM 9%
+  // faster than 4; GQA decode shard 2 per SM 4% faster than 4, 3 and 5 per SM
+  // 20% slower (the model's ranking).
   bool prefill_beside = groups && groups->n > 0;  // prefix-group items join the prefill launch
   for (int r = 0; r < batch && !prefill_beside; ++r) prefill_beside = qo[r + 1] - qo[r] > short_max;
-  const int64_t tc_per_sm = prefill_beside ? 6 : 4;
-  int64_t split_tc = (page_heads + (int64_t)sms * tc_per_sm - 1) / ((int64_t)sms * tc_per_sm);
-  split_tc = (split_tc + 7) / 8 * 8;
-  split_tc = std::max<int64_t>(32, std::min<int64_t>(2048, split_tc));
+  int64_t cur_split = 0;  // split (pages) being modelled below
+  auto tc_split_for = [&](int64_t per_sm) {
+    int64_t sp = (page_heads + (int64_t)sms * per_sm - 1) / ((int64_t)sms * per_sm);
+    sp = (sp + 7) / 8 * 8;
+    return std::max<int64_t>(32, std::min<int64_t>(2048, sp));
+  };
+  int64_t split_tc = tc_split_for(prefill_beside ? 6 : 4);
+  if (!prefill_beside && tc_decode) {
+    // alone on the GPU, the persistent decode CTAs take their units greedily,
+    // most keys first, so the split whose units pack the CTAs most evenly is
+    // found by simulating that (GB300: this model ranks 2 < 4 < 6 < 8 < 5 < 3
+    // items per SM for the GQA decode shard exactly as measured)
+    auto unit_keys = [&](int r, auto&& emit) {
+      const int nq = qo[r + 1] - qo[r];
+      if (nq < 1 || nq > verify_max) return;
+      const int np = kv[r + 1] - kv[r];
+      const int64_t kv_len = (int64_t)(np - 1) * P + last[r];
+      const int64_t keys = kv_len - nq + 1 - shared_of(r);
+      const int64_t sk_ = (int64_t)cur_split * P;
+      const int64_t n = (keys + sk_ - 1) / sk_;
+      for (int64_t s2 = 0; s2 + 1 < n; ++s2) emit(sk_);
+      emit(kv_len - shared_of(r) - (n - 1) * sk_);
+    };
+    int64_t best = -1;
+    for (int64_t per_sm : {2, 3, 4, 5, 6, 8}) {
+      cur_split = tc_split_for(per_sm);
+      const int64_t m = plan_lpt_makespan(batch, d.num_kv_heads, 2 * sms, cur_split * P,
+                                          /*overhead=*/64, unit_keys);
+      if (m < 0) break;
+      if (best < 0 || m < best) {
+        best = m;
+        split_tc = cur_split;
+      }
+    }
+  }
   int64_t split_cc = (page_heads + (int64_t)sms * 20 - 1) / ((int64_t)sms * 20);
   split_cc = std::max<int64_t>(16, std::min<int64_t>(1024, split_cc));
 
