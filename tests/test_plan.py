@@ -210,3 +210,67 @@ def test_plan_prefill_request_ends_a_run(harness):
     assert sorted((t[0], t[5]) for t in groups) == [(0, 2), (602, 2)]
     prefill = [t for t in plan["T"] if t[-1] == 0 and t[1] == 600]
     assert prefill and all(t[7] == 0 and t[9] == -1 for t in prefill)
+
+
+def _model_split(qos, kvs, Hkv, sms=152):
+    """The planner's choice of tensor-core decode split for a batch with no
+    prefill items, restated: pages per split for 2..8 items per SM, each
+    scored by greedy most-keys-first assignment of its (split, kv head) units
+    to 2 x SM persistent CTAs (64 keys of overhead per unit); first minimum."""
+    import heapq
+    pages = sum(-(-k // P) for q, k in zip(qos, kvs) if 1 <= q <= 16)
+    ph = pages * Hkv
+    best, best_split = None, None
+    for per_sm in (2, 3, 4, 5, 6, 8):
+        sp = (ph + sms * per_sm - 1) // (sms * per_sm)
+        sp = max(32, min(2048, (sp + 7) // 8 * 8))
+        units = []
+        for q, k in zip(qos, kvs):
+            if not 1 <= q <= 16:
+                continue
+            keys = k - q + 1
+            n = -(-keys // (sp * P))
+            units += [sp * P] * (n - 1) + [k - (n - 1) * sp * P]
+        units = sorted(units * Hkv, reverse=True)
+        h = [0] * (2 * sms)
+        for u in units:
+            heapq.heapreplace(h, h[0] + u + 64)
+        m = max(h)
+        if best is None or m < best:
+            best, best_split = m, sp
+    return best_split
+
+
+def test_plan_decode_split_follows_the_assignment_model(harness):
+    """GQA decode alone: the number of decode items equals the split the
+    greedy-assignment model picks (GQA decode shard: 2 per SM, 362 items)."""
+    from synth import make_workload
+    rng = np.random.default_rng(77)
+    batches = []
+    wl = make_workload("gqa_decode_shard")
+    batches.append(([r.qo_len for r in wl.steps[0].requests], [r.kv_len for r in wl.steps[0].requests],
+                    wl.num_qo_heads, wl.num_kv_heads))
+    for _ in range(12):
+        n = int(rng.integers(8, 200))
+        kvs = rng.integers(200, 40000, size=n).tolist()
+        qos = [1 if rng.random() < 0.85 else int(rng.integers(2, 9)) for _ in range(n)]
+        Hkv = int(rng.choice([1, 2, 8]))
+        batches.append((qos, [max(k, q) for k, q in zip(kvs, qos)], 8 * Hkv, Hkv))
+    for qos, kvs, Hq, Hkv in batches:
+        qo = np.concatenate([[0], np.cumsum(qos)]).astype(int).tolist()
+        npg = [-(-k // P) for k in kvs]
+        kv = np.concatenate([[0], np.cumsum(npg)]).astype(int).tolist()
+        last = [k - (m - 1) * P for k, m in zip(kvs, npg)]
+        case = ((Hq, Hkv, 128, 152), qo, kv, last, None)
+        plan = _plan(harness, [case])[0]
+        _check(case, plan)
+        sp = _model_split(qos, kvs, Hkv)
+        # the Q rows of a verify request need qo_len * g <= 128 to stay in the decode launch
+        g = Hq // Hkv
+        expect = sum(-(-(k - q + 1) // (sp * P)) for q, k in zip(qos, kvs) if 1 <= q <= min(16, 128 // g))
+        assert plan["L"][3] == expect, (plan["L"][3], expect, sp)
+    gq = batches[0]
+    assert _plan(harness, [((gq[2], gq[3], 128, 152),
+                            np.concatenate([[0], np.cumsum(gq[0])]).astype(int).tolist(),
+                            np.concatenate([[0], np.cumsum([-(-k // P) for k in gq[1]])]).astype(int).tolist(),
+                            [k - (-(-k // P) - 1) * P for k in gq[1]], None)])[0]["L"][3] == 362
