@@ -254,14 +254,17 @@ daa_status daa_batch_attention_tree(const void* q, const void* kv_pages,
  *
  * The result -- out, lse_out -- is that of daa_batch_attention on the same
  * arguments (equal up to fp32 rounding order).  What differs is the schedule.
- * For every group of two or more requests, the query rows of all its requests
- * (one per new token and query head) are attended to the group's shared keys
- * in one pass, with the rows of several requests packed into the same
- * 128-row tensor-core tiles.  Only whole 128-key tiles of the prefix are
- * shared; the rest of it is read per request.  Each request's own items then
- * cover only the keys after the shared part.  softmax_merge combines the two
- * parts per row.  K/V bytes of the shared prefix are read once per group
- * instead of once per request.
+ * Within a group, every run of consecutive decode, verify and short requests
+ * (1 <= qo_len <= two 128-row Q tiles of packed (token, head) rows) with two
+ * or more such members has the query rows of all its members (one per new
+ * token and query head) attended to the group's shared keys in one pass, the
+ * rows of several requests packed into the same 128-row tensor-core tiles.
+ * Only whole 128-key tiles of the prefix are shared; the rest of it is read
+ * per request.  Each member's own items then cover only the keys after the
+ * shared part, and softmax_merge combines the two parts per row.  K/V bytes of
+ * the shared prefix are read once per run instead of once per request.
+ * Prefill requests of a group (and runs of one member) attend the prefix in
+ * their own items: their Q tiles are full already.
  *
  * Groups (host arrays): group i is requests [h_prefix_indptr[i],
  * h_prefix_indptr[i+1]) -- consecutive requests, groups in request order --
@@ -271,8 +274,9 @@ daa_status daa_batch_attention_tree(const void* q, const void* kv_pages,
  * this (page ids live only on the device); a group that breaks it gives wrong
  * outputs, never an access outside the pool.  h_prefix_len[i] must be a
  * multiple of page_size and cached: at most kv_len_r - qo_len_r for every
- * request of the group.  Requests in no group, and groups of one request,
- * are planned as in daa_batch_attention.
+ * request of the group.  Requests in no group are planned as in
+ * daa_batch_attention; a request between two groups may sit in a group of
+ * prefix length 0.
  *
  *  h_prefix_indptr  host int32 [n_groups + 1], non-decreasing, in [0, batch]
  *  h_prefix_len     host int32 [n_groups]
