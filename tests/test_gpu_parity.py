@@ -398,3 +398,39 @@ def test_chain_mask_matches_unmasked_bitwise(dev):
 def test_no_device_error_recorded(dev):
     import decode_attention_append_gb300 as daa
     assert daa.device_error(reset=True) == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(32, 4, 128), (16, 2, 64)])
+def test_persistent_decode_many_units(dev, Hq, Hkv, d):
+    """The persistent decode kernel over thousands of short units: every CTA
+    runs many of them back to back (barrier phases carried across units),
+    most end in a partial key tile (stale V rows zeroed by the MMA warp),
+    one-token and verify items interleave, and the same plan then runs again
+    (the work counter resets itself)."""
+    import decode_attention_append_gb300 as daa
+    from gpu_support import gpu_fill, new_pool
+    rng = np.random.default_rng(Hq * 7 + d)
+    reqs = [(1, int(k)) for k in rng.integers(1, 400, size=1600)]
+    reqs += [(int(q), int(q + c)) for q, c in zip(rng.integers(2, 9, size=200), rng.integers(0, 500, size=200))]
+    order = rng.permutation(len(reqs))
+    reqs = [reqs[i] for i in order]
+    wl = make_random_workload(900 + Hq, Hq, Hkv, d, 16, reqs, extra_pages=11)
+    stats = _run_both(wl, dev)
+    assert stats
+    # the same plan, run twice more on a stored plan: identical bits
+    pool = new_pool(wl, dev)
+    gpu_fill(wl, pool, dev)
+    st = wl.step_table(0)
+    tab = daa.PageTable.from_host(st["qo_indptr"], st["kv_indptr"], st["page_indices"],
+                                  st["last_page_len"], dev)
+    runner = daa.BatchAttention(tab, wl.num_qo_heads, pool, sm_scale=wl.sm_scale)
+    q, kn, vn = wl.step_inputs(0)
+    runner.append(kn.to(dev), vn.to(dev))
+    qd = q.to(dev)
+    ref = runner.run(qd).clone()
+    runner.plan()
+    for _ in range(2):
+        out = runner.run(qd)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert daa.device_error(reset=True) == 0
