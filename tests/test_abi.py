@@ -257,3 +257,20 @@ def test_plan_and_run_reject_before_any_launch(lib):
                                         ctypes.byref(info), None) == 0
     assert run(ctypes.byref(info), d) == 0
     assert run(ctypes.byref(info), _dims(Hq=8, Hkv=1, d=64, n=256)) == -1  # other dims
+
+
+def test_binding_prefix_groups_and_plan_records(lib):
+    """Python binding, host side only: prefix groups are checked for shape
+    before the library sees them; the shared-prefix workspace query follows
+    the groups; an empty batch plans to a record without touching a device."""
+    import decode_attention_append_gb300 as daa
+    qo, kv, last = _G_QO, _G_KV, _G_LAST
+    with pytest.raises(ValueError):
+        daa.shared_prefix_workspace_size(qo, kv, last, ([0, 3], [256, 16]), 8, 1, 128, 16, 256)
+    with pytest.raises(daa.DaaError):
+        daa.shared_prefix_workspace_size(qo, kv, last, ([0, 3], [250]), 8, 1, 128, 16, 256)
+    plain = daa.batch_attention_workspace_size(qo, kv, last, 8, 1, 128, 16, 256)
+    assert daa.shared_prefix_workspace_size(qo, kv, last, ([0, 3], [0]), 8, 1, 128, 16, 256) == plain
+    assert daa.shared_prefix_workspace_size(qo, kv, last, ([0, 3], [256]), 8, 1, 128, 16, 256) > plain
+    rec = daa.PlanInfo()
+    assert ctypes.sizeof(rec) == 24 * 8
