@@ -798,6 +798,11 @@ def main():
             dm = float(np.mean(per_kernel[kern]))
             line["decode_gbs"] = acc["decode_bytes"] / (dm * 1e-3) / 1e9
             line["decode_kernel"] = kern
+    if acc["append_bytes"] and "kv_append" in per_kernel:
+        # the append's own rate (latency bound for a few tokens per request)
+        am = float(np.mean(per_kernel["kv_append"]))
+        line["append_gbs"] = acc["append_bytes"] / (am * 1e-3) / 1e9
+        line["append_frac_of_hbm"] = line["append_gbs"] / hbm
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
         line["cpu_baseline"] = cpu_baseline(wl)
     print(json.dumps(line), flush=True)
