@@ -2,23 +2,32 @@
 """Benchmark of the paged-attention hot path: one step = kv_append of the step's
 new tokens + batch_attention over the whole mixed batch.
 
-Default workload (N=1): the 7B-class MHA decode batch -- 32 decode requests with
-kv_len ~ U[512, 4096], 32 query / 32 kv heads, head_dim 128, page_size 16, random
-page permutation, plus the append of one token per request.  Other workloads
-(``--workload``): tiny_mixed, chunked_prefill_mixed, gqa_decode_shard,
-long_prefill.
+Headline workload (N=1, default ``--workload long_prefill``): the long-prompt
+prefill batch -- 4 prompts of 16384 tokens processed as their second chunk
+(8192 new tokens over 8192 cached) plus 64 decode requests with kv_len ~
+U[2048, 16384]; 64 query / 8 kv heads, head_dim 128, page_size 16, random page
+permutation.  Its time is dominated by the prefill chunks' tensor-core work, so
+the headline unit is prefill TFLOP/s ("Chunked prefill" (k4i.top), #flops:
+4 d per attended (query, key) pair and query head, the causally masked pairs not
+counted).  Workloads whose time is dominated by streaming the KV cache report
+algorithmic GB/s (K/V pages read once per request, q, out, page ids, append
+read + write).
 
-Prints ONE JSON line (rank 0).  ``value`` = algorithmic HBM bytes of the step
-(K/V pages read once per request, q, out, page ids, append read + write) per
-second of device time with inputs resident in HBM; ``e2e`` = the same bytes per
-second of a step that also copies the step's inputs from pinned host memory and
-reads the output back; ``roofline`` = the dominant kernel's algorithmic bytes
-(or FLOPs) per launch over its mean CUDA-event duration, against the measured
-peak; ``cpu_baseline`` = the CPU oracle on a bounded sample of the workload.
+Prints ONE JSON line (rank 0):
+* ``value`` -- the headline workload's work per second of device time with
+  inputs resident in HBM;
+* ``e2e`` -- the same work per second of a step that also copies its inputs
+  from pinned host memory and reads the output back;
+* ``roofline`` -- the dominant kernel's algorithmic FLOPs (or bytes) per launch
+  over its mean CUDA-event duration, against the measured burst peak;
+* ``cpu_baseline`` -- the CPU oracle on a bounded sample of the workload;
+* ``per_config`` -- the other four workloads (tiny mixed batch, 7B-class MHA
+  decode, chunked-prefill mixed batch, large-model GQA decode shard), each timed
+  the same way, with its own unit, roofline and end-to-end rate.
 
 ``--impl reference`` times the CPU oracle (the only reference this method has)
-on the same workload and metric.  Multi-GPU (torchrun): independent replicas,
-one per GPU, no collective on the data path (``scaling: weak``).
+on the same workload, metric and unit.  Multi-GPU (torchrun): independent
+replicas, one per GPU, no collective on the data path (``scaling: weak``).
 """
 from __future__ import annotations
 
@@ -30,6 +39,7 @@ import shutil
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -41,6 +51,11 @@ sys.path.insert(0, ROOT)
 METRIC = "mixed-batch paged attention: decode KV GB/s, prefill TFLOP/s, % of roofline"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+HEADLINE = "long_prefill"
+# the five workloads of the method's cases, in order (tiny mixed batch, 7B-class
+# MHA decode, chunked-prefill mixed batch, large-model GQA decode shard,
+# long-prompt prefill); the ones not chosen as headline go to ``per_config``
+CONFIGS = ["tiny_mixed", "mha_decode", "chunked_prefill_mixed", "gqa_decode_shard", "long_prefill"]
 
 
 # ----------------------------------------------------------------- accounting
@@ -167,12 +182,13 @@ class ClockSampler:
         self.path = None
 
     def start(self):
+        """Start sampling (query only: nothing about the GPU is changed).  The
+        samples go to a temporary file that stop() reads and removes."""
         if not shutil.which("nvidia-smi"):
             return
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
-            self.fh = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(prefix="daa_clocks_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
@@ -199,18 +215,23 @@ class ClockSampler:
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
+            lines = f.readlines()
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        for line in lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
         if not sm:
             return None
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "samples": len(sm),
@@ -527,14 +548,112 @@ class OracleSample:
         return time.perf_counter() - t0
 
 
-def cpu_baseline(wl, budget_s=12.0, reps=None):
-    s = OracleSample(wl, budget_s)
+class OracleRowSample:
+    """The CPU oracle on sampled query rows of the step's first prefill request
+    (for workloads measured in prefill TFLOP/s, whose whole prefill would take
+    the fp64 oracle hours).  The request's cached prefix is appended once;
+    each run() appends the request's new tokens and attends the sampled rows:
+    the chunk's first and last rows, the first and last row of every 16th
+    128-key tile boundary, and seeded random rows, until the estimated work
+    reaches the budget.  Work = 4 d Hq per attended (query, key) pair
+    ("Chunked prefill", #flops), counted by the oracle itself."""
+
+    def __init__(self, wl, budget_s=12.0):
+        import copy
+
+        import oracle
+        from synth import SENTINEL_BF16, Request, Step
+        self.oracle = oracle
+        reqs = wl.steps[0].requests
+        ri = next(i for i, r in enumerate(reqs) if r.qo_len > 1)
+        r = reqs[ri]
+        src = wl.seqs[r.seq]
+        P = wl.page_size
+        sw = copy.copy(wl)
+        n = -(-r.kv_len // P)
+        sw.seqs = [type(src)(src.length, np.arange(n, dtype=np.int32))]
+        sw.steps, sw.num_pages = [Step([Request(0, r.qo_len, r.kv_len, r.parents)])], n
+        sw._block = lambda seq, kind, block, _w=wl, _s=r.seq: _w._block(_s, kind, block)
+        self.sw = sw
+        self.pool = oracle.new_pool(sw.pool_shape(), SENTINEL_BF16)
+        it = sw.initial_table()
+        k0, v0 = sw.initial_kv()
+        oracle.kv_append(self.pool, k0, v0, it["qo_indptr"], it["page_indices"], it["kv_indptr"],
+                         it["last_page_len"])
+        self.table = sw.step_table(0)
+        self.q, self.kn, self.vn = sw.step_inputs(0)
+        threads = max(1, oracle.num_threads())
+        cached = r.kv_len - r.qo_len
+        # rows in order of priority: chunk edges, key-tile boundaries, random
+        rng = np.random.default_rng(wl.seed)
+        edges = [0, r.qo_len - 1]
+        for kb in range(0, r.kv_len, 16 * 128):
+            for t in (kb - cached - 1, kb - cached):
+                if 0 <= t < r.qo_len:
+                    edges.append(t)
+        order = list(dict.fromkeys(edges)) + [int(x) for x in rng.permutation(r.qo_len)]
+        order = list(dict.fromkeys(order))
+        # calibrate the oracle's rate on the first rows, then fill the budget
+        probe = order[:8]
+        st = self.table
+        t0 = time.perf_counter()
+        _, _, pairs = oracle.attention(self.q, self.pool, st["qo_indptr"], st["kv_indptr"],
+                                       st["page_indices"], st["last_page_len"], sw.causal,
+                                       sw.sm_scale, sw.num_qo_heads, sel_rows=probe)
+        rate = pairs / max(time.perf_counter() - t0, 1e-6)  # pairs per second
+        picked, est = [], 0.0
+        for t in order:
+            cost = (cached + t + 1 if wl.causal else r.kv_len) / rate
+            if picked and est + cost > budget_s:
+                break
+            picked.append(t)
+            est += cost
+        self.rows = sorted(picked)
+        self.flops_per_pair = 4 * wl.head_dim * wl.num_qo_heads
+        self.cores = threads
+        self.sample = (f"{len(self.rows)} of {r.qo_len} query rows of prefill request {ri} "
+                       f"({r.qo_len} new over {cached} cached: chunk edges, rows at 128-key tile "
+                       f"boundaries, seeded random rows) plus its append; fp64 oracle on {threads} "
+                       f"host threads")
+
+    def run(self):
+        """Seconds for one pass; sets self.flops to the pass's algorithmic work."""
+        o, st = self.oracle, self.table
+        t0 = time.perf_counter()
+        o.kv_append(self.pool, self.kn, self.vn, st["qo_indptr"], st["page_indices"], st["kv_indptr"],
+                    st["last_page_len"])
+        _, _, pairs = o.attention(self.q, self.pool, st["qo_indptr"], st["kv_indptr"],
+                                  st["page_indices"], st["last_page_len"], self.sw.causal,
+                                  self.sw.sm_scale, self.sw.num_qo_heads, sel_rows=self.rows)
+        dt = time.perf_counter() - t0
+        self.flops = self.flops_per_pair * pairs
+        return dt
+
+
+def oracle_sample(wl, unit, budget_s):
+    """The oracle sample that measures `unit` on this workload."""
+    return OracleRowSample(wl, budget_s) if unit == "TFLOP/s" else OracleSample(wl, budget_s)
+
+
+def sample_work(s, unit):
+    """Work of one run of a sample, in the unit's base (FLOP or bytes)."""
+    return s.flops if unit == "TFLOP/s" else s.nbytes
+
+
+def cpu_baseline(wl, unit, step_work, budget_s=12.0, reps=None):
+    """The oracle, as it stands, on a bounded sample of the workload; `value`
+    in the headline's unit.  `step_work` (the whole step's work in that unit's
+    base) gives the extrapolated time of a full step for the record."""
+    s = oracle_sample(wl, unit, budget_s)
     dt = s.run()
     reps = reps or max(1, min(20, int(budget_s / max(dt, 1e-3))))
     times = [dt] + [s.run() for _ in range(reps - 1)]
     t = float(np.median(times))
-    return dict(value=s.nbytes / t / 1e9, unit="GB/s", cores=s.cores, kind="oracle",
-                sample=s.sample + f", median of {len(times)} runs of {t:.3f} s")
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    rate = sample_work(s, unit) / t
+    return dict(value=rate / scale, unit=unit, cores=s.cores, kind="oracle",
+                sample=s.sample + f", median of {len(times)} runs of {t:.3f} s; a whole step at "
+                                  f"this rate: {step_work / rate:.1f} s (extrapolated)")
 
 
 def compact_pool(wl):
@@ -553,13 +672,231 @@ def compact_pool(wl):
 
 
 # ---------------------------------------------------------------------- main
+def headline_unit(acc, hbm, bf16):
+    """TFLOP/s when the step's ideal tensor-core time (its prefill FLOPs at the
+    bf16 peak) exceeds its ideal memory time (decode + append bytes at the HBM
+    peak); GB/s of algorithmic bytes otherwise."""
+    t_tensor = acc["prefill_flops"] / (bf16 * 1e12)
+    t_hbm = (acc["decode_bytes"] + acc["append_bytes"]) / (hbm * 1e9)
+    return "TFLOP/s" if t_tensor > t_hbm else "GB/s"
+
+
+def step_work(acc, unit):
+    """Work of one step in the unit's base: prefill FLOPs, or algorithmic bytes."""
+    if unit == "TFLOP/s":
+        return acc["prefill_flops"]
+    return acc["decode_bytes"] + acc["append_bytes"] + acc["prefill_bytes"]
+
+
+def rate(work, steps, world, ms, unit):
+    """Whole-job rate: every replica did `work` per step for `steps` steps."""
+    return job_rate(work, steps, world, ms) / (1e3 if unit == "TFLOP/s" else 1.0)
+
+
+def measure(wl, dev, args, full, clocks=None):
+    """Time one workload on this GPU.  Returns the raw timings (ms over
+    args.steps steps): device-resident steps, per-kernel CUDA-event records,
+    end-to-end steps through the public API with host buffers, and steps on a
+    stored plan.  `full` adds the clock window (back-to-back steps around the
+    timed region, sampled by `clocks`)."""
+    import decode_attention_append_gb300 as daa
+    acc = step_accounting(wl)
+    algo_bytes = acc["decode_bytes"] + acc["append_bytes"] + acc["prefill_bytes"]
+    g = GpuStep(wl, dev, fused=args.api == "fused", prefix_groups=not args.no_prefix_groups)
+    flush_buf = None
+    need_flush = algo_bytes < 2 * L2_BYTES
+    if need_flush:
+        flush_buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = (lambda: flush_buf.fill_(1.0)) if need_flush else None
+    l2 = ("flushed between steps (256 MB write)" if need_flush
+          else f"inputs larger than L2 ({algo_bytes / 1e9:.2f} GB per step)")
+    for _ in range(max(3, args.warmup)):
+        g.step()
+    torch.cuda.synchronize()
+
+    # ---- main timed region: device-resident inputs.  With a clock window,
+    # nvidia-smi samples (100 ms period) cover ~1 s of identical steps before
+    # the timed region and ~0.5 s after it.
+    if full and clocks is not None:
+        clocks.start()
+        soak(g.step, 1.0)
+    args.barrier()
+    ms = timed(g.step, args.steps, flush)
+    args.barrier()
+    # ---- per-kernel roofline pass: CUDA events around each launch
+    recs, clk = [], None
+    if not args.quick:
+        daa.trace_enable(8 * args.steps + 64)
+        timed(g.step, args.steps, flush)
+        recs = daa.trace_read()
+        daa.trace_disable()
+        args.barrier()
+    if full and clocks is not None:
+        soak(g.step, 0.5)
+        clk = clocks.stop()
+        if clk is not None:
+            clk["window"] = "nvidia-smi samples over back-to-back steps around the timed region"
+
+    # ---- e2e: host buffers through the public API.  Inputs larger than L2:
+    # a pipelined serving loop (one packed upload per step on a copy stream,
+    # overlapping the previous step's compute; the output read back behind
+    # it).  L2-flushed small batches: serial steps with the flush between.
+    ms_e2e = float("nan")
+    e2e_mode = None
+    h2d, d2h = g.e2e_bytes()
+    if not args.quick:
+        if flush is None:
+            g.setup_pipeline()
+            g.run_pipeline(3)
+            args.barrier()
+            ms_e2e = g.run_pipeline(args.steps)
+            h2d = g.pack_bytes
+            e2e_mode = ("pipelined: one packed H2D upload per step on an upload stream overlapping the "
+                        "previous step's compute, the output's D2H on a download stream behind it; all "
+                        "copies inside the timed region")
+        else:
+            for _ in range(2):
+                g.step_e2e(torch.cuda.current_stream())
+            args.barrier()
+            ms_e2e = timed(lambda: g.step_e2e(torch.cuda.current_stream()), args.steps, flush)
+            e2e_mode = "serial: H2D inputs, the call, D2H output per step, L2 flushed between steps"
+        args.barrier()
+    # draft-tree batches: the same steps without the mask, for the mask's cost
+    ms_plain = None
+    if g.tree and not args.quick:
+        for _ in range(3):
+            g.step_plain()
+        args.barrier()
+        ms_plain = timed(g.step_plain, args.steps, flush)
+        args.barrier()
+    # the same steps on a plan uploaded once (in a model one plan serves every
+    # layer of a step): each call launches the kernels only
+    ms_planned = float("nan")
+    if not g.tree and not args.quick:
+        g.runner.plan()
+        for _ in range(3):
+            g.step()
+        args.barrier()
+        ms_planned = timed(g.step, args.steps, flush)
+        args.barrier()
+        g.runner.info = None
+    err = daa.device_error(reset=True)
+    res = dict(acc=acc, ms=ms, ms_e2e=ms_e2e, ms_planned=ms_planned, ms_plain=ms_plain, recs=recs,
+               clk=clk, err=err, h2d=h2d, d2h=d2h, e2e_mode=e2e_mode, l2=l2,
+               prefix_groups=g.groups is not None)
+    del g, flush_buf
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def roofline(wl, name, acc, recs, steps, hbm, bf16, bf16_sus, peak_src):
+    """The dominant kernel (largest share of traced time): its algorithmic
+    FLOPs or bytes per launch over its mean CUDA-event duration, against the
+    measured burst peak (each launch runs for microseconds to milliseconds
+    inside a step, not back to back for seconds)."""
+    per_kernel = {}
+    for kname, kms in recs:
+        per_kernel.setdefault(kname, []).append(kms)
+    tot = {k: sum(v) for k, v in per_kernel.items()}
+    if not tot:
+        return None, per_kernel
+    dom = max(tot, key=tot.get)
+    mean_ms = float(np.mean(per_kernel[dom]))
+    n_launch = len(per_kernel[dom]) / steps
+    t = mean_ms * 1e-3
+    if dom in ("prefill_tc", "short_tc"):
+        # the tensor-core prefill kernels: bound by whichever ideal time is larger
+        key = "tc" if dom == "prefill_tc" else "short"
+        fl, by = acc[key + "_flops"] / n_launch, acc[key + "_bytes"] / n_launch
+        t_tensor, t_hbm = fl / (bf16 * 1e12), by / (hbm * 1e9)
+        if t_tensor >= t_hbm:
+            roof = {"bound": "tensor", "achieved": fl / t / 1e12, "peak": bf16, "unit": "TFLOP/s",
+                    "peak_source": f"{peak_src} bf16 dense GEMM, burst",
+                    "frac_of_sustained": fl / t / 1e12 / bf16_sus,
+                    "sustained_peak": bf16_sus}
+        else:
+            roof = {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm, "unit": "GB/s",
+                    "peak_source": f"{peak_src} HBM copy"}
+        roof["ideal_fraction"] = (t_tensor + t_hbm) / t
+        kfile = "prefill_pair.cu" if wl.head_dim == 128 and dom == "prefill_tc" else "prefill.cu"
+    else:
+        kb = {"decode_splitkv": acc["cuda_decode_bytes"], "decode_tc": acc["tc_decode_bytes"],
+              "kv_append": acc["append_bytes"]}.get(dom, 0)
+        roof = {"bound": "hbm", "achieved": kb / n_launch / t / 1e9, "peak": hbm, "unit": "GB/s",
+                "peak_source": f"{peak_src} HBM copy"}
+        kfile = {"decode_splitkv": "decode.cu", "decode_tc": "prefill.cu",
+                 "kv_append": "append.cu"}.get(dom, "decode.cu")
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = dom
+    roof["mean_ms"] = mean_ms
+    roof["traffic"] = measured_traffic(name, kfile)
+    roof["share"] = {k: round(v / sum(tot.values()), 4) for k, v in tot.items()}
+    return roof, per_kernel
+
+
+def make_entry(wl, name, m, args, world, unit):
+    """Rates, roofline and per-kernel figures of one measured workload."""
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    acc = m["acc"]
+    work = step_work(acc, unit)
+    roof, per_kernel = roofline(wl, name, acc, m["recs"], args.steps, hbm, bf16, bf16_sus, peak_src)
+    summary = wl.summary()
+    e = {"workload": name, "description": wl.description,
+         "value": rate(work, args.steps, world, m["ms"], unit), "unit": unit,
+         "ms_per_step": m["ms"] / args.steps,
+         "e2e": {"value": rate(work, args.steps, world, m["ms_e2e"], unit), "unit": unit,
+                 "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"],
+                 "ms_per_step": m["ms_e2e"] / args.steps, "mode": m["e2e_mode"]},
+         "gpu_launches": int(round(len(m["recs"]))),
+         "roofline": roof,
+         "algorithmic": {"bytes_per_step": acc["decode_bytes"] + acc["append_bytes"] + acc["prefill_bytes"],
+                         "decode_bytes": acc["decode_bytes"], "append_bytes": acc["append_bytes"],
+                         "prefill_flops": acc["prefill_flops"]},
+         "config": {"requests": summary["requests"], "decode_requests": summary["decode_requests"],
+                    "prefill_requests": summary["prefill_requests"], "kv_tokens": summary["kv_tokens"],
+                    "Hq": wl.num_qo_heads, "Hkv": wl.num_kv_heads, "head_dim": wl.head_dim,
+                    "page_size": wl.page_size, "num_pages": wl.num_pages,
+                    "prefix_groups": m["prefix_groups"], "l2": m["l2"]},
+         "device_error": m["err"]}
+    e["kernels_ms"] = {k: round(float(np.mean(v)), 5) for k, v in per_kernel.items()}
+    if m["ms_planned"] == m["ms_planned"]:  # not NaN
+        e["planned"] = {"value": rate(work, args.steps, world, m["ms_planned"], unit), "unit": unit,
+                        "ms_per_step": m["ms_planned"] / args.steps,
+                        "note": "plan uploaded once (batch_attention_plan), each step runs the "
+                                "kernels only; the headline value includes the plan"}
+    if m["ms_plain"] is not None:
+        e["tree_mask"] = {"ms_per_step_masked": m["ms"] / args.steps,
+                          "ms_per_step_unmasked": m["ms_plain"] / args.steps,
+                          "overhead": m["ms"] / m["ms_plain"] - 1.0,
+                          "note": "same batch and kernels, plain causal attention without the mask"}
+    if acc["prefill_flops"] and "prefill_tc" in per_kernel:
+        # conservative: the kernel time also covers any decode splits it ran
+        pm = float(np.mean(per_kernel["prefill_tc"]))
+        e["prefill_tflops"] = acc["prefill_flops"] / (pm * 1e-3) / 1e12
+        e["prefill_frac_of_bf16"] = e["prefill_tflops"] / bf16
+    if acc["decode_bytes"]:
+        kern = "decode_splitkv" if acc["cuda_decode_bytes"] else "decode_tc"
+        if kern in per_kernel:
+            dm = float(np.mean(per_kernel[kern]))
+            e["decode_gbs"] = acc["decode_bytes"] / (dm * 1e-3) / 1e9
+            e["decode_frac_of_hbm"] = e["decode_gbs"] / hbm
+            e["decode_kernel"] = kern
+    if acc["append_bytes"] and "kv_append" in per_kernel:
+        # the append's own rate (latency bound for a few tokens per request)
+        am = float(np.mean(per_kernel["kv_append"]))
+        e["append_gbs"] = acc["append_bytes"] / (am * 1e-3) / 1e9
+        e["append_frac_of_hbm"] = e["append_gbs"] / hbm
+    return e
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="mha_decode")
+    ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--api", default="fused", choices=["fused", "two-call"],
                     help="fused: one append_attention call per step; two-call: kv_append then "
                          "batch_attention")
@@ -567,8 +904,11 @@ def main():
                     help="requests that share a cached prefix: plain calls (each request reads "
                          "the prefix) instead of the shared-prefix calls")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time the headline workload only (no per_config map)")
     ap.add_argument("--quick", action="store_true",
-                    help="profiling runs: timed steps only (no clock window, no traced or e2e pass)")
+                    help="profiling runs: timed steps only (no clock window, no traced, e2e or "
+                         "planned pass, no per_config map)")
     ap.add_argument("--compact-pool", action="store_true",
                     help="renumber pages densely so the pool holds only the pages used "
                          "(same work; smaller device footprint for profiler captures)")
@@ -579,17 +919,17 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
     from synth import make_workload
-    wl = make_workload(args.workload)
-    if args.compact_pool:
-        wl = compact_pool(wl)
+
+    def load(name):
+        w = make_workload(name)
+        return compact_pool(w) if args.compact_pool else w
+
+    wl = load(args.workload)
     acc = step_accounting(wl)
-    algo_bytes = acc["decode_bytes"] + acc["append_bytes"] + acc["prefill_bytes"]
-    summary = wl.summary()
+    hbm, bf16, bf16_sus, _ = peaks()
+    unit = headline_unit(acc, hbm, bf16)
+    work = step_work(acc, unit)
     config = {"workload": args.workload, "description": wl.description,
-              "requests": summary["requests"], "decode_requests": summary["decode_requests"],
-              "prefill_requests": summary["prefill_requests"], "kv_tokens": summary["kv_tokens"],
-              "Hq": wl.num_qo_heads, "Hkv": wl.num_kv_heads, "head_dim": wl.head_dim,
-              "page_size": wl.page_size, "num_pages": wl.num_pages,
               "parallelism": f"replicas{args.gpus}", "compact_pool": bool(args.compact_pool),
               "api": ("append_attention" if args.api == "fused"
                       else "kv_append + batch_attention")}
@@ -597,18 +937,19 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        sample = OracleSample(wl, budget_s=6.0)
+        sample = oracle_sample(wl, unit, budget_s=6.0)
         for _ in range(args.warmup):
             sample.run()
         secs = [sample.run() for _ in range(args.steps)]
-        v = sample.nbytes * len(secs) / sum(secs) / 1e9
-        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+        scale = 1e12 if unit == "TFLOP/s" else 1e9
+        v = sample_work(sample, unit) * len(secs) / sum(secs) / scale
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(secs) / len(secs),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": config,
-                "cpu_baseline": {"value": v, "unit": "GB/s", "cores": sample.cores, "kind": "oracle",
+                "cpu_baseline": {"value": v, "unit": unit, "cores": sample.cores, "kind": "oracle",
                                  "sample": sample.sample},
-                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return 0
 
@@ -628,183 +969,55 @@ def main():
         dist.barrier()
         if rank != 0:
             __graft_entry__.build()
-    import decode_attention_append_gb300 as daa
-
-    g = GpuStep(wl, dev, fused=args.api == "fused", prefix_groups=not args.no_prefix_groups)
-    config["prefix_groups"] = g.groups is not None
-    flush_buf = None
-    need_flush = algo_bytes < 2 * L2_BYTES
-    if need_flush:
-        flush_buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    flush = (lambda: flush_buf.fill_(1.0)) if need_flush else None
-    config["l2"] = ("flushed between steps (256 MB write)" if need_flush
-                    else f"inputs larger than L2 ({algo_bytes / 1e9:.2f} GB per step)")
-
-    for _ in range(max(3, args.warmup)):
-        g.step()
-    torch.cuda.synchronize()
 
     def barrier():
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
+    args.barrier = barrier
 
-    # ---- main timed region: device-resident inputs.  Clocks are sampled by
-    # nvidia-smi (100 ms period) over a window of back-to-back identical steps
-    # that contains the timed region: ~1 s of steps before it, ~0.5 s after.
+    # ---- the headline workload, with its clock window
     clocks = ClockSampler(local)
-    if not args.quick:
-        clocks.start()
-        soak(g.step, 1.0)
-    barrier()
-    ms = timed(g.step, args.steps, flush)
-    barrier()
-    # ---- per-kernel roofline pass: CUDA events around each launch
-    recs, clk = [], None
-    if not args.quick:
-        daa.trace_enable(8 * args.steps + 64)
-        timed(g.step, args.steps, flush)
-        recs = daa.trace_read()
-        daa.trace_disable()
-        barrier()
-        soak(g.step, 0.5)
-        clk = clocks.stop()
-    if clk is not None:
-        clk["window"] = "nvidia-smi samples over back-to-back steps around the timed region"
+    m = measure(wl, dev, args, full=not args.quick, clocks=clocks)
+    ms, ms_e2e, ms_planned = max_over_ranks([m["ms"], m["ms_e2e"], m["ms_planned"]], dist, dev)
+    m.update(ms=ms, ms_e2e=ms_e2e, ms_planned=ms_planned)
 
-    # ---- e2e: host buffers through the public API.  Inputs larger than L2:
-    # a pipelined serving loop (one packed upload per step on a copy stream,
-    # overlapping the previous step's compute; the output read back behind
-    # it).  The L2-flushed tiny batch: serial steps with the flush between.
-    ms_e2e = float("nan")
-    e2e_mode = None
-    h2d, d2h = g.e2e_bytes()
-    if not args.quick:
-        if flush is None:
-            g.setup_pipeline()
-            g.run_pipeline(3)
-            barrier()
-            ms_e2e = g.run_pipeline(args.steps)
-            h2d = g.pack_bytes
-            e2e_mode = ("pipelined: one packed H2D upload per step on an upload stream overlapping the "
-                        "previous step's compute, the output's D2H on a download stream behind it; all "
-                        "copies inside the timed region")
-        else:
-            for _ in range(2):
-                g.step_e2e(torch.cuda.current_stream())
-            barrier()
-            ms_e2e = timed(lambda: g.step_e2e(torch.cuda.current_stream()), args.steps, flush)
-            e2e_mode = "serial: H2D inputs, the call, D2H output per step, L2 flushed between steps"
-        barrier()
-    # draft-tree batches: the same steps without the mask, for the mask's cost
-    ms_plain = None
-    if g.tree and not args.quick:
-        for _ in range(3):
-            g.step_plain()
-        barrier()
-        ms_plain = timed(g.step_plain, args.steps, flush)
-        barrier()
-    # the same steps on a plan uploaded once (in a model one plan serves every
-    # layer of a step): each call launches the kernels only
-    ms_planned = float("nan")
-    if not g.tree and not args.quick:
-        g.runner.plan()
-        for _ in range(3):
-            g.step()
-        barrier()
-        ms_planned = timed(g.step, args.steps, flush)
-        barrier()
-        g.runner.info = None
-    err = daa.device_error(reset=True)
+    # ---- the other configurations, each timed the same way (no clock window)
+    per_config = {}
+    if not args.quick and not args.no_per_config:
+        for name in CONFIGS:
+            if name == args.workload:
+                continue
+            w2 = load(name)
+            a2 = step_accounting(w2)
+            u2 = headline_unit(a2, hbm, bf16)
+            m2 = measure(w2, dev, args, full=False)
+            t = max_over_ranks([m2["ms"], m2["ms_e2e"], m2["ms_planned"]], dist, dev)
+            m2.update(ms=t[0], ms_e2e=t[1], ms_planned=t[2])
+            if rank == 0:
+                per_config[name] = make_entry(w2, name, m2, args, world, u2)
 
-    ms, ms_e2e, ms_planned = max_over_ranks([ms, ms_e2e, ms_planned], dist, dev)
     if rank != 0:
         dist.destroy_process_group()
         return 0
 
-    per_kernel = {}
-    for name, kms in recs:
-        per_kernel.setdefault(name, []).append(kms)
-    launches = len(recs) / max(1, args.steps)
-    hbm, bf16, bf16_sus, peak_src = peaks()
-    # dominant kernel: largest share of traced time
-    tot = {k: sum(v) for k, v in per_kernel.items()}
-    dom = max(tot, key=tot.get) if tot else None
-    roof = None
-    if dom is not None:
-        mean_ms = float(np.mean(per_kernel[dom]))
-        n_launch = len(per_kernel[dom]) / args.steps
-        t = mean_ms * 1e-3
-        if dom in ("prefill_tc", "short_tc"):
-            # the tensor-core prefill kernels: bound by whichever ideal time is larger
-            key = "tc" if dom == "prefill_tc" else "short"
-            fl, by = acc[key + "_flops"] / n_launch, acc[key + "_bytes"] / n_launch
-            t_tensor, t_hbm = fl / (bf16 * 1e12), by / (hbm * 1e9)
-            if t_tensor >= t_hbm:
-                # the kernel runs back to back for seconds (clock window + timed
-                # steps) under the power cap: the sustained GEMM rate is its peak
-                roof = {"bound": "tensor", "achieved": fl / t / 1e12, "peak": bf16_sus, "unit": "TFLOP/s",
-                        "peak_source": f"{peak_src} bf16 dense, sustained (burst {bf16:.1f})",
-                        "frac_of_burst": fl / t / 1e12 / bf16}
-            else:
-                roof = {"bound": "hbm", "achieved": by / t / 1e9, "peak": hbm, "unit": "GB/s",
-                        "peak_source": f"{peak_src} HBM copy"}
-            roof["ideal_fraction"] = (t_tensor + t_hbm) / t
-            kfile = "prefill_pair.cu" if wl.head_dim == 128 and dom == "prefill_tc" else "prefill.cu"
-        else:
-            kb = {"decode_splitkv": acc["cuda_decode_bytes"], "decode_tc": acc["tc_decode_bytes"],
-                  "kv_append": acc["append_bytes"]}.get(dom, 0)
-            roof = {"bound": "hbm", "achieved": kb / n_launch / t / 1e9, "peak": hbm, "unit": "GB/s",
-                    "peak_source": f"{peak_src} HBM copy"}
-            kfile = {"decode_splitkv": "decode.cu", "decode_tc": "prefill.cu",
-                     "kv_append": "append.cu"}.get(dom, "decode.cu")
-        roof["frac"] = roof["achieved"] / roof["peak"]
-        roof["kernel"] = dom
-        roof["mean_ms"] = mean_ms
-        roof["traffic"] = measured_traffic(args.workload, kfile)
-        roof["share"] = {k: round(v / sum(tot.values()), 4) for k, v in tot.items()}
-
-    value = job_rate(algo_bytes, args.steps, world, ms)
-    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+    e = make_entry(wl, args.workload, m, args, world, unit)
+    config.update(e["config"])
+    line = {"metric": METRIC, "value": e["value"], "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": e["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config,
-            "e2e": {"value": job_rate(algo_bytes, args.steps, world, ms_e2e), "unit": "GB/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": ms_e2e / args.steps, "mode": e2e_mode},
-            "gpu_launches": int(round(launches * args.steps)),
-            "roofline": roof,
-            "algorithmic": {"bytes_per_step": algo_bytes, "decode_bytes": acc["decode_bytes"],
-                            "append_bytes": acc["append_bytes"], "prefill_flops": acc["prefill_flops"]},
-            "clocks": clk, "device_error": err}
-    line["kernels_ms"] = {k: round(float(np.mean(v)), 5) for k, v in per_kernel.items()}
-    if ms_planned == ms_planned:  # not NaN
-        line["planned"] = {"value": job_rate(algo_bytes, args.steps, world, ms_planned), "unit": "GB/s",
-                           "ms_per_step": ms_planned / args.steps,
-                           "note": "plan uploaded once (batch_attention_plan), each step runs the "
-                                   "kernels only; the headline value includes the plan"}
-    if ms_plain is not None:
-        line["tree_mask"] = {"ms_per_step_masked": ms / args.steps,
-                             "ms_per_step_unmasked": ms_plain / args.steps,
-                             "overhead": ms / ms_plain - 1.0,
-                             "note": "same batch and kernels, plain causal attention without the mask"}
-    if acc["prefill_flops"] and "prefill_tc" in per_kernel:
-        # conservative: the kernel time also covers any decode splits it ran
-        pm = float(np.mean(per_kernel["prefill_tc"]))
-        line["prefill_tflops"] = acc["prefill_flops"] / (pm * 1e-3) / 1e12
-    if acc["decode_bytes"]:
-        kern = "decode_splitkv" if acc["cuda_decode_bytes"] else "decode_tc"
-        if kern in per_kernel:
-            dm = float(np.mean(per_kernel[kern]))
-            line["decode_gbs"] = acc["decode_bytes"] / (dm * 1e-3) / 1e9
-            line["decode_kernel"] = kern
-    if acc["append_bytes"] and "kv_append" in per_kernel:
-        # the append's own rate (latency bound for a few tokens per request)
-        am = float(np.mean(per_kernel["kv_append"]))
-        line["append_gbs"] = acc["append_bytes"] / (am * 1e-3) / 1e9
-        line["append_frac_of_hbm"] = line["append_gbs"] / hbm
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
-        line["cpu_baseline"] = cpu_baseline(wl)
+            "config": config, "e2e": e["e2e"],
+            "gpu_launches": e["gpu_launches"], "roofline": e["roofline"],
+            "algorithmic": e["algorithmic"], "clocks": m["clk"], "device_error": e["device_error"],
+            "kernels_ms": e["kernels_ms"]}
+    for k in ("planned", "tree_mask", "prefill_tflops", "prefill_frac_of_bf16", "decode_gbs",
+              "decode_frac_of_hbm", "decode_kernel", "append_gbs", "append_frac_of_hbm"):
+        if k in e:
+            line[k] = e[k]
+    if per_config:
+        line["per_config"] = per_config
+    if world == 1 and not args.no_cpu_baseline and not args.quick:
+        line["cpu_baseline"] = cpu_baseline(wl, unit, work)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -406,6 +406,8 @@ def batch_attention_noalloc(q, kv_pages, qo_indptr, kv_indptr, page_indices, las
     for n, t in (("qo_indptr", qo_indptr), ("kv_indptr", kv_indptr), ("page_indices", page_indices),
                  ("last_page_len", last_page_len)):
         _dev_i32(t, n)
+    if q.dim() != 3:
+        raise ValueError("q must be [nnz_qo, Hq, head_dim]")
     Hq, d = q.shape[1], q.shape[2]
     dims = _dims(kv_pages, Hq)
     if sm_scale is None:
@@ -414,6 +416,14 @@ def batch_attention_noalloc(q, kv_pages, qo_indptr, kv_indptr, page_indices, las
     if out is None:
         out = torch.empty_like(q)
     _dev_bf16(out, "out")
+    if out.shape != q.shape:
+        raise ValueError("out must have the shape of q")
+    if lse is not None:
+        if not (isinstance(lse, torch.Tensor) and lse.is_cuda and lse.dtype == torch.float32
+                and lse.is_contiguous()):
+            raise TypeError("lse must be a contiguous fp32 CUDA tensor")
+        if tuple(lse.shape) != (q.shape[0], Hq):
+            raise ValueError("lse must be [nnz_qo, Hq]")
     _check(lib.daa_batch_attention_noalloc(_ptr(q), _ptr(kv_pages), _ptr(qo_indptr), _ptr(kv_indptr),
                                            _ptr(page_indices), _ptr(last_page_len), _ptr(hq), _ptr(hk),
                                            _ptr(hl), len(hq) - 1, int(bool(causal)), float(sm_scale),

@@ -181,15 +181,28 @@ def test_config_full_rows(dev, name):
 
 
 def test_long_prefill_sampled_rows(dev):
+    """The long-prompt prefill batch (4 x 8192 new over 8192 cached, GQA 64/8,
+    + 64 decodes) on ~1,100 rows checked one by one against the oracle:
+    * prompt 0: one row in every 128-row Q tile (16 tokens x 8 heads each), at
+      a rotating offset inside the tile, so every tile slot of every four-tile
+      pair item, on both CTAs of the pair, is checked;
+    * every prompt: the last row before and the first row after every 128-key
+      tile boundary along the diagonal (the masked diagonal tiles and the key
+      tile that is read as a whole for the first time), and the chunk's edges;
+    * all 64 decode rows.
+    The pool is compared byte for byte."""
     wl = make_workload("long_prefill")
-    rng = np.random.default_rng(5)
-    prompt_rows = []
+    qo = 8192
+    tpt = 128 // wl.group_size  # tokens per 128-row Q tile
+    prompt_rows = [t * tpt + (7 * t) % tpt for t in range(qo // tpt)]
     for p in range(4):
-        base = p * 8192
-        prompt_rows += [base, base + 1, base + 15, base + 16, base + 8191]
-        prompt_rows += list(base + rng.choice(8192, 6, replace=False))
-    decode_rows = list(range(4 * 8192, 4 * 8192 + 64))
+        base = p * qo
+        prompt_rows += [base, base + 1, base + qo - 1]
+        for b in range(128, qo, 128):
+            prompt_rows += [base + b - 1, base + b]
+    decode_rows = list(range(4 * qo, 4 * qo + 64))
     sel = sorted(set(prompt_rows)) + decode_rows
+    assert len(set(r // tpt for r in prompt_rows if r < qo)) == qo // tpt
     _run_both(wl, dev, sel_rows=sel)
 
 
