@@ -903,6 +903,9 @@ def main():
     ap.add_argument("--no-prefix-groups", action="store_true",
                     help="requests that share a cached prefix: plain calls (each request reads "
                          "the prefix) instead of the shared-prefix calls")
+    ap.add_argument("--no-fused-prefill-append", action="store_true",
+                    help="fused calls: append every row with the append kernel instead of letting "
+                         "the CTA-pair prefill kernel write its chunk's own key tiles")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="time the headline workload only (no per_config map)")
@@ -975,6 +978,10 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
     args.barrier = barrier
+    import decode_attention_append_gb300 as daa
+    daa.set_prefill_append_fusion(not args.no_fused_prefill_append)
+    config["prefill_append"] = ("append kernel (every row)" if args.no_fused_prefill_append else
+                                "fused into the CTA-pair prefill kernel for long chunks")
 
     # ---- the headline workload, with its clock window
     clocks = ClockSampler(local)

@@ -114,6 +114,10 @@ def load_library():
         lib.daa_append_attention_run.restype = i32
         lib.daa_append_attention_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, pinfo, i32, f32, vp, vp,
                                                  vp, sz, _Dims, vp]
+        lib.daa_set_prefill_append_fusion.restype = i32
+        lib.daa_set_prefill_append_fusion.argtypes = [i32]
+        lib.daa_prefill_append_fusion.restype = i32
+        lib.daa_prefill_append_fusion.argtypes = []
         lib.daa_selftest_bounded_wait.restype = i32
         lib.daa_selftest_bounded_wait.argtypes = [ctypes.POINTER(i32)]
         lib.daa_device_error.restype = i32
@@ -592,6 +596,19 @@ class BatchAttention:
                                workspace=self.workspace,
                                host_indptr=(t.h_qo_indptr, t.h_kv_indptr, t.h_last_page_len),
                                stream=stream, prefix_groups=self.prefix_groups)
+
+
+def set_prefill_append_fusion(enable: bool) -> None:
+    """Fused calls (``append_attention``, ``BatchAttention.step``): whether the
+    CTA-pair prefill kernel reads long chunks' own key tiles from k_new / v_new
+    and writes them into their pages itself (True, the default) or the append
+    kernel writes every row (False).  Results are identical."""
+    _check(load_library().daa_set_prefill_append_fusion(int(bool(enable))),
+           "set_prefill_append_fusion")
+
+
+def prefill_append_fusion() -> bool:
+    return bool(load_library().daa_prefill_append_fusion())
 
 
 def device_error(reset: bool = True) -> int:

@@ -11,6 +11,7 @@
 // key range first.  The plan is built from the host mirrors of the indptr
 // arrays, so no call waits on the device.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -178,6 +179,21 @@ std::vector<uint8_t>& staging() {
   return buf;
 }
 
+// Fused calls: whether the CTA-pair prefill kernel reads its chunk's own key
+// tiles from k_new / v_new and writes them into the pages itself (1, the
+// default), or the append kernel writes every row and the prefill reads them
+// back from the pages (0).  Results are identical either way.
+std::atomic<int> g_fuse_prefill_append{1};
+
+// The smallest qo_len whose rows the prefill kernel appends in a fused call:
+// requests planned as CTA-pair prefill items (head_dim 128, more rows than
+// two 128-row Q tiles hold); 0 when nothing is fused.
+int fuse_min_qo_for(const daa_dims& d) {
+  if (!g_fuse_prefill_append.load(std::memory_order_relaxed) || !plan_prefill_quads(d)) return 0;
+  const int g = d.num_qo_heads / d.num_kv_heads;
+  return 2 * (kPrefillTileRows / g) + 1;
+}
+
 }  // namespace
 
 daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s, bool trace,
@@ -222,6 +238,10 @@ daa_status launch_all(const LaunchSet& ls, const PlanLayout& lay, cudaStream_t s
     a.err = ls.err;
     a.dec_counter = reinterpret_cast<int*>(ws + lay.off_sched);
     a.sms = ls.sms;
+    a.k_new = static_cast<const uint16_t*>(ls.k_new);
+    a.v_new = static_cast<const uint16_t*>(ls.v_new);
+    a.pool_w = const_cast<uint16_t*>(static_cast<const uint16_t*>(ls.kv_pages));
+    a.fuse_min_qo = ls.k_new && ls.v_new ? ls.fuse_min_qo : 0;
     if (a.n_tiles > 0) {
       const bool quads = plan_prefill_quads(dims);
       if (run(kKernelPrefill, [&] {
@@ -321,7 +341,7 @@ daa_status daa_kv_append(const void* k_new, const void* v_new, void* kv_pages,
   cudaError_t e = traced(kKernelAppend, s, [&] {
     return launch_kv_append(k_new, v_new, kv_pages, append_indptr, page_indices, kv_indptr,
                             last_page_len, batch, nnz_new, dims.num_kv_heads, dims.head_dim,
-                            dims.num_pages, num_sms(), err, s);
+                            dims.num_pages, num_sms(), /*fuse_min_qo=*/0, err, s);
   });
   return e == cudaSuccess ? DAA_OK : DAA_ERR_CUDA;
 }
@@ -398,12 +418,14 @@ daa_status attention_call(const void* k_new, const void* v_new, const void* q,
   if (cudaMemcpyAsync(ws, host.data(), lay.plan_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return DAA_ERR_CUDA;
   const int nnz_qo = h_qo_indptr[batch];
+  // the tree call never fuses (its mask path appends separately)
+  const int fuse_min_qo = fused && !tree_mask ? fuse_min_qo_for(dims) : 0;
   if (fused && nnz_qo > 0) {
     int* err = device_error_word();
     cudaError_t e = traced(kKernelAppend, s, [&] {
       return launch_kv_append(k_new, v_new, const_cast<void*>(kv_pages), qo_indptr, page_indices,
                               kv_indptr, last_page_len, batch, nnz_qo, dims.num_kv_heads,
-                              dims.head_dim, dims.num_pages, num_sms(), err, s);
+                              dims.head_dim, dims.num_pages, num_sms(), fuse_min_qo, err, s);
     });
     if (e != cudaSuccess) return DAA_ERR_CUDA;
   }
@@ -422,6 +444,11 @@ daa_status attention_call(const void* k_new, const void* v_new, const void* q,
   ls.scratch = ws;
   ls.err = device_error_word();
   ls.sms = num_sms();
+  if (fused) {
+    ls.k_new = k_new;
+    ls.v_new = v_new;
+    ls.fuse_min_qo = fuse_min_qo;
+  }
   return launch_all(ls, lay, s, /*trace=*/true, /*after_append=*/fused && nnz_qo > 0);
 }
 
@@ -574,12 +601,13 @@ daa_status run_call(const void* k_new, const void* v_new, const void* q, const v
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DAA_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int nnz_qo = (int)rec.nnz_qo;
+  const int fuse_min_qo = fused ? fuse_min_qo_for(dims) : 0;
   if (fused && nnz_qo > 0) {
     int* err = device_error_word();
     cudaError_t e = traced(kKernelAppend, s, [&] {
       return launch_kv_append(k_new, v_new, const_cast<void*>(kv_pages), qo_indptr, page_indices,
                               kv_indptr, last_page_len, (int)rec.batch, nnz_qo, dims.num_kv_heads,
-                              dims.head_dim, dims.num_pages, num_sms(), err, s);
+                              dims.head_dim, dims.num_pages, num_sms(), fuse_min_qo, err, s);
     });
     if (e != cudaSuccess) return DAA_ERR_CUDA;
   }
@@ -596,6 +624,11 @@ daa_status run_call(const void* k_new, const void* v_new, const void* q, const v
   ls.scratch = workspace;
   ls.err = device_error_word();
   ls.sms = num_sms();
+  if (fused) {
+    ls.k_new = k_new;
+    ls.v_new = v_new;
+    ls.fuse_min_qo = fuse_min_qo;
+  }
   return launch_all(ls, lay, s, /*trace=*/true, /*after_append=*/fused && nnz_qo > 0);
 }
 
@@ -625,6 +658,14 @@ daa_status daa_append_attention_run(const void* k_new, const void* v_new, const 
                   info, causal, sm_scale, out, lse_out, workspace, workspace_bytes, dims, stream,
                   true);
 }
+
+daa_status daa_set_prefill_append_fusion(int32_t enable) {
+  if (enable != 0 && enable != 1) return DAA_ERR_INVALID_ARG;
+  g_fuse_prefill_append.store(enable, std::memory_order_relaxed);
+  return DAA_OK;
+}
+
+int32_t daa_prefill_append_fusion(void) { return g_fuse_prefill_append.load(std::memory_order_relaxed); }
 
 daa_status daa_selftest_bounded_wait(int32_t* gave_up) {
   if (!gave_up) return DAA_ERR_INVALID_ARG;

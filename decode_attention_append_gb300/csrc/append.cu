@@ -14,6 +14,10 @@
 // then all threads stream 16-byte chunks with read-only, no-allocate loads.
 // Source rows are contiguous ([Hkv][d] per token); each destination (head,
 // slot) row is 2*d contiguous bytes, so warps write whole 128-byte lines.
+// In a fused append + attention call the CTA-pair prefill kernel writes the
+// rows of long prefill requests from their first 128-aligned key tile on
+// itself (it reads those tiles from k_new / v_new anyway); this kernel then
+// skips them (fuse_min_qo > 0).
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -38,7 +42,7 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
                  uint4* __restrict__ pool, const int32_t* __restrict__ append_indptr,
                  const int32_t* __restrict__ page_indices, const int32_t* __restrict__ kv_indptr,
                  const int32_t* __restrict__ last_page_len, int batch, int nnz_new, int Hkv,
-                 int chunks_per_cta, int64_t num_pages, int* err) {
+                 int chunks_per_cta, int64_t num_pages, int fuse_min_qo, int* err) {
   constexpr int P = 16;
   constexpr int CH = D / 8;  // 16-byte chunks per (head, slot) row
   __shared__ int64_t s_dst[kAppendMaxRows];  // chunk index of (page, K, head 0, slot, 0); -1 = skip
@@ -72,7 +76,9 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
     } else {
       const int64_t pos = kv_len - n_new + (row - a0);
       const int64_t page = __ldg(page_indices + p0 + pos / P);
-      if (page < 0 || page >= num_pages) {
+      if (fuse_min_qo > 0 && n_new >= fuse_min_qo && pos >= fused_from((int)kv_len, n_new)) {
+        // written by the prefill kernel of this fused call, from the same rows
+      } else if (page < 0 || page >= num_pages) {
         set_device_error(err, kDevErrPageRange);
       } else {
         dst = ((page * 2) * Hkv * P + (pos % P)) * CH;
@@ -117,7 +123,7 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* pool,
                              const int32_t* append_indptr, const int32_t* page_indices,
                              const int32_t* kv_indptr, const int32_t* last_page_len, int batch,
                              int nnz_new, int Hkv, int head_dim, int64_t num_pages, int num_sms,
-                             int* err, cudaStream_t stream) {
+                             int fuse_min_qo, int* err, cudaStream_t stream) {
   if (nnz_new <= 0 || batch <= 0) return cudaSuccess;
   const int per_row = 2 * Hkv * (head_dim / 8);
   const int64_t total = (int64_t)nnz_new * per_row;
@@ -133,11 +139,11 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* pool,
   if (head_dim == 128) {
     kv_append_kernel<128><<<(unsigned)grid, kAppendThreads, 0, stream>>>(
         (const uint4*)k_new, (const uint4*)v_new, (uint4*)pool, append_indptr, page_indices,
-        kv_indptr, last_page_len, batch, nnz_new, Hkv, (int)cpc, num_pages, err);
+        kv_indptr, last_page_len, batch, nnz_new, Hkv, (int)cpc, num_pages, fuse_min_qo, err);
   } else {
     kv_append_kernel<64><<<(unsigned)grid, kAppendThreads, 0, stream>>>(
         (const uint4*)k_new, (const uint4*)v_new, (uint4*)pool, append_indptr, page_indices,
-        kv_indptr, last_page_len, batch, nnz_new, Hkv, (int)cpc, num_pages, err);
+        kv_indptr, last_page_len, batch, nnz_new, Hkv, (int)cpc, num_pages, fuse_min_qo, err);
   }
   return cudaGetLastError();
 }

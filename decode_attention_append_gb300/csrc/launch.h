@@ -30,11 +30,22 @@ inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, 
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Key tiles are 128 keys; with the prefill append fused (fuse_min_qo > 0), a
+// request with qo_len >= fuse_min_qo has its new tokens at positions
+// >= fused_from(kv_len, qo_len) written by the prefill kernel, not the append.
+constexpr int kFuseTileKeys = 128;
+__host__ __device__ inline int fused_from(int kv_len, int qo_len) {
+  const int c = kv_len - qo_len;
+  return (c + kFuseTileKeys - 1) / kFuseTileKeys * kFuseTileKeys;
+}
+
+// fuse_min_qo: 0 appends every row; otherwise rows that the prefill kernel
+// writes itself (see fused_from) are skipped.
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* pool,
                              const int32_t* append_indptr, const int32_t* page_indices,
                              const int32_t* kv_indptr, const int32_t* last_page_len, int batch,
                              int nnz_new, int Hkv, int head_dim, int64_t num_pages, int num_sms,
-                             int* err, cudaStream_t stream);
+                             int fuse_min_qo, int* err, cudaStream_t stream);
 
 struct DecodeArgs {
   const uint16_t* q;            // [nnz_qo][Hq][d]
@@ -90,6 +101,16 @@ struct PrefillArgs {
   int* dec_counter;             // persistent decode kernel: [0] work counter, [1] CTAs
                                 // finished; zero before a launch, reset to zero by it
   int sms;                      // SMs of the device (persistent grid size)
+  // Prefill append fused into the CTA-pair prefill kernel (the fused call
+  // only; fuse_min_qo == 0 otherwise).  For a prefill item of a request with
+  // qo_len >= fuse_min_qo, key tiles from fused_from(kv_len, qo_len) on are
+  // read from k_new / v_new (rows laid out like q) instead of the pool, and the
+  // item that holds a tile's first new token writes the tile's rows into their
+  // pages (pool_w).
+  const uint16_t* k_new;        // [nnz_qo][Hkv][d]
+  const uint16_t* v_new;
+  uint16_t* pool_w;
+  int fuse_min_qo;
 };
 // Rows of packed (token, head) a prefill tile holds.
 constexpr int kPrefillTileRows = 128;
@@ -121,6 +142,10 @@ struct LaunchSet {
   void* scratch;
   int* err;
   int sms;
+  // the fused call's new rows and the fusion threshold (see PrefillArgs)
+  const void* k_new;
+  const void* v_new;
+  int fuse_min_qo;
 };
 struct PlanLayout;
 // The kernels run in the order prefill, decode, softmax_merge; each after the

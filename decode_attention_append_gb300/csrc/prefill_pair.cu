@@ -21,12 +21,27 @@
 //                    K_1, V_1, ... into a ring of RS half-tile stages (16 KB)
 //   warp 9           CTA 0: MMA issuer for the pair; CTA 1: relays "my half of
 //                    stage s has landed" to CTA 0 (remote mbarrier arrive)
+//   warp 10          page writer of the fused append (below); idle otherwise
+//
+// Fused append ("Chunked prefill", #io-overhead: the chunk's new K/V are
+// written to the cache once; "Disaggregated prefill and decode", "KV
+// Messenger": they are valid in the pages once the step's attention has run).
+// In a fused append + attention call, key tiles of a request that lie wholly
+// in its chunk -- from the first 128-aligned key at or after the cached prefix
+// -- are loaded straight from k_new / v_new (rows laid out like q) instead of
+// from the pages, so they need not wait for the append kernel, and the item
+// holding a tile's first new token also writes the tile's rows into their
+// pages from shared memory (warp 10); the append kernel skips those rows.  The
+// tile that holds both cached and new keys (when the prefix is not a multiple
+// of 128 keys) is still read from the pages after the append.
 // Tensor memory per CTA: S_q / P_q at q*128, O_q at 256 + q*128 (512 columns).
 // Completion of the pair's MMAs is committed to the barriers of both CTAs
 // (multicast); both CTAs' softmax warps hand P to CTA 0's issuer by arriving on
 // its p_full barrier.  Every tcgen05 instruction of this kernel uses
 // cta_group::2, as the instruction set requires within one kernel.
 #include <cuda.h>
+
+#include <climits>
 
 #include "launch.h"
 #include "ptx.cuh"
@@ -41,6 +56,8 @@ constexpr int kRows = kPrefillTileRows;
 struct __align__(64) PairParams {
   CUtensorMap tmap_q;   // q viewed as [nnz_qo][Hq][d], box {64, g, 128/g}
   CUtensorMap tmap_kv;  // pool viewed as [num_pages*2*Hkv][P][d], box {64, P, 1}
+  CUtensorMap tmap_kn;  // k_new viewed as [nnz_qo][Hkv][d], box {64, 1, 64} (fused append)
+  CUtensorMap tmap_vn;  // v_new, the same view, box {64, 1, 128}
   PrefillArgs a;
   const PrefillTile* tiles;
 };
@@ -117,8 +134,8 @@ __device__ __forceinline__ void commit_pair(uint64_t* bar) {
 
 struct PairCfg {
   static constexpr int D = 128, KT = 128, PPT = KT / kP;
-  static constexpr int THREADS = 320;
-  static constexpr int PRODUCER = 8, MMA = 9;
+  static constexpr int THREADS = 352;
+  static constexpr int PRODUCER = 8, MMA = 9, WRITER = 10;
   static constexpr int Q_BYTES = kRows * D * 2;           // one 128-row Q tile (32 KB)
   static constexpr int H_BYTES = KT * D;                  // half of a K or V tile (16 KB)
   static constexpr int BUDGET = 231424;
@@ -189,14 +206,34 @@ prefill_pair_kernel(const __grid_constant__ PairParams prm) {
   const int npages_req = (tile.kv_len + kP - 1) / kP;
   const bool last_partial = tile.kv_len - (kt0 + n_kt - 1) * KT < KT;
 
+  // fused append: key tiles from fuse_key on are the chunk's own keys, read
+  // from k_new / v_new; this item writes into the pages each such tile whose
+  // first new token (kb - first_new_key) is one of its own tokens, so every
+  // new row is written once per kv head
+  const int first_new_key = tile.kv_len - tile.qo_len;
+  const bool fuse = a.fuse_min_qo > 0 && !prefix_group && tile.qo_len >= a.fuse_min_qo;
+  const int fuse_key = fuse ? fused_from(tile.kv_len, tile.qo_len) : INT_MAX;
+  auto owns = [&](int j) {
+    const int kb = (kt0 + j) * KT, t = kb - first_new_key;
+    return kb >= fuse_key && t >= tile.tok0 && t < tile.tok0 + tile.ntok;
+  };
+  const int own_lo = max(fuse_key, first_new_key + tile.tok0);  // first key whose tile it may own
+  const bool writer_on =
+      fuse && (own_lo + KT - 1) / KT * KT < first_new_key + tile.tok0 + tile.ntok;
+
   if (tid == 0) {
     prefetch_tmap(&prm.tmap_q);
     prefetch_tmap(&prm.tmap_kv);
+    if (fuse) {
+      prefetch_tmap(&prm.tmap_kn);
+      prefetch_tmap(&prm.tmap_vn);
+    }
     mbar_init(q_full, 1);
     mbar_init(q_peer, 1);
     for (int i = 0; i < RS; ++i) {
       mbar_init(&ring_full[i], 1);
-      mbar_init(&ring_empty[i], 1);
+      // MMA completion, plus the page writer once it has copied the stage out
+      mbar_init(&ring_empty[i], writer_on ? 2 : 1);
       mbar_init(&peer_full[i], 1);
     }
     for (int q = 0; q < 2; ++q) {
@@ -252,14 +289,41 @@ prefill_pair_kernel(const __grid_constant__ PairParams prm) {
     for (int i = 0; i < 2 * n_kt; ++i) {
       const int st = i % RS;
       const bool is_v = i & 1;
-      const int pg0 = (kt0 + (i >> 1)) * PPT;
-      if (!dep_waited && (kt0 + (i >> 1) + 1) * KT > first_new) {
+      const int kb = (kt0 + (i >> 1)) * KT;
+      const int pg0 = kb / kP;
+      uint8_t* buf = smem + C::OFF_RING + st * C::H_BYTES;
+      if (kb >= fuse_key) {
+        // the chunk's own keys, from k_new / v_new (row = q_row0 + key - first
+        // new key); rows past the request's end are other requests' rows or
+        // zero fill, masked like stale slots
+        if (lane == 0) {
+          if (i >= RS) mbar_wait(&ring_empty[st], ((i / RS) - 1) & 1, a.err);
+          mbar_arrive_expect_tx(&ring_full[st], (uint32_t)C::H_BYTES);
+          const int row = tile.q_row0 + (kb - first_new_key);
+          if (is_v) {
+            tma_load_3d(buf, &prm.tmap_vn, (int)rank * 64, kvh, row, &ring_full[st]);
+          } else {
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+              tma_load_3d(buf + b * (64 * 128), &prm.tmap_kn, b * 64, kvh, row + 64 * (int)rank,
+                          &ring_full[st]);
+          }
+        }
+        __syncwarp();
+        if (is_v) {  // tile done: shift the id pipeline
+          id0 = id1;
+          id1 = id2;
+          id2 = id3;
+          id3 = load_ids((i >> 1) + 4);
+        }
+        continue;
+      }
+      if (!dep_waited && kb + KT > first_new) {
         grid_dep_wait();
         dep_waited = true;
       }
       const int np = min(PPT, npages_req - pg0);
       const int kp = max(0, min(4, np - 4 * (int)rank));  // pages of this CTA's K half
-      uint8_t* buf = smem + C::OFF_RING + st * C::H_BYTES;
       if (lane == 0) {
         if (i >= RS) mbar_wait(&ring_empty[st], ((i / RS) - 1) & 1, a.err);
         mbar_arrive_expect_tx(&ring_full[st], (uint32_t)((is_v ? np : 2 * kp) * kP * 128));
@@ -290,10 +354,11 @@ prefill_pair_kernel(const __grid_constant__ PairParams prm) {
         id3 = load_ids((i >> 1) + 4);
       }
     }
-    // a prefix-group item reads no appended row but still waits before it
-    // exits: a launch may hold nothing else, and the kernels after it rely on
-    // its completion implying that of the kernel before it
-    if (prefix_group && !dep_waited) grid_dep_wait();
+    // an item that read no appended row from the pages (a prefix-group item,
+    // or one whose new keys all came from k_new) still waits before it exits:
+    // a launch may hold nothing else, and the kernels after it rely on its
+    // completion implying that of the kernel before it
+    if (!dep_waited) grid_dep_wait();
     __syncwarp();
     if (last_partial) {
       // this CTA's half of the last V tile: rows past the request's last key
@@ -399,6 +464,75 @@ prefill_pair_kernel(const __grid_constant__ PairParams prm) {
       commit(&ring_empty[sv]);
       if (j + 1 < n_kt) commit(&ring_empty[sk]);
     }
+  } else if (warp == C::WRITER) {
+    // ----------------------------------------------------- page writer
+    // Fused append: write this CTA's part of every owned tile from shared
+    // memory into the pages (K: keys [64 r, 64 r + 64) of the tile, both
+    // 64-column halves; V: all 128 keys, columns [64 r, 64 r + 64)).  A page
+    // whose 16 slots are all keys of the request goes out as TMA stores of the
+    // same {64, 16, 1} boxes the loads use (the TMA unit undoes the 128-byte
+    // swizzle); the request's partial last page goes out row by row with plain
+    // stores (16-byte chunk c of stage row R sits at chunk c ^ (R % 8)), so no
+    // slot at or past kv_len is written.  The writer releases every ring stage
+    // (ring_empty counts it) once its stores have read the stage.
+    if (writer_on) {
+      for (int i = 0; i < 2 * n_kt; ++i) {
+        const int st = i % RS;
+        mbar_wait(&ring_full[st], (i / RS) & 1, a.err);
+        if (owns(i >> 1)) {
+          const uint8_t* buf = smem + C::OFF_RING + st * C::H_BYTES;
+          const bool is_v = i & 1;
+          const int kb = (kt0 + (i >> 1)) * KT;
+          const int key0 = is_v ? kb : kb + 64 * (int)rank;  // first key of this CTA's part
+          const int npg = is_v ? 8 : 4;                       // pages of this CTA's part
+          // lane l < npg: page l of the part
+          int64_t page = -1;
+          int keys = 0;  // keys of the request on page l
+          if (lane < npg) {
+            keys = min(kP, tile.kv_len - (key0 + lane * kP));
+            if (keys > 0) {
+              page = __ldg(a.page_indices + tile.page_base + key0 / kP + lane);
+              if (page < 0 || page >= a.num_pages) {
+                set_device_error(a.err, kDevErrPageRange);
+                page = -1;
+              }
+            }
+          }
+          if (page >= 0 && keys == kP) {
+            const int32_t slice = (int32_t)((page * 2 + (is_v ? 1 : 0)) * a.Hkv + kvh);
+            if (is_v) {
+              tma_store_3d(&prm.tmap_kv, (int)rank * 64, 0, slice, buf + lane * (kP * 128));
+            } else {
+#pragma unroll
+              for (int b = 0; b < 2; ++b)
+                tma_store_3d(&prm.tmap_kv, b * 64, 0, slice, buf + b * (64 * 128) + lane * (kP * 128));
+            }
+            bulk_commit();
+          }
+          // the partial last page (at most one per part): plain stores
+          const uint32_t part_mask = __ballot_sync(0xffffffffu, page >= 0 && keys < kP);
+          if (part_mask) {
+            const int pl = __ffs(part_mask) - 1;
+            const int pkeys = __shfl_sync(0xffffffffu, keys, pl);
+            const int64_t ppage = __shfl_sync(0xffffffffu, page, pl);
+            const int nch = is_v ? 8 : 16;  // 16-byte chunks per row of this part
+            uint16_t* row0 = a.pool_w + (((ppage * 2 + (is_v ? 1 : 0)) * a.Hkv + kvh) * kP) * D;
+            for (int idx = lane; idx < pkeys * nch; idx += 32) {
+              const int sl = idx / nch, ch = idx - sl * nch;
+              const int b = is_v ? 0 : ch >> 3, cc = ch & 7;
+              const int R = pl * kP + sl;  // row within this CTA's panel
+              const uint4 v = *reinterpret_cast<const uint4*>(buf + b * (64 * 128) + R * 128 +
+                                                              ((cc ^ (R & 7)) << 4));
+              reinterpret_cast<uint4*>(row0 + sl * D)[(is_v ? (int)rank : b) * 8 + cc] = v;
+            }
+          }
+          if (page >= 0 && keys == kP) bulk_wait_read();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring_empty[st]);
+      }
+      bulk_wait_all();
+    }
   } else if (warp / 4 < nq) {
     // ------------------------------------------------------------- softmax
     // Every warp of a live tile pair runs (rows past the item's tokens compute
@@ -494,6 +628,21 @@ cudaError_t launch_prefill_pair(const PrefillArgs& a, cudaStream_t stream, bool 
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
+  }
+  if (a.fuse_min_qo > 0) {
+    // the fused call's new rows: [nnz_qo][Hkv][d], K boxes of 64 rows (this
+    // CTA's half of a key tile), V boxes of 128 rows
+    for (int v = 0; v < 2; ++v) {
+      cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.Hkv, (cuuint64_t)a.nnz_qo};
+      cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.Hkv * D * 2};
+      cuuint32_t box[3] = {64, 1, v ? 128u : 64u};
+      cuuint32_t es[3] = {1, 1, 1};
+      if (enc(v ? &prm.tmap_vn : &prm.tmap_kn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+              (void*)(v ? a.v_new : a.k_new), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
   }
   // the draft-tree variant only when the call carries a mask
   auto kern = a.tree_mask ? prefill_pair_kernel<true> : prefill_pair_kernel<false>;

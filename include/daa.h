@@ -189,6 +189,18 @@ daa_status daa_batch_attention(const void* q, const void* kv_pages, const int32_
  * launches, so their set-up and the key splits that read only cached rows
  * overlap the append (the CTAs that read an appended row wait for it).
  *
+ * The append of long prefill chunks is fused into their attention ("Chunked
+ * prefill", #io-overhead: the chunk's K/V are written to the cache once).  For
+ * head_dim 128, a request with more new tokens than two 128-row tiles of packed
+ * (token, query head) rows hold (qo_len > 2 * (128 / (Hq / Hkv))) runs on the
+ * CTA-pair prefill kernel.  Its key tiles that lie wholly in the chunk -- keys
+ * from the first multiple of 128 at or after kv_len - qo_len -- are read by
+ * that kernel straight from k_new / v_new, and written into their pages by it
+ * from the same tiles; the append kernel writes only the other rows.  The
+ * pages end up with exactly the bytes the plain append writes.
+ * daa_set_prefill_append_fusion(0) turns this off (every row then goes
+ * through the append kernel and is read back from the pages).
+ *
  *  k_new, v_new   device, bf16 [nnz_qo][Hkv][head_dim]
  *  kv_pages       device, bf16 pool, written (the appended rows) and read
  *  other arguments as daa_batch_attention, with the same workspace size
@@ -204,6 +216,21 @@ daa_status daa_append_attention(const void* k_new, const void* v_new, const void
                                 int32_t batch, int32_t causal, float sm_scale, void* out,
                                 float* lse_out, void* workspace, size_t workspace_bytes,
                                 daa_dims dims, void* stream);
+
+/*
+ * Switch of the fused prefill append of daa_append_attention,
+ * daa_append_attention_shared_prefix and daa_append_attention_run ("Chunked
+ * prefill", #io-overhead; see daa_append_attention): 1 (the default) lets the
+ * CTA-pair prefill kernel read its chunk's own key tiles from k_new / v_new and
+ * write them into the pages; 0 appends every row with the append kernel.
+ * Results (pool bytes, out, lse_out) are identical; only the work differs.
+ * Process-wide; takes effect for calls made after it returns.
+ * Errors: DAA_ERR_INVALID_ARG for a value other than 0 or 1.
+ */
+daa_status daa_set_prefill_append_fusion(int32_t enable);
+
+/* The current setting of daa_set_prefill_append_fusion (0 or 1). */
+int32_t daa_prefill_append_fusion(void);
 
 /*
  * Mixed-batch paged attention under draft-tree masks, for verifying the draft

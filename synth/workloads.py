@@ -434,7 +434,7 @@ def make_tree_workload(name, Hq, Hkv, d, P, seed, trees, decodes=(), prompts=(),
 
 CONFIG_NAMES = ["tiny_mixed", "mha_decode", "chunked_prefill_mixed", "gqa_decode_shard", "long_prefill"]
 # further workloads beyond the five configurations
-EXTRA_NAMES = ["prefix_shared", "tree_verify"]
+EXTRA_NAMES = ["prefix_shared", "tree_verify", "long_prefill_d64", "first_chunk_prefill"]
 
 
 def make_workload(name: str) -> Workload:
@@ -508,6 +508,26 @@ def make_workload(name: str) -> Workload:
                                   description="32 verify requests, each a 64-node draft tree "
                                               "(random recursive tree) over kv ~ U[1024,4096] cached "
                                               "tokens under its tree mask; Hq 32 / Hkv 8, d 128, P 16")
+    if name == "long_prefill_d64":
+        # the long-prompt prefill batch at head_dim 64 (small-model heads, as
+        # in the tiny mixed batch): prefill items run the single-CTA
+        # tensor-core kernel instead of CTA pairs
+        seed = 1008
+        g = torch.Generator().manual_seed(seed)
+        kv = torch.randint(1024, 8192 + 1, (32,), generator=g).tolist()
+        return _single_step(name, 32, 4, 64, 16, seed, [(4096, 8192)] * 4, kv,
+                            description="4 prompts of 8192 at chunk 2 of 2 (4096 new over 4096 "
+                                        "cached) + 32 decodes kv ~ U[1024,8192]; Hq 32 / Hkv 4, d 64")
+    if name == "first_chunk_prefill":
+        # "Chunked prefill", #core-idea: the first chunk of a prompt has no
+        # cached prefix, so every key the chunk attends to is appended in the
+        # same step; 4 prompts' first 8192-token chunks + 64 decodes, GQA 64/8
+        seed = 1009
+        g = torch.Generator().manual_seed(seed)
+        kv = torch.randint(2048, 16384 + 1, (64,), generator=g).tolist()
+        return _single_step(name, 64, 8, 128, 16, seed, [(8192, 8192)] * 4, kv,
+                            description="first 8192-token chunks of 4 prompts (nothing cached) "
+                                        "+ 64 decodes kv ~ U[2048,16384]; Hq 64 / Hkv 8, d 128")
     raise KeyError(name)
 
 

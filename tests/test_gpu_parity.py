@@ -203,12 +203,16 @@ def test_long_prefill_sampled_rows(dev):
     decode_rows = list(range(4 * qo, 4 * qo + 64))
     sel = sorted(set(prompt_rows)) + decode_rows
     assert len(set(r // tpt for r in prompt_rows if r < qo)) == qo // tpt
-    _run_both(wl, dev, sel_rows=sel)
+    # the fused call, as the benchmark runs it: the prompts' new key tiles come
+    # from k_new / v_new and are written into the pages by the prefill kernel
+    _run_both(wl, dev, sel_rows=sel, fused=True)
 
 
-def test_chunked_vs_one_shot_gpu(dev):
+@pytest.mark.parametrize("fused", [False, True])
+def test_chunked_vs_one_shot_gpu(dev, fused):
     """#correctness on the GPU: 4 chunks of 512 vs one 2048-token prefill give
-    a byte-identical cache and outputs within 1e-2."""
+    a byte-identical cache and outputs within 1e-2 (two calls, or the fused
+    call whose prefill kernel appends the chunk itself)."""
     from gpu_support import gpu_fill, gpu_step, new_pool, pool_bits
     wc = make_prompt_workload(2048, 512, 32, 8, 128, 16, 1003, decodes=[1500, 3000])
     wo = make_prompt_workload(2048, 2048, 32, 8, 128, 16, 1003)
@@ -217,8 +221,8 @@ def test_chunked_vs_one_shot_gpu(dev):
     pc, po = new_pool(wc, dev), new_pool(wo, dev)
     gpu_fill(wc, pc, dev)
     gpu_fill(wo, po, dev)
-    chunks = [gpu_step(wc, pc, k, dev)[0][:512] for k in range(4)]
-    one, _ = gpu_step(wo, po, 0, dev)
+    chunks = [gpu_step(wc, pc, k, dev, fused=fused)[0][:512] for k in range(4)]
+    one, _ = gpu_step(wo, po, 0, dev, fused=fused)
     pages = torch.from_numpy(wc.seqs[0].pages.astype(np.int64)).to(dev)
     assert np.array_equal(pool_bits(pc[pages]), pool_bits(po[pages]))
     diff = (torch.cat(chunks, 0).double() - one.double()).abs().max().item()
@@ -251,6 +255,63 @@ def test_append_attention_equals_two_calls(dev, case):
         assert torch.equal(oa.view(torch.int16), ob.view(torch.int16)), f"step {k}: out differs"
         assert torch.equal(la, lb), f"step {k}: lse differs"
     assert np.array_equal(pool_bits(pa), pool_bits(pb))
+
+
+FUSED_PREFILL = [
+    # (seed, Hq, Hkv, [(qo, kv), ...], causal): head_dim 128 prefill requests on
+    # the CTA-pair kernel with their append fused in.  Cached prefixes that are
+    # whole 128-key tiles (every new tile read from k_new) and that are not (the
+    # tile holding both cached and new keys is read from the pages after the
+    # append); ragged last tiles; requests of several four-tile items; requests
+    # whose new keys never fill a whole 128-aligned tile (nothing fused); decode
+    # and short requests beside them.
+    (141, 32, 8, [(512, 2048), (300, 1000), (129, 129), (1, 3000), (40, 700)], True),  # g 4
+    (142, 64, 8, [(1000, 3000), (77, 207), (1, 500), (33, 33)], True),                # g 8
+    (143, 12, 1, [(333, 4000), (150, 150), (21, 600), (1, 900)], True),               # g 12
+    (144, 16, 1, [(600, 2500), (200, 1111), (1, 40)], True),                          # g 16
+    (145, 8, 8, [(700, 1700), (257, 300), (1, 64)], True),                            # g 1
+    (146, 32, 8, [(300, 900), (513, 513), (1, 100)], False),                          # not causal
+]
+
+
+@pytest.mark.parametrize("case", FUSED_PREFILL, ids=lambda c: f"seed{c[0]}")
+def test_fused_prefill_append(dev, case):
+    """The fused call with the prefill kernel appending its chunk's own key
+    tiles ("Chunked prefill", #io-overhead): pool bytes bit-exact against the
+    oracle's append (and sentinel pages untouched), outputs within tolerance."""
+    import decode_attention_append_gb300 as daa
+    seed, Hq, Hkv, reqs, causal = case
+    assert daa.prefill_append_fusion()
+    wl = make_random_workload(seed, Hq, Hkv, 128, 16, reqs, extra_pages=9)
+    wl.causal = causal
+    _run_both(wl, dev, fused=True)
+
+
+@pytest.mark.parametrize("case", [FUSED_PREFILL[0], FUSED_PREFILL[2], FUSED_PREFILL[5]],
+                         ids=lambda c: f"seed{c[0]}")
+def test_fused_prefill_append_matches_unfused_bitwise(dev, case):
+    """Fusion on and off run the same arithmetic on the same bits (a tile read
+    from k_new holds exactly the bytes the append writes): identical outputs,
+    LSE and pools."""
+    import decode_attention_append_gb300 as daa
+    from gpu_support import gpu_fill, gpu_step, new_pool, pool_bits
+    seed, Hq, Hkv, reqs, causal = case
+    wl = make_random_workload(seed, Hq, Hkv, 128, 16, reqs, extra_pages=9)
+    wl.causal = causal
+    res = []
+    try:
+        for on in (False, True):
+            daa.set_prefill_append_fusion(on)
+            pool = new_pool(wl, dev)
+            gpu_fill(wl, pool, dev)
+            out, lse = gpu_step(wl, pool, 0, dev, fused=True)
+            res.append((out, lse, pool_bits(pool)))
+    finally:
+        daa.set_prefill_append_fusion(True)
+    (oa, la, pa), (ob, lb, pb) = res
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    assert torch.equal(la, lb)
+    assert np.array_equal(pa, pb)
 
 
 SHARED = [
