@@ -80,9 +80,11 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, uint32_t rank
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
 // The same without release semantics.  Used to hand P (in this CTA's tensor
-// memory) to CTA 0's issuer: the stores are already complete
+// memory) to CTA 0's issuer -- the stores are already complete
 // (tcgen05.wait::st, then tcgen05.fence::before_thread_sync), and the release
-// form measured ~800 clocks per arrive on this critical path.
+// form measured ~800 clocks per arrive on this critical path -- and to tell
+// CTA 0 that this CTA's half of a ring stage (its own TMA loads, observed
+// complete) has landed.
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint64_t* bar, uint32_t rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(rank));
@@ -383,7 +385,11 @@ prefill_pair_kernel(const __grid_constant__ PairParams prm) {
   } else if (warp == C::MMA && rank == 1) {
     // ------------------------------------------------------ relay (CTA 1)
     // CTA 0 issues MMAs that read this CTA's shared memory: tell it when each
-    // of this CTA's Q tiles and ring stages has landed.
+    // of this CTA's Q tiles and ring stages has landed.  The stage arrives are
+    // relaxed: the bytes are this CTA's own TMA loads, complete once its
+    // ring_full phase is observed, and this thread publishes no writes of its
+    // own.  The release form cost ~1100 clocks per ring item here, about two
+    // thirds of this warp's time, and CTA 0 waited on it.
     mbar_wait(q_full, 0, a.err);
     __syncwarp();
     if (lane == 0) mbar_arrive_cluster(q_peer, 0);
@@ -391,7 +397,7 @@ prefill_pair_kernel(const __grid_constant__ PairParams prm) {
       const int st = i % RS;
       mbar_wait(&ring_full[st], (i / RS) & 1, a.err);
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(&peer_full[st], 0);
+      if (lane == 0) mbar_arrive_cluster_relaxed(&peer_full[st], 0);
     }
   } else if (warp == C::MMA) {
     // ------------------------------------------------- MMA issuer (CTA 0)
