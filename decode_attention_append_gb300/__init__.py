@@ -57,6 +57,19 @@ class _Dims(ctypes.Structure):
                 ("num_pages", ctypes.c_int64)]
 
 
+class StepLayout(ctypes.Structure):
+    """daa_step_layout: byte offsets of a host step's sections in its packed buffer."""
+    _fields_ = [(n, ctypes.c_size_t) for n in ("qo_indptr", "kv_indptr", "page_indices", "last_page_len",
+                                               "q", "k_new", "v_new", "total")]
+
+
+class StepStreams(ctypes.Structure):
+    """daa_step_streams: the streams and events of one host step."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("upload_stream", "compute_stream", "download_stream",
+                                               "uploaded", "computed", "downloaded", "inputs_free",
+                                               "out_free")]
+
+
 class PlanInfo(ctypes.Structure):
     """daa_plan_info: the record of a plan uploaded by ``batch_attention_plan``."""
     _fields_ = [("words", ctypes.c_int64 * 24)]
@@ -114,6 +127,9 @@ def load_library():
         lib.daa_append_attention_run.restype = i32
         lib.daa_append_attention_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, pinfo, i32, f32, vp, vp,
                                                  vp, sz, _Dims, vp]
+        lib.daa_append_attention_host.restype = i32
+        lib.daa_append_attention_host.argtypes = [vp, vp, ctypes.POINTER(StepLayout), i32, i32, f32, vp, vp,
+                                                  vp, vp, sz, _Dims, ctypes.POINTER(StepStreams)]
         lib.daa_set_prefill_append_fusion.restype = i32
         lib.daa_set_prefill_append_fusion.argtypes = [i32]
         lib.daa_prefill_append_fusion.restype = i32
@@ -596,6 +612,93 @@ class BatchAttention:
                                workspace=self.workspace,
                                host_indptr=(t.h_qo_indptr, t.h_kv_indptr, t.h_last_page_len),
                                stream=stream, prefix_groups=self.prefix_groups)
+
+
+class HostStep:
+    """Serving steps fed from pinned host memory, one library call each
+    (``daa_append_attention_host``): upload the packed inputs, append +
+    attention, read the output back.  Two sets of device buffers alternate, so
+    step i + 1's upload and step i - 1's read-back overlap step i's kernels.
+
+    ``sections``: the step's host tensors by name -- qo_indptr, kv_indptr,
+    page_indices, last_page_len (int32) and q, k_new, v_new (bf16) -- packed
+    once into one pinned buffer (``pack``; refill it with ``update``).  The
+    page table must not change shape between steps (the workspace is sized for
+    it).  ``step(i)`` enqueues step i on the current stream (compute) and two
+    side streams; ``out(i)`` is step i's pinned output once ``done(i)`` has
+    completed."""
+
+    NAMES = ("qo_indptr", "kv_indptr", "page_indices", "last_page_len", "q", "k_new", "v_new")
+
+    def __init__(self, sections, kv_pages, num_qo_heads, causal=True, sm_scale=None, workspace=None):
+        lib = load_library()
+        self.lib = lib
+        dev = kv_pages.device
+        self.kv_pages = kv_pages
+        offs, at = {}, 0
+        for n in self.NAMES:
+            t = sections[n]
+            offs[n] = at
+            at += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.layout = StepLayout(*(offs[n] for n in self.NAMES), at)
+        self.offsets = offs
+        self.pack = torch.empty(at, dtype=torch.uint8, pin_memory=True)
+        self.update(sections)
+        hq, hk, hl = (sections[n].numpy() for n in ("qo_indptr", "kv_indptr", "last_page_len"))
+        self.batch = len(hq) - 1
+        q = sections["q"]
+        self.dims = _dims(kv_pages, num_qo_heads)
+        self.causal = int(bool(causal))
+        self.sm_scale = float(sm_scale if sm_scale is not None else 1.0 / float(q.shape[2]) ** 0.5)
+        if workspace is None:
+            need = _workspace_need(lib, _host_i32(hq), _host_i32(hk), _host_i32(hl), self.dims, None,
+                                   "HostStep")
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        self.workspace = workspace
+        self.d_inputs = [torch.empty(at, dtype=torch.uint8, device=dev) for _ in range(2)]
+        self.d_out = [torch.empty(q.shape, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.h_out = [torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
+        self.up = torch.cuda.Stream(device=dev)
+        self.down = torch.cuda.Stream(device=dev)
+        self.events = [[torch.cuda.Event() for _ in range(3)] for _ in range(2)]
+        cur = torch.cuda.current_stream(dev)
+        for evs in self.events:  # events are created on first record
+            for e in evs:
+                e.record(cur)
+        torch.cuda.synchronize(dev)
+        self._args = []
+        for k in range(2):
+            up_ev, comp_ev, down_ev = (e.cuda_event for e in self.events[k])
+            ss = StepStreams(self.up.cuda_stream, cur.cuda_stream, self.down.cuda_stream, up_ev, comp_ev,
+                             down_ev, comp_ev, down_ev)
+            self._args.append((ctypes.c_void_p(self.pack.data_ptr()),
+                               ctypes.c_void_p(self.d_inputs[k].data_ptr()), ctypes.byref(self.layout),
+                               self.batch, self.causal, ctypes.c_float(self.sm_scale),
+                               ctypes.c_void_p(kv_pages.data_ptr()), ctypes.c_void_p(self.d_out[k].data_ptr()),
+                               ctypes.c_void_p(self.h_out[k].data_ptr()),
+                               ctypes.c_void_p(self.workspace.data_ptr()),
+                               self.workspace.numel(), self.dims, ctypes.byref(ss), ss))
+        self._stream = cur
+
+    def update(self, sections):
+        """Copy the step's host tensors into the pinned pack (wait for the
+        previous step's ``uploaded`` event before calling this)."""
+        for n in self.NAMES:
+            t = sections[n].contiguous()
+            nb = t.numel() * t.element_size()
+            self.pack[self.offsets[n]:self.offsets[n] + nb].copy_(t.reshape(-1).view(torch.uint8))
+
+    def step(self, i):
+        """Enqueue step i (slot i % 2)."""
+        a = self._args[i & 1]
+        _check(self.lib.daa_append_attention_host(*a[:-1]), "append_attention_host")
+
+    def done(self, i):
+        """The event after which step i's output is in ``out(i)``."""
+        return self.events[i & 1][2]
+
+    def out(self, i):
+        return self.h_out[i & 1]
 
 
 def set_prefill_append_fusion(enable: bool) -> None:

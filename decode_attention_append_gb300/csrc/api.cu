@@ -372,6 +372,13 @@ size_t daa_batch_attention_shared_prefix_workspace_size(
 
 namespace {
 
+// Work a caller enqueues once the arguments have been checked and before the
+// call's own work (the host step's input upload); a failure is returned as is.
+struct BeforeEnqueue {
+  daa_status (*fn)(void* ctx);
+  void* ctx;
+};
+
 // Shared body of daa_batch_attention and daa_append_attention: validate, plan,
 // stage the plan, then (fused call) launch the append, then the attention.
 daa_status attention_call(const void* k_new, const void* v_new, const void* q,
@@ -383,7 +390,8 @@ daa_status attention_call(const void* k_new, const void* v_new, const void* q,
                           float* lse_out, void* workspace, size_t workspace_bytes,
                           const daa_dims& dims, void* stream, bool fused,
                           const uint32_t* tree_mask = nullptr, int32_t mask_words = 0,
-                          const PrefixGroups* groups = nullptr) {
+                          const PrefixGroups* groups = nullptr,
+                          const BeforeEnqueue* before = nullptr) {
   if (!(std::isfinite(sm_scale)) || !(sm_scale > 0.f)) return DAA_ERR_INVALID_ARG;
   HostPlan& pl = host_plan();
   daa_status st =
@@ -409,6 +417,10 @@ daa_status attention_call(const void* k_new, const void* v_new, const void* q,
   }
   if (!workspace || workspace_bytes < lay.total) return DAA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return DAA_ERR_ALIGNMENT;
+  if (before) {
+    st = before->fn(before->ctx);
+    if (st != DAA_OK) return st;
+  }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -657,6 +669,108 @@ daa_status daa_append_attention_run(const void* k_new, const void* v_new, const 
   return run_call(k_new, v_new, q, kv_pages, qo_indptr, kv_indptr, page_indices, last_page_len,
                   info, causal, sm_scale, out, lse_out, workspace, workspace_bytes, dims, stream,
                   true);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The host step's upload, enqueued by attention_call once every argument has
+// passed its checks: the packed inputs on the upload stream (after the
+// previous reader of the device copy), then the compute stream waits for them
+// and for the previous read-back of the output buffer.
+struct HostStepUpload {
+  const void* h_inputs;
+  void* d_inputs;
+  size_t bytes;
+  const daa_step_streams* ss;
+};
+
+daa_status host_step_upload(void* ctx) {
+  const HostStepUpload& u = *static_cast<const HostStepUpload*>(ctx);
+  cudaStream_t us = static_cast<cudaStream_t>(u.ss->upload_stream);
+  cudaStream_t cs = static_cast<cudaStream_t>(u.ss->compute_stream);
+  cudaEvent_t uploaded = static_cast<cudaEvent_t>(u.ss->uploaded);
+  if (u.ss->inputs_free &&
+      cudaStreamWaitEvent(us, static_cast<cudaEvent_t>(u.ss->inputs_free), 0) != cudaSuccess)
+    return DAA_ERR_CUDA;
+  if (cudaMemcpyAsync(u.d_inputs, u.h_inputs, u.bytes, cudaMemcpyHostToDevice, us) != cudaSuccess ||
+      cudaEventRecord(uploaded, us) != cudaSuccess || cudaStreamWaitEvent(cs, uploaded, 0) != cudaSuccess)
+    return DAA_ERR_CUDA;
+  if (u.ss->out_free &&
+      cudaStreamWaitEvent(cs, static_cast<cudaEvent_t>(u.ss->out_free), 0) != cudaSuccess)
+    return DAA_ERR_CUDA;
+  return DAA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+daa_status daa_append_attention_host(const void* h_inputs, void* d_inputs,
+                                     const daa_step_layout* layout, int32_t batch, int32_t causal,
+                                     float sm_scale, void* kv_pages, void* d_out, void* h_out,
+                                     void* workspace, size_t workspace_bytes, daa_dims dims,
+                                     const daa_step_streams* streams) {
+  if (!h_inputs || !d_inputs || !layout || !streams || !d_out || !h_out) return DAA_ERR_INVALID_ARG;
+  if (!streams->uploaded || !streams->computed || !streams->downloaded) return DAA_ERR_INVALID_ARG;
+  if (batch < 0) return DAA_ERR_INVALID_ARG;
+  daa_status st = plan_check_dims(dims);
+  if (st != DAA_OK) return st;
+  const daa_step_layout& L = *layout;
+  // every section inside the buffer; int32 sections 4-byte aligned, bf16 ones
+  // 16-byte aligned (the device copy starts on a 256-byte boundary)
+  if ((reinterpret_cast<uintptr_t>(d_inputs) & (kAlign - 1)) != 0) return DAA_ERR_ALIGNMENT;
+  const size_t ints[4] = {L.qo_indptr, L.kv_indptr, L.page_indices, L.last_page_len};
+  const size_t vecs[3] = {L.q, L.k_new, L.v_new};
+  for (size_t o : ints)
+    if (o % 4 != 0) return DAA_ERR_ALIGNMENT;
+  for (size_t o : vecs)
+    if (o % 16 != 0) return DAA_ERR_ALIGNMENT;
+  const uint8_t* h = static_cast<const uint8_t*>(h_inputs);
+  uint8_t* d = static_cast<uint8_t*>(d_inputs);
+  auto fits = [&](size_t off, size_t n) { return off <= L.total && n <= L.total - off; };
+  if (!fits(L.qo_indptr, 4 * ((size_t)batch + 1)) || !fits(L.kv_indptr, 4 * ((size_t)batch + 1)) ||
+      !fits(L.last_page_len, 4 * (size_t)batch))
+    return DAA_ERR_SHAPE;
+  const int32_t* h_qo = reinterpret_cast<const int32_t*>(h + L.qo_indptr);
+  const int32_t* h_kv = reinterpret_cast<const int32_t*>(h + L.kv_indptr);
+  const int32_t* h_last = reinterpret_cast<const int32_t*>(h + L.last_page_len);
+  if (batch > 0 && (h_qo[batch] < 0 || h_kv[batch] < 0)) return DAA_ERR_SHAPE;
+  const size_t nnz_qo = batch > 0 ? (size_t)h_qo[batch] : 0;
+  const size_t row_q = (size_t)dims.num_qo_heads * dims.head_dim * 2;
+  const size_t row_kv = (size_t)dims.num_kv_heads * dims.head_dim * 2;
+  if (!fits(L.page_indices, 4 * (size_t)(batch > 0 ? h_kv[batch] : 0)) || !fits(L.q, nnz_qo * row_q) ||
+      !fits(L.k_new, nnz_qo * row_kv) || !fits(L.v_new, nnz_qo * row_kv))
+    return DAA_ERR_SHAPE;
+  cudaStream_t us = static_cast<cudaStream_t>(streams->upload_stream);
+  cudaStream_t cs = static_cast<cudaStream_t>(streams->compute_stream);
+  cudaStream_t ds = static_cast<cudaStream_t>(streams->download_stream);
+  HostStepUpload up{h_inputs, d_inputs, L.total, streams};
+  BeforeEnqueue before{host_step_upload, &up};
+  if (nnz_qo == 0) {
+    // no query rows: nothing to compute or read back; the events still mark
+    // this step on their streams
+    if (cudaEventRecord(static_cast<cudaEvent_t>(streams->uploaded), us) != cudaSuccess ||
+        cudaEventRecord(static_cast<cudaEvent_t>(streams->computed), cs) != cudaSuccess ||
+        cudaEventRecord(static_cast<cudaEvent_t>(streams->downloaded), ds) != cudaSuccess)
+      return DAA_ERR_CUDA;
+    return DAA_OK;
+  }
+  st = attention_call(d + L.k_new, d + L.v_new, d + L.q, kv_pages,
+                      reinterpret_cast<const int32_t*>(d + L.qo_indptr),
+                      reinterpret_cast<const int32_t*>(d + L.kv_indptr),
+                      reinterpret_cast<const int32_t*>(d + L.page_indices),
+                      reinterpret_cast<const int32_t*>(d + L.last_page_len), h_qo, h_kv, h_last,
+                      batch, causal, sm_scale, d_out, nullptr, workspace, workspace_bytes, dims, cs,
+                      /*fused=*/true, nullptr, 0, nullptr, &before);
+  if (st != DAA_OK) return st;
+  cudaEvent_t computed = static_cast<cudaEvent_t>(streams->computed);
+  if (cudaEventRecord(computed, cs) != cudaSuccess || cudaStreamWaitEvent(ds, computed, 0) != cudaSuccess ||
+      cudaMemcpyAsync(h_out, d_out, nnz_qo * row_q, cudaMemcpyDeviceToHost, ds) != cudaSuccess ||
+      cudaEventRecord(static_cast<cudaEvent_t>(streams->downloaded), ds) != cudaSuccess)
+    return DAA_ERR_CUDA;
+  return DAA_OK;
 }
 
 daa_status daa_set_prefill_append_fusion(int32_t enable) {

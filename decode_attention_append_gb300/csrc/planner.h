@@ -418,14 +418,50 @@ daa_status plan_batch(const int32_t* qo, const int32_t* kv, const int32_t* last,
                         : std::min(t.key_hi, t.kv_len - t.qo_len + t.tok0 + toks);
     return (int64_t)(end - t.key_lo) * ntiles;
   };
-  std::sort(tiles.data(), tiles.data() + tiles.size(), [&](const PrefillTile& x, const PrefillTile& y) {
-    const int gx = group(x), gy = group(y);
-    if (gx != gy) return gx < gy;
-    const int64_t wx = work(x), wy = work(y);
-    if (wx != wy) return wx > wy;
+  // Sort keys computed once per item (a comparator that recomputes them made
+  // the sort most of the host time of a call: ~70 us for 362 items), then the
+  // items permuted in place.  Batches past the key buffer sort directly.
+  struct SortKey {
+    int64_t work;
+    int32_t group, q_row0, tok0, key_lo, idx, pad;
+  };
+  auto key_less = [](const SortKey& x, const SortKey& y) {
+    if (x.group != y.group) return x.group < y.group;
+    if (x.work != y.work) return x.work > y.work;
     if (x.q_row0 != y.q_row0) return x.q_row0 < y.q_row0;
     return x.tok0 != y.tok0 ? x.tok0 < y.tok0 : x.key_lo < y.key_lo;
-  });
+  };
+  constexpr int kMaxSortKeys = 16384;
+  thread_local SortKey sort_keys[kMaxSortKeys];
+  const int n_tiles = (int)tiles.size();
+  PrefillTile* td = tiles.data();
+  if (n_tiles <= kMaxSortKeys) {
+    for (int i = 0; i < n_tiles; ++i)
+      sort_keys[i] = SortKey{work(td[i]), group(td[i]), td[i].q_row0, td[i].tok0, td[i].key_lo, i, 0};
+    std::sort(sort_keys, sort_keys + n_tiles, key_less);
+    // position i takes item sort_keys[i].idx: follow each cycle of the
+    // permutation once, marking placed positions with idx = -1
+    for (int i = 0; i < n_tiles; ++i) {
+      if (sort_keys[i].idx < 0 || sort_keys[i].idx == i) continue;
+      const PrefillTile first = td[i];
+      int at = i;
+      while (true) {
+        const int from = sort_keys[at].idx;
+        sort_keys[at].idx = -1;
+        if (from == i) {
+          td[at] = first;
+          break;
+        }
+        td[at] = td[from];
+        at = from;
+      }
+    }
+  } else {
+    std::sort(td, td + n_tiles, [&](const PrefillTile& x, const PrefillTile& y) {
+      return key_less(SortKey{work(x), group(x), x.q_row0, x.tok0, x.key_lo, 0, 0},
+                      SortKey{work(y), group(y), y.q_row0, y.tok0, y.key_lo, 0, 0});
+    });
+  }
   for (size_t i = 0; i < tiles.size(); ++i) {
     const int gi = group(tiles.data()[i]);
     lay.n_dec_tiles += gi == 2 ? 1 : 0;

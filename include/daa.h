@@ -218,6 +218,67 @@ daa_status daa_append_attention(const void* k_new, const void* v_new, const void
                                 daa_dims dims, void* stream);
 
 /*
+ * One serving step fed from host memory: upload the step's inputs, run
+ * daa_append_attention on them, read the output back -- one call per step,
+ * every copy and kernel asynchronous, so consecutive steps overlap when the
+ * caller alternates two sets of device buffers.  It feeds the attention and
+ * the append as a serving loop does ("Accelerating Sonar through
+ * speculation", section "Inference with speculative decoding": a step's input
+ * tokens and KV page information are packed into one buffer on the host and
+ * the metadata is then copied to GPU memory).
+ *
+ * Inputs: one pinned host buffer `h_inputs` of layout->total bytes holding,
+ * at the byte offsets of `layout`, the step's qo_indptr, kv_indptr,
+ * page_indices, last_page_len (int32, 4-byte aligned offsets) and q, k_new,
+ * v_new (bf16, 16-byte aligned offsets), with the shapes of
+ * daa_append_attention.  The call reads the page table from this host buffer
+ * to plan (no device sync), copies the whole buffer to `d_inputs` (device,
+ * 256-byte aligned, layout->total bytes) on the upload stream, runs the append
+ * and the attention on the compute stream from the device copy, and copies
+ * out ([nnz_qo][Hq][head_dim] bf16 in `d_out`) back to `h_out` (pinned host)
+ * on the download stream.  `workspace` is that of daa_append_attention.
+ *
+ * Ordering (all cudaEvent_t / cudaStream_t, created by the caller):
+ *   upload:   waits for streams->inputs_free (if not NULL: the previous step
+ *             that read this d_inputs has finished computing), copies, records
+ *             streams->uploaded;
+ *   compute:  waits for uploaded and for streams->out_free (if not NULL: the
+ *             previous read-back of this d_out has finished), runs the kernels,
+ *             records streams->computed;
+ *   download: waits for computed, copies, records streams->downloaded.
+ * h_inputs must not change until `uploaded` has completed; h_out holds the
+ * output once `downloaded` has completed.  A batch with no query rows copies
+ * nothing and only records the three events.
+ *
+ * Errors: those of daa_append_attention, plus DAA_ERR_INVALID_ARG for a NULL
+ * buffer, layout, stream set or event, DAA_ERR_ALIGNMENT for misaligned
+ * offsets or d_inputs, DAA_ERR_SHAPE when a section runs past layout->total.
+ * All are found before anything is enqueued.
+ */
+typedef struct {
+  size_t qo_indptr, kv_indptr, page_indices, last_page_len; /* int32 sections */
+  size_t q, k_new, v_new;                                   /* bf16 sections */
+  size_t total;                                             /* bytes uploaded */
+} daa_step_layout;
+
+typedef struct {
+  void* upload_stream;   /* cudaStream_t */
+  void* compute_stream;  /* cudaStream_t */
+  void* download_stream; /* cudaStream_t */
+  void* uploaded;        /* cudaEvent_t, recorded by the call */
+  void* computed;        /* cudaEvent_t, recorded by the call */
+  void* downloaded;      /* cudaEvent_t, recorded by the call */
+  void* inputs_free;     /* cudaEvent_t waited for, or NULL */
+  void* out_free;        /* cudaEvent_t waited for, or NULL */
+} daa_step_streams;
+
+daa_status daa_append_attention_host(const void* h_inputs, void* d_inputs,
+                                     const daa_step_layout* layout, int32_t batch, int32_t causal,
+                                     float sm_scale, void* kv_pages, void* d_out, void* h_out,
+                                     void* workspace, size_t workspace_bytes, daa_dims dims,
+                                     const daa_step_streams* streams);
+
+/*
  * Switch of the fused prefill append of daa_append_attention,
  * daa_append_attention_shared_prefix and daa_append_attention_run ("Chunked
  * prefill", #io-overhead; see daa_append_attention): 1 (the default) lets the

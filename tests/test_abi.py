@@ -274,3 +274,38 @@ def test_binding_prefix_groups_and_plan_records(lib):
     assert daa.shared_prefix_workspace_size(qo, kv, last, ([0, 3], [256]), 8, 1, 128, 16, 256) > plain
     rec = daa.PlanInfo()
     assert ctypes.sizeof(rec) == 24 * 8
+
+
+def test_host_step_rejects_before_any_launch(lib):
+    """daa_append_attention_host checks its layout and handles on the host:
+    a NULL event, misaligned sections or device copy, sections past the
+    buffer, and the fused call's own errors -- all before enqueuing anything
+    (the device pointers here are never dereferenced)."""
+    import decode_attention_append_gb300 as daa
+    d = _dims()
+    # one request: 1 new token over 1 cached; qo, kv, pages, last, q, k, v
+    host = np.zeros(4096, np.uint8)
+    ints = host[:256].view(np.int32)
+    ints[0:2] = [0, 1]      # qo_indptr at 0
+    ints[16:18] = [0, 1]    # kv_indptr at 64
+    ints[32] = 7            # page_indices at 128
+    ints[48] = 2            # last_page_len at 192
+    lay = daa.StepLayout(0, 64, 128, 192, 256, 1280, 1536, 2048)
+    ev = [ctypes.c_void_p(0x100 + 8 * i) for i in range(3)]
+    ss = daa.StepStreams(None, None, None, ev[0], ev[1], ev[2], None, None)
+    hp = host.ctypes.data_as(ctypes.c_void_p)
+    dev = lambda x: ctypes.c_void_p(x)  # noqa: E731
+
+    def call(layout=lay, streams=ss, d_inputs=dev(0x100000), scale=0.125):
+        return lib.daa_append_attention_host(hp, d_inputs, ctypes.byref(layout), 1, 1, scale,
+                                             dev(0x200000), dev(0x300000), dev(0x400000),
+                                             dev(0x500000), 1 << 20, d, ctypes.byref(streams))
+    bad = daa.StepStreams(None, None, None, ev[0], None, ev[2], None, None)
+    assert call(streams=bad) == -1                                    # a NULL event
+    assert call(d_inputs=dev(0x100010)) == -7                         # device copy not 256-aligned
+    assert call(layout=daa.StepLayout(0, 64, 128, 194, 256, 1280, 1536, 2048)) == -7  # int32 offset
+    assert call(layout=daa.StepLayout(0, 64, 128, 192, 264, 1280, 1536, 2048)) == -7  # bf16 offset
+    assert call(layout=daa.StepLayout(0, 64, 128, 192, 256, 1280, 1536, 1600)) == -2  # v_new past the end
+    assert call(scale=0.0) == -1                                      # the fused call's own check
+    ints[48] = 0                                                      # last_page_len out of range
+    assert call() == -2
