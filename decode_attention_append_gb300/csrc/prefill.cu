@@ -441,9 +441,9 @@ template <class C>
 struct PersistLayout {
   static constexpr int RS = C::RS;
   // barriers after C::OFF_BAR, then two item slots and the TMEM address
-  static constexpr int NBAR = 2 + 2 * RS + 2 + 2 + 1 + 1 + 2 + 2;
-  static constexpr int OFF_SLOT = C::OFF_BAR + NBAR * 8;
-  static constexpr int OFF_TMEM = OFF_SLOT + 8;
+  static constexpr int NBAR = 2 + 2 * RS + 2 + 2 + 1 + 1 + 2 + 2 + 1;
+  static constexpr int OFF_SLOT = C::OFF_BAR + NBAR * 8;  // item slots [2], S-done count
+  static constexpr int OFF_TMEM = OFF_SLOT + 16;
   static constexpr int ALLOC = OFF_TMEM + 16 + 1024;
   static_assert(C::NQX == 1, "one Q tile per item");
   static_assert(ALLOC <= (C::MIN_BLOCKS == 1 ? 232448 : 115712), "shared memory budget");
@@ -471,7 +471,10 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
   uint64_t* o_free = o_done + 1;
   uint64_t* item_full = o_free + 1;       // [2]
   uint64_t* item_empty = item_full + 2;   // [2]
+  uint64_t* drained = item_empty + 2;     // the MMA warp's last MMAs have completed
   volatile int* item_slot = reinterpret_cast<volatile int*>(smem + PL::OFF_SLOT);  // [2]
+  // index of the last S tile known complete (-1: none), written by the MMA warp
+  volatile int* s_done_upto = item_slot + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + PL::OFF_TMEM);
 
   const int g = a.group;
@@ -495,6 +498,8 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
     }
     mbar_init(o_done, 1);
     mbar_init(o_free, 4);
+    mbar_init(drained, 1);
+    *s_done_upto = -1;
     fence_mbar_init();
   }
   if (warp == C::MMA) {
@@ -665,6 +670,14 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
         commit(&ring_empty[stage(ik)]);
         if (j == n_kt - 1) commit(q_empty);  // Q may be replaced
       };
+      // every S tile before this item has completed (the last one issued is
+      // S(j0 - 1); waiting for it is within one phase of s_full): publish that
+      // for the softmax warps that join this item after skipping others
+      if (j0 > 0) {
+        wait(&s_full[(j0 - 1) & 1], ((j0 - 1) >> 1) & 1);
+        if (lane == 0) *s_done_upto = j0 - 1;
+        __syncwarp();
+      }
       wait(q_full, k & 1);
       s_tile(0);
       if (n_kt > 1) s_tile(1);
@@ -696,6 +709,10 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
       r0 += 2 * n_kt;
       j0 += n_kt;
     }
+    // every MMA this warp issued has completed before the CTA frees its tensor
+    // memory, whatever the softmax warps have observed
+    commit(drained);
+    wait(drained, 0);
   } else {
     // ------------------------------------------------------------- softmax
     const int row = tid & 127;
@@ -714,6 +731,21 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
       // warp 0 always holds a real row; it arrives for the warps that do not
       const uint32_t cnt = warp == 0 ? (uint32_t)(5 - ge.act) : 1u;
       if (warp < ge.act) {
+        // A warp other than warp 0 skips the items that hold no row of its
+        // lanes, without waiting on their S tiles.  A parity wait must not run
+        // two phases ahead of its barrier, so before its first S wait here it
+        // waits until every S before this item is known complete (published by
+        // the MMA warp; a count, which cannot alias).
+        if (warp > 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (*s_done_upto < j0 - 1) {
+            if (global_timer_ns() - t0 > kWaitLimitNs ||
+                *reinterpret_cast<volatile int*>(a.err) == kDevErrBarrierTimeout) {
+              set_device_error(a.err, kDevErrBarrierTimeout);
+              break;
+            }
+          }
+        }
         const int tl = row / g;
         const int qpos = tile.kv_len - tile.qo_len + tile.tok0 + tl;
         const int row_end = min(a.causal ? min(qpos + 1, tile.kv_len) : tile.kv_len, ge.kend);
