@@ -443,7 +443,8 @@ struct PersistLayout {
   // barriers after C::OFF_BAR, then two item slots and the TMEM address
   static constexpr int NBAR = 2 + 2 * RS + 2 + 2 + 1 + 1 + 2 + 2 + 1;
   static constexpr int OFF_SLOT = C::OFF_BAR + NBAR * 8;  // item slots [2], S-done count
-  static constexpr int OFF_TMEM = OFF_SLOT + 16;
+  static constexpr int OFF_ITEM = OFF_SLOT + 16;          // the two slots' descriptors
+  static constexpr int OFF_TMEM = OFF_ITEM + 2 * (int)sizeof(PrefillTile);
   static constexpr int ALLOC = OFF_TMEM + 16 + 1024;
   static_assert(C::NQX == 1, "one Q tile per item");
   static_assert(ALLOC <= (C::MIN_BLOCKS == 1 ? 232448 : 115712), "shared memory budget");
@@ -475,6 +476,9 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
   volatile int* item_slot = reinterpret_cast<volatile int*>(smem + PL::OFF_SLOT);  // [2]
   // index of the last S tile known complete (-1: none), written by the MMA warp
   volatile int* s_done_upto = item_slot + 2;
+  // the descriptor of the unit in each mailbox slot, copied there by the
+  // producer, so the MMA and softmax warps start a unit without a global load
+  PrefillTile* item_tile = reinterpret_cast<PrefillTile*>(smem + PL::OFF_ITEM);  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + PL::OFF_TMEM);
 
   const int g = a.group;
@@ -542,11 +546,13 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
         const bool ok = k < 2 || mbar_wait(&item_empty[slot], ((k >> 1) - 1) & 1, a.err);
         unit = ok ? atomicAdd(a.dec_counter, 1) : n_units;
         item_slot[slot] = unit;
-        mbar_arrive(&item_full[slot]);
+        if (unit < n_units) item_tile[slot] = prm.tiles[unit / a.Hkv];
+        mbar_arrive(&item_full[slot]);  // release: the slot's writes precede it
       }
       unit = __shfl_sync(0xffffffffu, unit, 0);
       if (unit >= n_units) break;
-      const PrefillTile tile = prm.tiles[unit / a.Hkv];
+      __syncwarp();
+      const PrefillTile tile = item_tile[slot];
       const int kvh = unit % a.Hkv;
       const Geo ge = geometry(tile);
       const int n_kt = ge.n_kt;
@@ -650,10 +656,11 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
       const int slot = k & 1;
       const bool ok = wait(&item_full[slot], (k >> 1) & 1);
       const int unit = ok ? item_slot[slot] : n_units;
+      PrefillTile tile{};
+      if (unit < n_units) tile = item_tile[slot];  // read before the slot is released
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_empty[slot]);
       if (unit >= n_units) break;
-      const PrefillTile tile = prm.tiles[unit / a.Hkv];
       const Geo ge = geometry(tile);
       const int n_kt = ge.n_kt;
       auto stage = [&](int i) { return (int)((r0 + i) % RS); };
@@ -722,10 +729,11 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
       const int slot = k & 1;
       const bool ok = mbar_wait(&item_full[slot], (k >> 1) & 1, a.err);
       const int unit = ok ? item_slot[slot] : n_units;
+      PrefillTile tile{};
+      if (unit < n_units) tile = item_tile[slot];  // read before the slot is released
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_empty[slot]);
       if (unit >= n_units) break;
-      const PrefillTile tile = prm.tiles[unit / a.Hkv];
       const int kvh = unit % a.Hkv;
       const Geo ge = geometry(tile);
       // warp 0 always holds a real row; it arrives for the warps that do not
