@@ -179,17 +179,18 @@ std::vector<uint8_t>& staging() {
   return buf;
 }
 
-// Fused calls: whether the CTA-pair prefill kernel reads its chunk's own key
-// tiles from k_new / v_new and writes them into the pages itself (1, the
+// Fused calls: whether the prefill kernels read their chunk's own key tiles
+// from k_new / v_new and write them into the pages themselves (1, the
 // default), or the append kernel writes every row and the prefill reads them
 // back from the pages (0).  Results are identical either way.
 std::atomic<int> g_fuse_prefill_append{1};
 
 // The smallest qo_len whose rows the prefill kernel appends in a fused call:
-// requests planned as CTA-pair prefill items (head_dim 128, more rows than
-// two 128-row Q tiles hold); 0 when nothing is fused.
+// requests planned as prefill items (more rows than two 128-row Q tiles hold:
+// CTA-pair items for head_dim 128, single-CTA items for head_dim 64); 0 when
+// nothing is fused.
 int fuse_min_qo_for(const daa_dims& d) {
-  if (!g_fuse_prefill_append.load(std::memory_order_relaxed) || !plan_prefill_quads(d)) return 0;
+  if (!g_fuse_prefill_append.load(std::memory_order_relaxed)) return 0;
   const int g = d.num_qo_heads / d.num_kv_heads;
   return 2 * (kPrefillTileRows / g) + 1;
 }

@@ -101,7 +101,7 @@ struct PrefillArgs {
   int* dec_counter;             // persistent decode kernel: [0] work counter, [1] CTAs
                                 // finished; zero before a launch, reset to zero by it
   int sms;                      // SMs of the device (persistent grid size)
-  // Prefill append fused into the CTA-pair prefill kernel (the fused call
+  // Prefill append fused into the prefill kernels (the fused call
   // only; fuse_min_qo == 0 otherwise).  For a prefill item of a request with
   // qo_len >= fuse_min_qo, key tiles from fused_from(kv_len, qo_len) on are
   // read from k_new / v_new (rows laid out like q) instead of the pool, and the

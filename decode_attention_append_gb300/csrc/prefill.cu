@@ -18,6 +18,7 @@
 //   warp 8           TMA producer: Q tiles, then K_0, V_0, K_1, V_1, ... into a
 //                    ring of RS shared-memory stages (one 128-key tile each)
 //   warp 9           MMA issuer (one lane)
+//   warp 10          page writer of the fused append (below); idle otherwise
 // Tensor memory: S_q / P_q at q*KT, O_q at 2*KT + q*D (512 columns for pairs).
 //   S_q = Q_q K_j^T      A = Q (smem), B = K (smem), fp32 S in TMEM
 //   P_q (bf16) overwrites the first 64 columns of S_q (softmax, tcgen05.st)
@@ -32,9 +33,20 @@
 // more than 2^8) and rescales O in TMEM only then.  V rows past the request's
 // last key (stale slots, or pages not loaded) are zeroed by the producer
 // before the last PV so they cannot poison it.
+//
+// Fused append ("Chunked prefill", #io-overhead: the chunk's new K/V go to the
+// cache once; "Disaggregated prefill and decode", "KV Messenger": they are
+// valid in the pages once the step's attention has run).  In a fused append +
+// attention call, a prefill item's key tiles that lie wholly in its request's
+// chunk -- from the first 128-aligned key at or after the cached prefix --
+// are loaded straight from k_new / v_new (rows laid out like q) instead of
+// from the pages, so they need not wait for the append kernel; the item that
+// holds a tile's first new token also writes the tile's rows into their pages
+// from shared memory (warp 10), and the append kernel skips those rows.
 #include <cuda.h>
 
 #include <algorithm>
+#include <climits>
 
 #include "launch.h"
 #include "ptx.cuh"
@@ -50,6 +62,8 @@ struct __align__(64) PrefillParams {
   CUtensorMap tmap_q;     // q viewed as [nnz_qo][Hq][d], box {64, g, 128/g}
   CUtensorMap tmap_q1;    // the same view, box {64, g, 1} (one-token decode items)
   CUtensorMap tmap_kv;    // pool viewed as [num_pages*2*Hkv][P][d], box {64, P, 1}
+  CUtensorMap tmap_kn;    // k_new viewed as [nnz_qo][Hkv][d], box {64, 1, KT} (fused append)
+  CUtensorMap tmap_vn;    // v_new, the same view and box
   PrefillArgs a;
   const PrefillTile* tiles;
 };
@@ -65,9 +79,12 @@ struct TcCfg {
   static constexpr int D = D_, KT = KT_, NQX = NQX_, MIN_BLOCKS = MINB_;
   static constexpr int PPT = KT / kP;               // pages per K/V tile
   static constexpr int KB = D / 64;                 // 64-column (128-byte) blocks per row
-  static constexpr int THREADS = 32 * (4 * NQX + 2);
+  // prefill instantiations (Q-tile pairs) carry the fused append's page writer
+  static constexpr bool WRITES = NQX == 2;
+  static constexpr int THREADS = 32 * (4 * NQX + 2 + (WRITES ? 1 : 0));
   static constexpr int PRODUCER = 4 * NQX;          // warp ids
   static constexpr int MMA = 4 * NQX + 1;
+  static constexpr int WRITER = 4 * NQX + 2;        // when WRITES
   static constexpr int Q_BYTES = kRows * D * 2;
   static constexpr int T_BYTES = KT * D * 2;        // one K or V tile
   static constexpr int BUDGET = MINB_ == 1 ? 231424 : 114688;
@@ -168,13 +185,32 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
   const int act0 = (tile.ntok * g + 31) / 32;
   const int act1 = (tile.ntok1 * g + 31) / 32;
 
+  // fused append: key tiles from fuse_key on are the chunk's own keys, read
+  // from k_new / v_new; this item writes into the pages each such tile whose
+  // first new token (kb - first_new_key) is one of its own tokens, so every
+  // new row is written once per kv head
+  const int first_new_key = tile.kv_len - tile.qo_len;
+  const bool fuse = C::WRITES && a.fuse_min_qo > 0 && !prefix_group && tile.qo_len >= a.fuse_min_qo;
+  const int fuse_key = fuse ? fused_from(tile.kv_len, tile.qo_len) : INT_MAX;
+  auto owns = [&](int kt) {  // kt: key tile index
+    const int kb = kt * KT, t = kb - first_new_key;
+    return kb >= fuse_key && t >= tile.tok0 && t < tile.tok0 + ntok_all;
+  };
+  const int own_lo = max(fuse_key, first_new_key + tile.tok0);  // first key whose tile it may own
+  const bool writer_on = fuse && (own_lo + KT - 1) / KT * KT < first_new_key + tile.tok0 + ntok_all;
+
   if (tid == 0) {
     prefetch_tmap(one_token ? (const void*)&prm.tmap_q1 : (const void*)&prm.tmap_q);
     prefetch_tmap(&prm.tmap_kv);
+    if (fuse) {
+      prefetch_tmap(&prm.tmap_kn);
+      prefetch_tmap(&prm.tmap_vn);
+    }
     mbar_init(q_full, 1);
     for (int i = 0; i < RS; ++i) {
       mbar_init(&ring_full[i], 1);
-      mbar_init(&ring_empty[i], 1);
+      // MMA completion, plus the page writer once it has copied the stage out
+      mbar_init(&ring_empty[i], writer_on ? 2 : 1);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(&s_full[q], 1);
@@ -228,12 +264,29 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
       const int st = i % RS;
       const bool is_v = ring_is_v(i, nq, n_kt);
       const int pg0 = (kt0 + ring_tile(i, nq, n_kt)) * PPT;
+      uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
+      if (pg0 * kP >= fuse_key) {
+        // the chunk's own keys, from k_new / v_new (row = q_row0 + key - first
+        // new key); rows past the request's end are other requests' rows or
+        // zero fill, masked like stale slots
+        if (lane == 0) {
+          if (i >= RS) mbar_wait(&ring_empty[st], ((i / RS) - 1) & 1, a.err);
+          mbar_arrive_expect_tx(&ring_full[st], (uint32_t)L::T_BYTES);
+          const int row = tile.q_row0 + (pg0 * kP - first_new_key);
+#pragma unroll
+          for (int b = 0; b < L::KB; ++b)
+            tma_load_3d(buf + b * (KT * 128), is_v ? (const void*)&prm.tmap_vn : (const void*)&prm.tmap_kn,
+                        b * 64, kvh, row, &ring_full[st]);
+        }
+        __syncwarp();
+        pid = pid_next;
+        continue;
+      }
       if (!dep_waited && (pg0 / PPT + 1) * KT > first_new) {
         grid_dep_wait();
         dep_waited = true;
       }
       const int np = min(PPT, npages_req - pg0);
-      uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
       if (lane == 0) {
         if (i >= RS) mbar_wait(&ring_empty[st], ((i / RS) - 1) & 1, a.err);
         mbar_arrive_expect_tx(&ring_full[st], (uint32_t)(np * kP * D * 2));
@@ -253,11 +306,12 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
       }
       pid = pid_next;
     }
-    // a prefix-group item reads no appended row but still waits before it
-    // exits: a launch may hold nothing else, and the kernels after it rely on
-    // its completion implying that of the kernel before it.  (Key splits of
-    // cached rows need not: their request's last split waits.)
-    if (prefix_group && !dep_waited) grid_dep_wait();
+    // a prefix-group item reads no appended row, and a fused item may read
+    // none, but they still wait before they exit: a launch may hold nothing
+    // else, and the kernels after it rely on its completion implying that of
+    // the kernel before it.  (Key splits of cached rows need not: their
+    // request's last split waits.)
+    if ((prefix_group || fuse) && !dep_waited) grid_dep_wait();
     __syncwarp();
     if (last_partial) {
       // last V tile: rows past the request's last key must hold finite values
@@ -378,6 +432,69 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
         commit(&ring_empty[sv]);
         if (j + 1 < n_kt) commit(&ring_empty[sk]);
       }
+    }
+  } else if (C::WRITES && warp == C::WRITER) {
+    // ----------------------------------------------------- page writer
+    // Fused append: write every owned K or V tile from shared memory into the
+    // pages.  A page whose 16 slots are all keys of the request goes out as
+    // TMA stores of the same {64, 16, 1} boxes the loads use (the TMA unit
+    // undoes the 128-byte swizzle); the request's partial last page goes out
+    // row by row with plain stores (16-byte chunk c of stage row R sits at
+    // chunk c ^ (R % 8)), so no slot at or past kv_len is written.  The writer
+    // releases every ring stage (ring_empty counts it) once its stores have
+    // read the stage.
+    if (writer_on) {
+      for (int i = 0; i < 2 * n_kt; ++i) {
+        const int st = i % RS;
+        mbar_wait(&ring_full[st], (i / RS) & 1, a.err);
+        const int kt = kt0 + ring_tile(i, nq, n_kt);
+        if (owns(kt)) {
+          const uint8_t* buf = smem + L::OFF_RING + st * L::T_BYTES;
+          const bool is_v = ring_is_v(i, nq, n_kt);
+          const int key0 = kt * KT;
+          // lane l < PPT: page l of the tile
+          int64_t page = -1;
+          int keys = 0;  // keys of the request on page l
+          if (lane < PPT) {
+            keys = min(kP, tile.kv_len - (key0 + lane * kP));
+            if (keys > 0) {
+              page = __ldg(a.page_indices + tile.page_base + key0 / kP + lane);
+              if (page < 0 || page >= a.num_pages) {
+                set_device_error(a.err, kDevErrPageRange);
+                page = -1;
+              }
+            }
+          }
+          if (page >= 0 && keys == kP) {
+            const int32_t slice = (int32_t)((page * 2 + (is_v ? 1 : 0)) * a.Hkv + kvh);
+#pragma unroll
+            for (int b = 0; b < L::KB; ++b)
+              tma_store_3d(&prm.tmap_kv, b * 64, 0, slice, buf + b * (KT * 128) + lane * (kP * 128));
+            bulk_commit();
+          }
+          // the partial last page (at most one per tile): plain stores
+          const uint32_t part_mask = __ballot_sync(0xffffffffu, page >= 0 && keys < kP);
+          if (part_mask) {
+            const int pl = __ffs(part_mask) - 1;
+            const int pkeys = __shfl_sync(0xffffffffu, keys, pl);
+            const int64_t ppage = __shfl_sync(0xffffffffu, page, pl);
+            constexpr int nch = D / 8;  // 16-byte chunks per row
+            uint16_t* row0 = a.pool_w + (((ppage * 2 + (is_v ? 1 : 0)) * a.Hkv + kvh) * kP) * D;
+            for (int idx = lane; idx < pkeys * nch; idx += 32) {
+              const int sl = idx / nch, ch = idx - sl * nch;
+              const int b = ch >> 3, cc = ch & 7;
+              const int R = pl * kP + sl;  // row within the stage's panels
+              const uint4 v = *reinterpret_cast<const uint4*>(buf + b * (KT * 128) + R * 128 +
+                                                              ((cc ^ (R & 7)) << 4));
+              reinterpret_cast<uint4*>(row0 + sl * D)[ch] = v;
+            }
+          }
+          if (page >= 0 && keys == kP) bulk_wait_read();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring_empty[st]);
+      }
+      bulk_wait_all();
     }
   } else if (warp / 4 < nq && (warp & 3) < ((warp >> 2) == 0 ? act0 : act1)) {
     // ------------------------------------------------------------- softmax
@@ -851,6 +968,20 @@ cudaError_t launch_tc(const PrefillArgs& a, const PrefillTile* tiles, int n_tile
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
+  }
+  if (!kDecode && a.fuse_min_qo > 0) {
+    // the fused call's new rows: [nnz_qo][Hkv][d], boxes of one key tile
+    for (int v = 0; v < 2; ++v) {
+      cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.Hkv, (cuuint64_t)a.nnz_qo};
+      cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.Hkv * D * 2};
+      cuuint32_t box[3] = {64, 1, (cuuint32_t)C::KT};
+      cuuint32_t es[3] = {1, 1, 1};
+      if (enc(v ? &prm.tmap_vn : &prm.tmap_kn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+              (void*)(v ? a.v_new : a.k_new), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
   }
   // decode: a persistent grid of MIN_BLOCKS CTAs per SM (over all kv heads),
   // each taking items from the work counter; otherwise one CTA per item

@@ -190,14 +190,15 @@ daa_status daa_batch_attention(const void* q, const void* kv_pages, const int32_
  * overlap the append (the CTAs that read an appended row wait for it).
  *
  * The append of long prefill chunks is fused into their attention ("Chunked
- * prefill", #io-overhead: the chunk's K/V are written to the cache once).  For
- * head_dim 128, a request with more new tokens than two 128-row tiles of packed
- * (token, query head) rows hold (qo_len > 2 * (128 / (Hq / Hkv))) runs on the
- * CTA-pair prefill kernel.  Its key tiles that lie wholly in the chunk -- keys
- * from the first multiple of 128 at or after kv_len - qo_len -- are read by
- * that kernel straight from k_new / v_new, and written into their pages by it
- * from the same tiles; the append kernel writes only the other rows.  The
- * pages end up with exactly the bytes the plain append writes.
+ * prefill", #io-overhead: the chunk's K/V are written to the cache once).  A
+ * request with more new tokens than two 128-row tiles of packed (token, query
+ * head) rows hold (qo_len > 2 * (128 / (Hq / Hkv))) runs on a prefill kernel
+ * (CTA pairs for head_dim 128, one CTA per two tiles for head_dim 64).  Its
+ * key tiles that lie wholly in the chunk -- keys from the first multiple of 128
+ * at or after kv_len - qo_len -- are read by that kernel straight from k_new /
+ * v_new, and written into their pages by it from the same tiles; the append
+ * kernel writes only the other rows.  The pages end up with exactly the bytes
+ * the plain append writes.
  * daa_set_prefill_append_fusion(0) turns this off (every row then goes
  * through the append kernel and is read back from the pages).
  *
@@ -282,7 +283,7 @@ daa_status daa_append_attention_host(const void* h_inputs, void* d_inputs,
  * Switch of the fused prefill append of daa_append_attention,
  * daa_append_attention_shared_prefix and daa_append_attention_run ("Chunked
  * prefill", #io-overhead; see daa_append_attention): 1 (the default) lets the
- * CTA-pair prefill kernel read its chunk's own key tiles from k_new / v_new and
+ * prefill kernels read their chunk's own key tiles from k_new / v_new and
  * write them into the pages; 0 appends every row with the append kernel.
  * Results (pool bytes, out, lse_out) are identical; only the work differs.
  * Process-wide; takes effect for calls made after it returns.

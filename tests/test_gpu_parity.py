@@ -258,19 +258,23 @@ def test_append_attention_equals_two_calls(dev, case):
 
 
 FUSED_PREFILL = [
-    # (seed, Hq, Hkv, [(qo, kv), ...], causal): head_dim 128 prefill requests on
-    # the CTA-pair kernel with their append fused in.  Cached prefixes that are
-    # whole 128-key tiles (every new tile read from k_new) and that are not (the
-    # tile holding both cached and new keys is read from the pages after the
-    # append); ragged last tiles; requests of several four-tile items; requests
-    # whose new keys never fill a whole 128-aligned tile (nothing fused); decode
-    # and short requests beside them.
-    (141, 32, 8, [(512, 2048), (300, 1000), (129, 129), (1, 3000), (40, 700)], True),  # g 4
-    (142, 64, 8, [(1000, 3000), (77, 207), (1, 500), (33, 33)], True),                # g 8
-    (143, 12, 1, [(333, 4000), (150, 150), (21, 600), (1, 900)], True),               # g 12
-    (144, 16, 1, [(600, 2500), (200, 1111), (1, 40)], True),                          # g 16
-    (145, 8, 8, [(700, 1700), (257, 300), (1, 64)], True),                            # g 1
-    (146, 32, 8, [(300, 900), (513, 513), (1, 100)], False),                          # not causal
+    # (seed, Hq, Hkv, head_dim, [(qo, kv), ...], causal): prefill requests with
+    # their append fused in -- head_dim 128 on the CTA-pair kernel, head_dim 64
+    # on the single-CTA kernel.  Cached prefixes that are whole 128-key tiles
+    # (every new tile read from k_new) and that are not (the tile holding both
+    # cached and new keys is read from the pages after the append); ragged last
+    # tiles; requests of several items; requests whose new keys never fill a
+    # whole 128-aligned tile (nothing fused); decode and short requests beside
+    # them.
+    (141, 32, 8, 128, [(512, 2048), (300, 1000), (129, 129), (1, 3000), (40, 700)], True),  # g 4
+    (142, 64, 8, 128, [(1000, 3000), (77, 207), (1, 500), (33, 33)], True),                # g 8
+    (143, 12, 1, 128, [(333, 4000), (150, 150), (21, 600), (1, 900)], True),               # g 12
+    (144, 16, 1, 128, [(600, 2500), (200, 1111), (1, 40)], True),                          # g 16
+    (145, 8, 8, 128, [(700, 1700), (257, 300), (1, 64)], True),                            # g 1
+    (146, 32, 8, 128, [(300, 900), (513, 513), (1, 100)], False),                          # not causal
+    (147, 8, 4, 64, [(512, 2048), (300, 1000), (129, 129), (1, 3000), (40, 700)], True),   # g 2
+    (148, 32, 4, 64, [(1000, 3000), (77, 207), (1, 500), (33, 33), (17, 400)], True),     # g 8
+    (149, 8, 8, 64, [(700, 1700), (257, 300), (1, 64)], False),                            # g 1, not causal
 ]
 
 
@@ -280,14 +284,14 @@ def test_fused_prefill_append(dev, case):
     tiles ("Chunked prefill", #io-overhead): pool bytes bit-exact against the
     oracle's append (and sentinel pages untouched), outputs within tolerance."""
     import decode_attention_append_gb300 as daa
-    seed, Hq, Hkv, reqs, causal = case
+    seed, Hq, Hkv, d, reqs, causal = case
     assert daa.prefill_append_fusion()
-    wl = make_random_workload(seed, Hq, Hkv, 128, 16, reqs, extra_pages=9)
+    wl = make_random_workload(seed, Hq, Hkv, d, 16, reqs, extra_pages=9)
     wl.causal = causal
     _run_both(wl, dev, fused=True)
 
 
-@pytest.mark.parametrize("case", [FUSED_PREFILL[0], FUSED_PREFILL[2], FUSED_PREFILL[5]],
+@pytest.mark.parametrize("case", [FUSED_PREFILL[i] for i in (0, 2, 5, 6, 7)],
                          ids=lambda c: f"seed{c[0]}")
 def test_fused_prefill_append_matches_unfused_bitwise(dev, case):
     """Fusion on and off run the same arithmetic on the same bits (a tile read
@@ -295,8 +299,8 @@ def test_fused_prefill_append_matches_unfused_bitwise(dev, case):
     LSE and pools."""
     import decode_attention_append_gb300 as daa
     from gpu_support import gpu_fill, gpu_step, new_pool, pool_bits
-    seed, Hq, Hkv, reqs, causal = case
-    wl = make_random_workload(seed, Hq, Hkv, 128, 16, reqs, extra_pages=9)
+    seed, Hq, Hkv, d, reqs, causal = case
+    wl = make_random_workload(seed, Hq, Hkv, d, 16, reqs, extra_pages=9)
     wl.causal = causal
     res = []
     try:
