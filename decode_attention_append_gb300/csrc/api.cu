@@ -116,6 +116,9 @@ struct PlanRecord {
   int64_t num_qo_heads, num_kv_heads, head_dim, page_size, num_pages;
   int64_t batch, nnz_qo;
   PlanLayout lay;
+  // rows the append kernel of a fused run covers with the prefill append
+  // fused (append_span at the fusion threshold of these dims)
+  int32_t fused_span_begin, fused_span_end;
 };
 constexpr int64_t kPlanMagic = 0x4441415f504c414eLL;  // "DAA_PLAN"
 static_assert(sizeof(PlanRecord) <= sizeof(daa_plan_info), "daa_plan_info too small");
@@ -189,10 +192,12 @@ std::atomic<int> g_fuse_prefill_append{1};
 // requests planned as prefill items (more rows than two 128-row Q tiles hold:
 // CTA-pair items for head_dim 128, single-CTA items for head_dim 64); 0 when
 // nothing is fused.
-int fuse_min_qo_for(const daa_dims& d) {
-  if (!g_fuse_prefill_append.load(std::memory_order_relaxed)) return 0;
+int fuse_threshold(const daa_dims& d) {
   const int g = d.num_qo_heads / d.num_kv_heads;
   return 2 * (kPrefillTileRows / g) + 1;
+}
+int fuse_min_qo_for(const daa_dims& d) {
+  return g_fuse_prefill_append.load(std::memory_order_relaxed) ? fuse_threshold(d) : 0;
 }
 
 }  // namespace
@@ -341,7 +346,7 @@ daa_status daa_kv_append(const void* k_new, const void* v_new, void* kv_pages,
   int* err = device_error_word();
   cudaError_t e = traced(kKernelAppend, s, [&] {
     return launch_kv_append(k_new, v_new, kv_pages, append_indptr, page_indices, kv_indptr,
-                            last_page_len, batch, nnz_new, dims.num_kv_heads, dims.head_dim,
+                            last_page_len, batch, 0, nnz_new, dims.num_kv_heads, dims.head_dim,
                             dims.num_pages, num_sms(), /*fuse_min_qo=*/0, err, s);
   });
   return e == cudaSuccess ? DAA_OK : DAA_ERR_CUDA;
@@ -433,12 +438,18 @@ daa_status attention_call(const void* k_new, const void* v_new, const void* q,
   const int nnz_qo = h_qo_indptr[batch];
   // the tree call never fuses (its mask path appends separately)
   const int fuse_min_qo = fused && !tree_mask ? fuse_min_qo_for(dims) : 0;
-  if (fused && nnz_qo > 0) {
+  // the append kernel covers only the rows the prefill kernels do not write
+  const AppendSpan span = fused ? append_span(h_qo_indptr, h_kv_indptr, h_last_page_len, batch,
+                                              dims.page_size, fuse_min_qo)
+                                : AppendSpan{0, 0};
+  const bool appended = span.end > span.begin;
+  if (appended) {
     int* err = device_error_word();
     cudaError_t e = traced(kKernelAppend, s, [&] {
       return launch_kv_append(k_new, v_new, const_cast<void*>(kv_pages), qo_indptr, page_indices,
-                              kv_indptr, last_page_len, batch, nnz_qo, dims.num_kv_heads,
-                              dims.head_dim, dims.num_pages, num_sms(), fuse_min_qo, err, s);
+                              kv_indptr, last_page_len, batch, span.begin, span.end - span.begin,
+                              dims.num_kv_heads, dims.head_dim, dims.num_pages, num_sms(),
+                              fuse_min_qo, err, s);
     });
     if (e != cudaSuccess) return DAA_ERR_CUDA;
   }
@@ -462,7 +473,7 @@ daa_status attention_call(const void* k_new, const void* v_new, const void* q,
     ls.v_new = v_new;
     ls.fuse_min_qo = fuse_min_qo;
   }
-  return launch_all(ls, lay, s, /*trace=*/true, /*after_append=*/fused && nnz_qo > 0);
+  return launch_all(ls, lay, s, /*trace=*/true, /*after_append=*/appended);
 }
 
 }  // namespace
@@ -576,6 +587,10 @@ daa_status daa_batch_attention_plan(const int32_t* h_qo_indptr, const int32_t* h
   rec.batch = batch;
   rec.nnz_qo = batch > 0 ? h_qo_indptr[batch] : 0;
   rec.lay = lay;
+  const AppendSpan span = append_span(h_qo_indptr, h_kv_indptr, h_last_page_len, batch,
+                                      dims.page_size, fuse_threshold(dims));
+  rec.fused_span_begin = span.begin;
+  rec.fused_span_end = span.end;
   std::memcpy(info, &rec, sizeof(rec));
   return DAA_OK;
 }
@@ -615,12 +630,19 @@ daa_status run_call(const void* k_new, const void* v_new, const void* q, const v
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int nnz_qo = (int)rec.nnz_qo;
   const int fuse_min_qo = fused ? fuse_min_qo_for(dims) : 0;
-  if (fused && nnz_qo > 0) {
+  // rows the append kernel covers: those of the stored span with the fusion
+  // on, every row with it off
+  const AppendSpan span = !fused ? AppendSpan{0, 0}
+                          : fuse_min_qo > 0 ? AppendSpan{rec.fused_span_begin, rec.fused_span_end}
+                                            : AppendSpan{0, nnz_qo};
+  const bool appended = span.end > span.begin;
+  if (appended) {
     int* err = device_error_word();
     cudaError_t e = traced(kKernelAppend, s, [&] {
       return launch_kv_append(k_new, v_new, const_cast<void*>(kv_pages), qo_indptr, page_indices,
-                              kv_indptr, last_page_len, (int)rec.batch, nnz_qo, dims.num_kv_heads,
-                              dims.head_dim, dims.num_pages, num_sms(), fuse_min_qo, err, s);
+                              kv_indptr, last_page_len, (int)rec.batch, span.begin,
+                              span.end - span.begin, dims.num_kv_heads, dims.head_dim,
+                              dims.num_pages, num_sms(), fuse_min_qo, err, s);
     });
     if (e != cudaSuccess) return DAA_ERR_CUDA;
   }
@@ -642,7 +664,7 @@ daa_status run_call(const void* k_new, const void* v_new, const void* q, const v
     ls.v_new = v_new;
     ls.fuse_min_qo = fuse_min_qo;
   }
-  return launch_all(ls, lay, s, /*trace=*/true, /*after_append=*/fused && nnz_qo > 0);
+  return launch_all(ls, lay, s, /*trace=*/true, /*after_append=*/appended);
 }
 
 }  // namespace

@@ -39,13 +39,24 @@ __host__ __device__ inline int fused_from(int kv_len, int qo_len) {
   return (c + kFuseTileKeys - 1) / kFuseTileKeys * kFuseTileKeys;
 }
 
-// fuse_min_qo: 0 appends every row; otherwise rows that the prefill kernel
-// writes itself (see fused_from) are skipped.
+// Appends rows [row_begin, row_begin + n_rows) of k_new / v_new (all rows:
+// 0, nnz_new).  fuse_min_qo: 0 appends every row of that span; otherwise rows
+// that the prefill kernel writes itself (see fused_from) are skipped.
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* pool,
                              const int32_t* append_indptr, const int32_t* page_indices,
                              const int32_t* kv_indptr, const int32_t* last_page_len, int batch,
-                             int nnz_new, int Hkv, int head_dim, int64_t num_pages, int num_sms,
-                             int fuse_min_qo, int* err, cudaStream_t stream);
+                             int row_begin, int n_rows, int Hkv, int head_dim, int64_t num_pages,
+                             int num_sms, int fuse_min_qo, int* err, cudaStream_t stream);
+
+// The span of rows the append kernel of a fused call must cover: every row
+// except those the prefill kernels write (a request's new tokens from
+// fused_from on when qo_len >= fuse_min_qo).  Host side, from the host copies
+// of the lengths; begin == end when there is none.
+struct AppendSpan {
+  int begin, end;
+};
+AppendSpan append_span(const int32_t* h_qo_indptr, const int32_t* h_kv_indptr,
+                       const int32_t* h_last_page_len, int batch, int page_size, int fuse_min_qo);
 
 struct DecodeArgs {
   const uint16_t* q;            // [nnz_qo][Hq][d]

@@ -69,8 +69,11 @@ def test_runs_on_a_plan_match_planning_calls(dev, name, make, groups):
     assert daa.device_error(reset=True) == 0
 
 
-@pytest.mark.parametrize("groups", [False, True])
-def test_append_attention_run_matches_fused_call(dev, groups):
+@pytest.mark.parametrize("groups,fusion_at_run", [(False, True), (True, True), (False, False)])
+def test_append_attention_run_matches_fused_call(dev, groups, fusion_at_run):
+    """A fused run on a stored plan gives the bits of the fused call that plans
+    for itself, also when the prefill append fusion is switched off between the
+    plan and the run (the run's append then covers every row)."""
     wl = make_prefix_groups_workload("g504", 32, 8, 128, 16, 504,
                                      [("group", 512, [(1, 600 + 131 * i) for i in range(12)]),
                                       ("solo", 200, 700), ("solo", 1, 3000)])
@@ -81,7 +84,12 @@ def test_append_attention_run_matches_fused_call(dev, groups):
         if planned:
             runner.plan()
         lse = torch.empty(q.shape[0], wl.num_qo_heads, device=dev)
-        outs.append((runner.step(kn, vn, q, lse=lse), lse))
+        try:
+            if planned and not fusion_at_run:
+                daa.set_prefill_append_fusion(False)
+            outs.append((runner.step(kn, vn, q, lse=lse), lse))
+        finally:
+            daa.set_prefill_append_fusion(True)
         pools.append(pool)
     torch.cuda.synchronize()
     assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
