@@ -81,8 +81,20 @@ def step_accounting(wl, k=0):
     # prefill runs on CTA pairs (head_dim 128)
     short_max = 2 * (128 // wl.group_size) if wl.head_dim == 128 else verify_max
     ver_flops = ver_bytes = sh_flops = sh_bytes = 0
+    # rows the append kernel itself writes when the prefill kernels append
+    # their chunks' own key tiles (requests with qo_len > two Q tiles' tokens:
+    # new tokens from the first 128-aligned key at or after the cached prefix)
+    fuse_min = 2 * (128 // wl.group_size) + 1
+    app_rows_fused = 0
+    tree = False
     for r in wl.steps[k].requests:
         nnz_new += r.qo_len
+        tree = tree or r.parents is not None
+        keep = r.qo_len
+        if r.qo_len >= fuse_min:
+            cached = r.kv_len - r.qo_len
+            keep = min(r.qo_len, max(0, -(-cached // 128) * 128 - cached))
+        app_rows_fused += keep
         sq = wl.seqs[r.seq]
         kv_read = r.kv_len
         if sq.prefix >= 0:
@@ -118,6 +130,9 @@ def step_accounting(wl, k=0):
     tc_decode = wl.group_size >= TC_DECODE_MIN_GROUP
     return dict(decode_bytes=dec_bytes, append_bytes=app_bytes, prefill_flops=pre_flops,
                 prefill_bytes=pre_bytes, nnz_new=nnz_new,
+                # the append kernel's own bytes in a fused call (the tree call
+                # never fuses)
+                append_kernel_bytes_fused=app_bytes if tree else app_rows_fused * Hkv * d * 2 * 2 * 2,
                 # work per kernel
                 tc_flops=pre_flops - ver_flops - sh_flops, tc_bytes=pre_bytes - ver_bytes - sh_bytes,
                 short_flops=sh_flops, short_bytes=sh_bytes,
@@ -924,9 +939,14 @@ def make_entry(wl, name, m, args, world, unit):
             e["decode_frac_of_hbm"] = e["decode_gbs"] / hbm
             e["decode_kernel"] = kern
     if acc["append_bytes"] and "kv_append" in per_kernel:
-        # the append's own rate (latency bound for a few tokens per request)
+        # the append kernel's own rate (latency bound for a few tokens per
+        # request), over the rows it writes: with the prefill append fused,
+        # the prefill kernels write the long chunks' own key tiles
+        fused = args.api == "fused" and not args.no_fused_prefill_append
+        ab = acc["append_kernel_bytes_fused"] if fused else acc["append_bytes"]
         am = float(np.mean(per_kernel["kv_append"]))
-        e["append_gbs"] = acc["append_bytes"] / (am * 1e-3) / 1e9
+        e["append_kernel_bytes"] = ab
+        e["append_gbs"] = ab / (am * 1e-3) / 1e9
         e["append_frac_of_hbm"] = e["append_gbs"] / hbm
     return e
 
@@ -1022,7 +1042,7 @@ def main():
     import decode_attention_append_gb300 as daa
     daa.set_prefill_append_fusion(not args.no_fused_prefill_append)
     config["prefill_append"] = ("append kernel (every row)" if args.no_fused_prefill_append else
-                                "fused into the CTA-pair prefill kernel for long chunks")
+                                "fused into the prefill kernels for long chunks")
 
     # ---- the headline workload, with its clock window
     clocks = ClockSampler(local)
