@@ -29,6 +29,10 @@
 // A CTA with a single Q tile (decode splits, a request's last odd tile) instead
 // double-buffers S over both S regions, so S(j+1) is ready while softmax works
 // on tile j, and PV(j) is followed by S(j+2) into the buffer it just read.
+// V tiles of head_dim 128 are page-major in shared memory: one TMA box per
+// (page, head) slice lands as its two 64-column panels of 16 rows, and each
+// PV step of 16 keys reads one page (a K tile stays column-block-major, as
+// the S MMA's K-major operand needs, at two boxes per page).
 // Softmax keeps a lazily raised running max (raised only when it grows by
 // more than 2^8) and rescales O in TMEM only then.  V rows past the request's
 // last key (stale slots, or pages not loaded) are zeroed by the producer
@@ -57,6 +61,15 @@ namespace {
 
 constexpr int kP = 16;
 constexpr int kRows = kPrefillTileRows;  // 128 packed query rows per Q tile
+// 4-D tiled TMA load through a tensor map (coordinates innermost first).
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const void* tmap, int32_t c0, int32_t c1,
+                                            int32_t c2, int32_t c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
 
 struct __align__(64) PrefillParams {
   CUtensorMap tmap_q;     // q viewed as [nnz_qo][Hq][d], box {64, g, 128/g}
@@ -64,6 +77,7 @@ struct __align__(64) PrefillParams {
   CUtensorMap tmap_kv;    // pool viewed as [num_pages*2*Hkv][P][d], box {64, P, 1}
   CUtensorMap tmap_kn;    // k_new viewed as [nnz_qo][Hkv][d], box {64, 1, KT} (fused append)
   CUtensorMap tmap_vn;    // v_new, the same view and box
+  CUtensorMap tmap_vp;    // pool as [slices][half][P][64], box {64, P, 2, 1}: one page (d = 128)
   PrefillArgs a;
   const PrefillTile* tiles;
 };
@@ -190,7 +204,10 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
   // first new token (kb - first_new_key) is one of its own tokens, so every
   // new row is written once per kv head
   const int first_new_key = tile.kv_len - tile.qo_len;
-  const bool fuse = C::WRITES && a.fuse_min_qo > 0 && !prefix_group && tile.qo_len >= a.fuse_min_qo;
+  // (head_dim 64 only: head_dim-128 prefill runs on CTA pairs, and the short
+  // items here stay below the fusion threshold)
+  const bool fuse = C::WRITES && C::KB == 1 && a.fuse_min_qo > 0 && !prefix_group &&
+                    tile.qo_len >= a.fuse_min_qo;
   const int fuse_key = fuse ? fused_from(tile.kv_len, tile.qo_len) : INT_MAX;
   auto owns = [&](int kt) {  // kt: key tile index
     const int kb = kt * KT, t = kb - first_new_key;
@@ -299,10 +316,14 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
           page = 0;  // fetch a valid page instead; the output is undefined anyway
         }
         const int32_t slice = (int32_t)((page * 2 + (is_v ? 1 : 0)) * a.Hkv + kvh);
+        if (is_v && L::KB == 2) {  // the whole page in one box, page-major
+          tma_load_4d(buf + lane * (2 * kP * 128), &prm.tmap_vp, 0, 0, 0, slice, &ring_full[st]);
+        } else {
 #pragma unroll
-        for (int b = 0; b < L::KB; ++b)
-          tma_load_3d(buf + b * (KT * 128) + lane * (kP * 128), &prm.tmap_kv, b * 64, 0, slice,
-                      &ring_full[st]);
+          for (int b = 0; b < L::KB; ++b)
+            tma_load_3d(buf + b * (KT * 128) + lane * (kP * 128), &prm.tmap_kv, b * 64, 0, slice,
+                        &ring_full[st]);
+        }
       }
       pid = pid_next;
     }
@@ -323,7 +344,9 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
       for (int idx = lane; idx < nz * L::KB; idx += 32) {
         const int b = idx / nz, rem = idx - b * nz;
         const int r = tile_keys + (rem >> 3), ch = rem & 7;
-        *reinterpret_cast<uint4*>(buf + b * (KT * 128) + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+        uint8_t* at = L::KB == 2 ? buf + (r >> 4) * (2 * kP * 128) + b * (kP * 128) + (r & 15) * 128
+                                 : buf + b * (KT * 128) + r * 128;
+        *reinterpret_cast<uint4*>(at + ch * 16) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -357,11 +380,13 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
       }
       __syncwarp();
     };
-    // O (columns [ocol, ocol + D)) += P (bf16 in columns [pcol, pcol + KT/2)) V (ring stage st)
+    // O (columns [ocol, ocol + D)) += P (bf16 in columns [pcol, pcol + KT/2)) V (ring stage st;
+    // head_dim 128: page-major, page k's two 64-column panels 2 KB apart)
     auto issue_pv = [&](uint32_t ocol, uint32_t pcol, int st, bool accumulate) {
 #pragma unroll
       for (int k = 0; k < KT / 16; ++k) {
-        const uint64_t db = desc_mnmajor(sR + st * L::T_BYTES + k * (16 * 128), KT * 128);
+        const uint64_t db = L::KB == 2 ? desc_mnmajor(sR + st * L::T_BYTES + k * (2 * 16 * 128), 16 * 128)
+                                       : desc_mnmajor(sR + st * L::T_BYTES + k * (16 * 128), KT * 128);
         if (elect_one())
           tc_mma_ts(tmem + ocol, tmem + pcol + k * 8, db, idesc_o, (accumulate || k > 0) ? 1u : 0u);
       }
@@ -716,10 +741,14 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
             page = 0;  // fetch a valid page instead; the output is undefined anyway
           }
           const int32_t slice = (int32_t)((page * 2 + (is_v ? 1 : 0)) * a.Hkv + kvh);
+          if (is_v && C::KB == 2) {  // the whole page in one box, page-major
+            tma_load_4d(buf + lane * (2 * kP * 128), &prm.tmap_vp, 0, 0, 0, slice, &ring_full[st]);
+          } else {
 #pragma unroll
-          for (int b = 0; b < C::KB; ++b)
-            tma_load_3d(buf + b * (KT * 128) + lane * (kP * 128), &prm.tmap_kv, b * 64, 0, slice,
-                        &ring_full[st]);
+            for (int b = 0; b < C::KB; ++b)
+              tma_load_3d(buf + b * (KT * 128) + lane * (kP * 128), &prm.tmap_kv, b * 64, 0, slice,
+                          &ring_full[st]);
+          }
         }
         pid = pid_next;
       }
@@ -761,7 +790,8 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
     auto issue_pv = [&](uint32_t pcol, int st, bool accumulate) {
 #pragma unroll
       for (int k = 0; k < KT / 16; ++k) {
-        const uint64_t db = desc_mnmajor(sR + st * C::T_BYTES + k * (16 * 128), KT * 128);
+        const uint64_t db = C::KB == 2 ? desc_mnmajor(sR + st * C::T_BYTES + k * (2 * 16 * 128), 16 * 128)
+                                       : desc_mnmajor(sR + st * C::T_BYTES + k * (16 * 128), KT * 128);
         if (elect_one())
           tc_mma_ts(tmem + C::O_COL, tmem + pcol + k * 8, db, idesc_o, (accumulate || k > 0) ? 1u : 0u);
       }
@@ -818,7 +848,9 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
           for (int x = lane; x < nz * C::KB; x += 32) {
             const int b = x / nz, rem = x - b * nz;
             const int r = keys + (rem >> 3), ch = rem & 7;
-            *reinterpret_cast<uint4*>(buf + b * (KT * 128) + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+            uint8_t* at = C::KB == 2 ? buf + (r >> 4) * (2 * kP * 128) + b * (kP * 128) + (r & 15) * 128
+                                     : buf + b * (KT * 128) + r * 128;
+            *reinterpret_cast<uint4*>(at + ch * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -965,6 +997,18 @@ cudaError_t launch_tc(const PrefillArgs& a, const PrefillTile* tiles, int n_tile
     cuuint32_t box[3] = {64, (cuuint32_t)kP, 1};
     cuuint32_t es[3] = {1, 1, 1};
     if (enc(&prm.tmap_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.pool, dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (D == 128) {
+    // one V page per box: [slices][half][P rows][64 columns] (the halves' stride
+    // is 128 bytes, the rows' 256), so a page lands as two 16-row panels
+    cuuint64_t dims[4] = {64, (cuuint64_t)kP, 2, (cuuint64_t)a.num_pages * 2 * a.Hkv};
+    cuuint64_t strides[3] = {(cuuint64_t)D * 2, 128, (cuuint64_t)kP * D * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)kP, 2, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(&prm.tmap_vp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void*)a.pool, dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
