@@ -966,7 +966,7 @@ def main():
                          "the prefix) instead of the shared-prefix calls")
     ap.add_argument("--no-fused-prefill-append", action="store_true",
                     help="fused calls: append every row with the append kernel instead of letting "
-                         "the CTA-pair prefill kernel write its chunk's own key tiles")
+                         "the prefill kernels write their chunks' own key tiles")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="time the headline workload only (no per_config map)")

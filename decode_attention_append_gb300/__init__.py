@@ -703,9 +703,9 @@ class HostStep:
 
 def set_prefill_append_fusion(enable: bool) -> None:
     """Fused calls (``append_attention``, ``BatchAttention.step``): whether the
-    CTA-pair prefill kernel reads long chunks' own key tiles from k_new / v_new
-    and writes them into their pages itself (True, the default) or the append
-    kernel writes every row (False).  Results are identical."""
+    prefill kernels read long chunks' own key tiles from k_new / v_new and write
+    them into their pages themselves (True, the default) or the append kernel
+    writes every row (False).  Results are identical."""
     _check(load_library().daa_set_prefill_append_fusion(int(bool(enable))),
            "set_prefill_append_fusion")
 
