@@ -18,7 +18,8 @@
 //   warp 8           TMA producer: Q tiles, then K_0, V_0, K_1, V_1, ... into a
 //                    ring of RS shared-memory stages (one 128-key tile each)
 //   warp 9           MMA issuer (one lane)
-//   warp 10          page writer of the fused append (below); idle otherwise
+//   warp 10          page writer of the fused append (below); otherwise a second
+//                    TMA producer (the odd ring items)
 // Tensor memory: S_q / P_q at q*KT, O_q at 2*KT + q*D (512 columns for pairs).
 //   S_q = Q_q K_j^T      A = Q (smem), B = K (smem), fp32 S in TMEM
 //   P_q (bf16) overwrites the first 64 columns of S_q (softmax, tcgen05.st)
@@ -247,8 +248,14 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
   const uint32_t tmem = *tmem_slot;
   if (tid == 0) grid_dep_launch();  // the next kernel may start its CTAs
 
-  if (warp == C::PRODUCER) {
+  // Two producers when the item has no page to write: the page writer's warp
+  // issues the odd ring items, the producer warp the even ones.  One warp's
+  // issue loop (a wait, an arrive and the page boxes per stage) paced the
+  // stream at about 32 GB/s per SM; two overlap their issue.
+  const int n_prod = C::WRITES && !writer_on ? 2 : 1;
+  if (warp == C::PRODUCER || (n_prod == 2 && warp == C::WRITER)) {
     // ------------------------------------------------------------ producer
+    const int pw = warp == C::PRODUCER ? 0 : 1;  // this warp issues ring items i = pw (mod n_prod)
     // Page ids of ring item i: lane l (< 8) holds the id of the item's l-th
     // page.  Fetched with one coalesced load per item, one item ahead, so its
     // latency overlaps the wait for a free stage; each lane then issues the
@@ -260,7 +267,7 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
       const int np = min(PPT, npages_req - pg0);
       return lane < np ? (int64_t)__ldg(a.page_indices + tile.page_base + pg0 + lane) : -1;
     };
-    if (lane == 0) {
+    if (lane == 0 && pw == 0) {
       const int tpt = one_token ? 1 : kRows / g;
       const void* tmap_q = one_token ? (const void*)&prm.tmap_q1 : (const void*)&prm.tmap_q;
       mbar_arrive_expect_tx(q_full, (uint32_t)(nq * tpt * g * D * 2));
@@ -269,15 +276,15 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
           tma_load_3d(smem + L::OFF_Q + q * L::Q_BYTES + b * (kRows * 128), tmap_q, b * 64,
                       kvh * g, tile.q_row0 + tile.tok0 + q * tile.ntok, q_full);
     }
-    int64_t pid = load_ids(0);
+    int64_t pid = load_ids(pw);
     // the request's last qo_len keys are the rows appended in this step: the
     // first ring item that reaches them waits for the kernel launched before
     // this one (tiles of cached keys stream while that kernel still runs).  A
     // prefix-group item reads only cached keys.
     const int first_new = prefix_group ? tile.kv_len : tile.kv_len - tile.qo_len;
     bool dep_waited = false;
-    for (int i = 0; i < 2 * n_kt; ++i) {
-      const int64_t pid_next = load_ids(i + 1);
+    for (int i = pw; i < 2 * n_kt; i += n_prod) {
+      const int64_t pid_next = load_ids(i + n_prod);
       const int st = i % RS;
       const bool is_v = ring_is_v(i, nq, n_kt);
       const int pg0 = (kt0 + ring_tile(i, nq, n_kt)) * PPT;
@@ -334,7 +341,7 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
     // request's last split waits.)
     if ((prefix_group || fuse) && !dep_waited) grid_dep_wait();
     __syncwarp();
-    if (last_partial) {
+    if (last_partial && (2 * n_kt - 1) % n_prod == pw) {  // the last ring item's producer
       // last V tile: rows past the request's last key must hold finite values
       const int i = 2 * n_kt - 1, st = i % RS;  // V of the last tile is the last ring item
       const int tile_keys = tile.kv_len - (kt0 + n_kt - 1) * KT;
