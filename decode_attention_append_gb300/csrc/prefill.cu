@@ -96,7 +96,10 @@ struct TcCfg {
   static constexpr int KB = D / 64;                 // 64-column (128-byte) blocks per row
   // prefill instantiations (Q-tile pairs) carry the fused append's page writer
   static constexpr bool WRITES = NQX == 2;
-  static constexpr int THREADS = 32 * (4 * NQX + 2 + (WRITES ? 1 : 0));
+  static constexpr int THREADS = 32 * (4 * NQX + 2 + (WRITES ? 1 : 0) + (NQX == 1 ? 1 : 0));
+  // the decode instantiation's second TMA producer warp (one warp's issue loop
+  // paced the page stream; two overlap their issue)
+  static constexpr int PRODUCER2 = 4 * NQX + 2;
   static constexpr int PRODUCER = 4 * NQX;          // warp ids
   static constexpr int MMA = 4 * NQX + 1;
   static constexpr int WRITER = 4 * NQX + 2;        // when WRITES
@@ -576,8 +579,9 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
 // current one.  Per CTA, ring stages, S buffers and the phases of s_full,
 // p_full and o_done follow running counts of ring items and key tiles over
 // all its items, exactly as within one item.  Hand-offs across items:
-//   item_full / item_empty [2]  item index from the producer to the MMA warp and
-//                               the four softmax warps (two slots)
+//   item_full / item_empty [2]  item index from the first producer to the MMA
+//                               warp, the four softmax warps and the second
+//                               producer (two slots)
 //   q_empty      the last S of an item is done: Q may be overwritten
 //   o_free       the epilogue of an item has read O: the next PV may overwrite
 // The MMA warp itself zeroes the stale rows of a request's last V tile once
@@ -647,7 +651,7 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
       mbar_init(&s_full[b], 1);
       mbar_init(&p_full[b], 4);
       mbar_init(&item_full[b], 1);
-      mbar_init(&item_empty[b], 5);  // the MMA warp and the four softmax warps
+      mbar_init(&item_empty[b], 6);  // the MMA warp, the four softmax warps, the second producer
     }
     mbar_init(o_done, 1);
     mbar_init(o_free, 4);
@@ -684,24 +688,42 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
     return q;
   };
 
-  if (warp == C::PRODUCER) {
+  if (warp == C::PRODUCER || warp == C::PRODUCER2) {
     // ------------------------------------------------------------ producer
+    // Two producer warps: the first takes each unit from the work counter,
+    // publishes it in the mailbox and loads Q; the second reads the unit from
+    // the mailbox like the consumers do.  Of each unit's ring items, the first
+    // issues the even ones and the second the odd ones (K and V of a key tile
+    // go to different warps), each with its own page-id pipeline.
+    const int pw = warp == C::PRODUCER ? 0 : 1;
     int64_t r0 = 0;       // ring items issued before the current item
     bool dep_waited = false;
     for (int k = 0;; ++k) {
       const int slot = k & 1;
       int unit = n_units;
-      if (lane == 0) {
-        const bool ok = k < 2 || mbar_wait(&item_empty[slot], ((k >> 1) - 1) & 1, a.err);
-        unit = ok ? atomicAdd(a.dec_counter, 1) : n_units;
-        item_slot[slot] = unit;
-        if (unit < n_units) item_tile[slot] = prm.tiles[unit / a.Hkv];
-        mbar_arrive(&item_full[slot]);  // release: the slot's writes precede it
+      if (pw == 0) {
+        if (lane == 0) {
+          const bool ok = k < 2 || mbar_wait(&item_empty[slot], ((k >> 1) - 1) & 1, a.err);
+          unit = ok ? atomicAdd(a.dec_counter, 1) : n_units;
+          item_slot[slot] = unit;
+          if (unit < n_units) item_tile[slot] = prm.tiles[unit / a.Hkv];
+          mbar_arrive(&item_full[slot]);  // release: the slot's writes precede it
+        }
+        unit = __shfl_sync(0xffffffffu, unit, 0);
+        if (unit >= n_units) break;
+        __syncwarp();
+      } else {
+        const bool ok = mbar_wait(&item_full[slot], (k >> 1) & 1, a.err);
+        unit = ok ? item_slot[slot] : n_units;
+        __syncwarp();
+        if (unit >= n_units) {
+          if (lane == 0) mbar_arrive(&item_empty[slot]);
+          break;
+        }
       }
-      unit = __shfl_sync(0xffffffffu, unit, 0);
-      if (unit >= n_units) break;
-      __syncwarp();
       const PrefillTile tile = item_tile[slot];
+      __syncwarp();
+      if (pw == 1 && lane == 0) mbar_arrive(&item_empty[slot]);  // descriptor read
       const int kvh = unit % a.Hkv;
       const Geo ge = geometry(tile);
       const int n_kt = ge.n_kt;
@@ -711,8 +733,8 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
         const int np = min(PPT, ge.npages_req - pg0);
         return lane < np ? (int64_t)__ldg(a.page_indices + tile.page_base + pg0 + lane) : -1;
       };
-      int64_t pid = load_ids(0);
-      if (lane == 0) {
+      int64_t pid = load_ids(pw);
+      if (lane == 0 && pw == 0) {
         // Q, once the previous item's last S has read it
         if (k > 0) mbar_wait(q_empty, (k - 1) & 1, a.err);
         const int tpt = ge.one_token ? 1 : kRows / g;
@@ -723,8 +745,8 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
                       tile.q_row0 + tile.tok0, q_full);
       }
       const int first_new = tile.kv_len - tile.qo_len;
-      for (int i = 0; i < 2 * n_kt; ++i) {
-        const int64_t pid_next = load_ids(i + 1);
+      for (int i = pw; i < 2 * n_kt; i += 2) {
+        const int64_t pid_next = load_ids(i + 2);
         const int64_t rg = r0 + i;
         const int st = (int)(rg % RS);
         const uint32_t ph = (uint32_t)((rg / RS) & 1);
@@ -764,7 +786,7 @@ __device__ __forceinline__ void tc_decode_persistent(const PrefillParams& prm) {
     // the last CTA to finish resets the work counter (dec_counter[0]) and the
     // finish count (dec_counter[1]) for the next launch on this plan: every
     // CTA has taken its last ticket before it counts itself finished
-    if (lane == 0 && atomicAdd(a.dec_counter + 1, 1) == (int)(gridDim.x * gridDim.y) - 1) {
+    if (pw == 0 && lane == 0 && atomicAdd(a.dec_counter + 1, 1) == (int)(gridDim.x * gridDim.y) - 1) {
       atomicExch(a.dec_counter, 0);
       atomicExch(a.dec_counter + 1, 0);
     }
