@@ -483,10 +483,11 @@ daa_status daa_append_attention_run(const void* k_new, const void* v_new, const 
  * anything is enqueued.
  *
  * Set-up: the first call on each device (with that device current) looks up
- * the array's device address with cudaGetSymbolAddress and caches it.  The cached address
- * belongs to the device context it was looked up in: after cudaDeviceReset
- * (or anything else that destroys the primary context) it is stale, so do not
- * call this entry point again in a process that has reset the device.
+ * the array's device address with cudaGetSymbolAddress and caches it.  The
+ * cached address belongs to the device context it was looked up in: after
+ * cudaDeviceReset (or anything else that destroys the primary context) it is
+ * stale, so do not call this entry point again in a process that has reset the
+ * device.
  *
  * Sharing: every call, on every stream and host thread, uses the same array,
  * which keeps the last call's contents.  Nothing in it has to start at zero --
