@@ -85,10 +85,11 @@ struct __align__(64) PrefillParams {
 
 // One instantiation of the kernel: head dim D, KT keys per K/V tile, at most
 // NQX Q tiles per CTA, MIN_BLOCKS CTAs meant to share an SM.
-//   <D, 128, 2, 1>  prefill pairs: 224 KB of shared memory, 512 TMEM columns
+//   <D, 128, 2, 1>  prefill pairs (and, for head_dim 128, short items): 224 KB
+//                   of shared memory, 512 TMEM columns
 //   <D,  64, 1, 2>  decode splits: ~100 KB, 256 TMEM columns, two CTAs per SM
-//                   (two independent TMA producers per SM stream K/V faster
-//                   than one)
+//                   with two producer warps each (more independent TMA issue
+//                   loops per SM stream K/V faster)
 template <int D_, int KT_, int NQX_, int MINB_>
 struct TcCfg {
   static constexpr int D = D_, KT = KT_, NQX = NQX_, MIN_BLOCKS = MINB_;
@@ -574,7 +575,7 @@ __device__ __forceinline__ void tc_attention(const PrefillParams& prm) {
 // of two CTAs per SM, each CTA taking item after item from a work counter in
 // the plan's order (most keys first), so the last wave is never partly empty
 // and each CTA pays its set-up (barriers, TMEM, tensor-map prefetch) once.
-// Across items the pipeline does not drain: the producer streams the next
+// Across items the pipeline does not drain: the producers stream the next
 // item's K/V tiles while the MMA issuer and the softmax warps finish the
 // current one.  Per CTA, ring stages, S buffers and the phases of s_full,
 // p_full and o_done follow running counts of ring items and key tiles over
